@@ -1,0 +1,357 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA hot path on GB300: prefill tokens/s and decode steps/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kda|reference]
+
+One JSON line on stdout (rank 0).  The headline ``value`` is chunked-prefill
+throughput on one 8192-token sequence with 32 heads of d = 128 (bf16 q/k/v,
+fp32 state), inputs resident in HBM.  The same line carries the single-token
+decode step (256 sequences x 32 heads, fp32 state updated in place, a fresh
+token set every step) under ``decode``, the end-to-end number through the C
+ABI from pinned host buffers under ``e2e``, the roofline of the dominant
+kernel, the clocks seen during the timed region and the fp64 CPU oracle timed
+on this host's cores.  Every (sequence, head) chain is independent, so N > 1
+runs N replicas (one per GPU) with no collective ("replicas only").
+
+``--impl reference`` times the fp64 CPU oracle (the reference arm of this
+build) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PREFILL = "prefill_bf16_T8192_H32_D128"
+DECODE = "decode_bf16_N256_H32_D128"
+METRIC = "KDA prefill tokens/s and decode steps/s (H=32,d=128) on 1 GB300; % roofline"
+# compulsory bytes per token-head: bf16 q, k, v, O + fp32 log_alpha + fp32 beta
+BYTES_TOKEN_HEAD = 3 * 256 + 512 + 4 + 256
+# contraction flops per token-head (8 C D + 6 D^2 with C = 64, D = 128), without the inverse
+FLOPS_TOKEN_HEAD = 8 * 64 * 128 + 6 * 128 * 128
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier_max(t, world, device):
+    if world == 1:
+        return t
+    import torch.distributed as dist
+    x = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(x, op=dist.ReduceOp.MAX)
+    return float(x.item())
+
+
+def sync_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- oracle baseline
+def oracle_sample(n_tokens, seed=0):
+    """Time the fp64 oracle on the first n_tokens of the prefill workload, all 32 heads."""
+    import oracle
+    from kimi_delta_attention_chunked_gb300 import inputs
+    w = inputs.WORKLOADS[PREFILL]
+    d = inputs.make_prefill(w, device="cpu", seed=seed, lengths=[n_tokens])
+    args = [d[x].contiguous() for x in ("q", "k", "v", "log_alpha", "beta")]
+    oracle.build()
+    oracle.prefill(*[a[:8] for a in args])                      # load + warm
+    t0 = time.perf_counter()
+    oracle.prefill(*args)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt, oracle.max_threads()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    n_tok = 1024
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample(n_tok)
+    t_all = 0.0
+    cores = 1
+    for _ in range(args.steps):
+        v, dt, cores = oracle_sample(n_tok)
+        vals.append(v)
+        t_all += dt
+    value = args.steps * n_tok / t_all
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_all / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL, "T": 8192, "H": 32, "dk": 128, "dv": 128, "chunk": 64,
+                   "sample": f"first {n_tok} tokens x 32 heads per step"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {n_tok} of 8192 tokens, all 32 heads, per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def time_prefill(kda, d, steps, warmup, stream, dev):
+    q, k, v, g, b = d["q"], d["k"], d["v"], d["log_alpha"], d["beta"]
+    T, H, dk = q.shape
+    ws = torch.empty(kda.kda_prefill_workspace_size(1, T, H, dk, v.shape[-1], 64, q.dtype), dtype=torch.uint8,
+                     device=dev)
+    O = torch.empty_like(v)
+    Sf = torch.empty((1, H, dk, v.shape[-1]), dtype=torch.float32, device=dev)
+    call = lambda: kda.kda_prefill(q, k, v, g, b, O=O, S_final=Sf, workspace=ws, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        # per-kernel events: [before prep, after prep, after chain] for every step
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for row in evs:
+            for e in row:
+                e.record(stream)
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(steps):
+            kda.kda_set_trace_events(evs[i])
+            call()
+        kda.kda_set_trace_events(None)
+        end.record(stream)
+        torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    prep_ms = [r[0].elapsed_time(r[1]) for r in evs]
+    chain_ms = [r[1].elapsed_time(r[2]) for r in evs]
+    return total_ms, statistics.mean(prep_ms), statistics.mean(chain_ms), 2 * steps
+
+
+def time_decode(kda, w, inputs, steps, warmup, stream, dev, seed=0):
+    n_sets = steps + warmup
+    d = inputs.make_decode(w, device=dev, seed=seed, n_token_sets=n_sets)
+    S = d["S"]
+    o = torch.empty((w.B, w.H, w.dv), dtype=w.dtype, device=dev)
+    with torch.cuda.stream(stream):
+        for t in range(warmup):
+            kda.kda_decode(d["q"][t], d["k"][t], d["v"][t], d["log_alpha"][t], d["beta"][t], S, o=o, stream=stream)
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for t in range(warmup, n_sets):
+            kda.kda_decode(d["q"][t], d["k"][t], d["v"][t], d["log_alpha"][t], d["beta"][t], S, o=o, stream=stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    return start.elapsed_time(end), steps
+
+
+def time_e2e(kda, d, steps, stream, dev):
+    """Through the C ABI from pinned host buffers: H2D inputs, prefill, D2H O and S_final."""
+    names = ("q", "k", "v", "log_alpha", "beta")
+    host = {n: d[n].cpu().pin_memory() for n in names}
+    devb = {n: torch.empty_like(d[n]) for n in names}
+    T, H, dk = d["q"].shape
+    dv = d["v"].shape[-1]
+    ws = torch.empty(kda.kda_prefill_workspace_size(1, T, H, dk, dv, 64, d["q"].dtype), dtype=torch.uint8,
+                     device=dev)
+    O = torch.empty_like(d["v"])
+    Sf = torch.empty((1, H, dk, dv), dtype=torch.float32, device=dev)
+    O_h = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    Sf_h = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = O.numel() * O.element_size() + Sf.numel() * Sf.element_size()
+
+    def step():
+        for n in names:
+            devb[n].copy_(host[n], non_blocking=True)
+        kda.kda_prefill(devb["q"], devb["k"], devb["v"], devb["log_alpha"], devb["beta"], O=O, S_final=Sf,
+                        workspace=ws, stream=stream)
+        O_h.copy_(O, non_blocking=True)
+        Sf_h.copy_(Sf, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    return start.elapsed_time(end), h2d, d2h
+
+
+def run_gpu(args):
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import kimi_delta_attention_chunked_gb300 as kda
+    from kimi_delta_attention_chunked_gb300 import build, inputs
+    build.build()
+    kda.load()
+    hbm, bf16_tf, peak_src = peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    wp = inputs.WORKLOADS[PREFILL]
+    d = inputs.make_prefill(wp, device=dev, seed=rank)
+    d["S0"] = None
+    T, H = d["T"], wp.H
+    in_bytes = sum(d[n].numel() * d[n].element_size() for n in ("q", "k", "v", "log_alpha", "beta"))
+
+    sync_barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms, prep_ms, chain_ms, launches = time_prefill(kda, d, args.steps, args.warmup, stream, dev)
+        sync_barrier(world)
+        wd = inputs.WORKLOADS[DECODE]
+        dec_steps = max(args.steps, args.decode_steps)
+        dms, dsteps = time_decode(kda, wd, inputs, dec_steps, args.warmup, stream, dev, seed=rank)
+    ms = barrier_max(ms, world, dev)
+    dms = barrier_max(dms, world, dev)
+    e2e_ms, h2d, d2h = time_e2e(kda, d, max(3, args.steps // 4), stream, dev)
+    e2e_ms = barrier_max(e2e_ms, world, dev)
+    e2e_steps = max(3, args.steps // 4)
+
+    tok_per_step = T * world
+    value = tok_per_step * args.steps / (ms / 1e3)
+    ms_step = ms / args.steps
+    # roofline of the dominant prefill kernel (compulsory bytes that kernel moves)
+    prep_bytes = T * H * (3 * 256 + 512 + 4)               # q, k, v, log_alpha, beta read once
+    chain_bytes = T * H * 256 + H * 128 * 128 * 4          # O written once + final state
+    dom = ("kda_tc_prep", prep_ms, prep_bytes) if prep_ms >= chain_ms else ("kda_tc_chain", chain_ms, chain_bytes)
+    achieved = dom[2] / (dom[1] / 1e3) / 1e9
+    step_bytes = T * H * BYTES_TOKEN_HEAD + H * 128 * 128 * 4
+    dec_bytes_step = wd.B * wd.H * (8 * wd.dk * wd.dv + 3 * 256 + 512 + 4 + 256)
+    dec_ms_step = dms / dsteps
+    dec_achieved = dec_bytes_step / (dec_ms_step / 1e3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": PREFILL, "B": 1, "T": T, "H": H, "dk": 128, "dv": 128, "chunk": 64,
+                   "state": "fp32, S0 = 0", "parallelism": "replicas" if world > 1 else "single",
+                   "l2": f"inputs {in_bytes / 1e6:.0f} MB per step > 129 MB L2 (no flush)"},
+        "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None, "peak_source": peak_src,
+                     "bytes_per_launch": dom[2], "launch_ms": dom[1]},
+        "step_roofline": {"bound": "hbm", "bytes_per_step": step_bytes,
+                          "achieved": step_bytes / (ms_step / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                          "frac": step_bytes / (ms_step / 1e3) / 1e9 / hbm,
+                          "tflops": T * H * FLOPS_TOKEN_HEAD / (ms_step / 1e3) / 1e12,
+                          "kernel_ms": {"kda_tc_prep": prep_ms, "kda_tc_chain": chain_ms}},
+        "decode": {"workload": DECODE, "value": dsteps * world / (dms / 1e3), "unit": "steps/s",
+                   "steps": dsteps, "ms_per_step": dec_ms_step,
+                   "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": dec_achieved,
+                                "peak": hbm, "unit": "GB/s", "frac": dec_achieved / hbm, "traffic": None,
+                                "bytes_per_launch": dec_bytes_step},
+                   "l2": "fp32 state 537 MB > L2; fresh token set per step"},
+        "e2e": {"value": tok_per_step * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches * world,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, dt, cores = oracle_sample(args.oracle_tokens)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"first {args.oracle_tokens} of 8192 tokens x 32 heads ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--oracle-tokens", type=int, default=2048)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "kda":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

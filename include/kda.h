@@ -1,0 +1,165 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention library.
+ *
+ * The operator.  Per head, KDA keeps a state S in R^{d_k x d_v} and, for every
+ * token t, applies
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = S_t^T q_t,
+ *
+ * with alpha_t in (0,1)^{d_k} a forget gate per key channel and beta_t a
+ * scalar write strength ("Kimi K3" blog, section "Kimi Delta Attention"; the
+ * same update in words on the "LLM architecture at trillion scale" page,
+ * section "The KDA update, in plain words").  The gate is passed as
+ * log_alpha = ln(alpha_t), expected in [-5, 0): the log-decay bound stated on
+ * that page.  Values outside it are computed but not guaranteed to meet the
+ * accuracy target.
+ *
+ * Two entry points compute it:
+ *   kda_prefill -- many tokens at once in the chunked form ("Kimi K3: the
+ *                  manos, the mythos, the legendos", section "FlashKDA
+ *                  Algorithm"), returning every o_t and the final state;
+ *   kda_decode  -- one token per sequence, updating an fp32 state in place
+ *                  (the per-token form of the same section).
+ *
+ * Conventions for every call
+ *   - All tensor arguments are caller-owned, contiguous, row-major DEVICE
+ *     pointers (cu_seqlens_host is the one host pointer).  The library never
+ *     allocates device memory and never synchronises the stream, except in
+ *     kda_get_last_device_status.
+ *   - Work is enqueued on `stream` (0 = the legacy default stream).  A call
+ *     returns once the work is enqueued.
+ *   - Arguments are checked before anything is launched; a failed check
+ *     returns an error and launches nothing.  A launch failure returns
+ *     KDA_ERR_CUDA.  Faults detected inside a kernel (a wait that ran out of
+ *     time) are recorded in a device status word read by
+ *     kda_get_last_device_status.
+ *   - Supported shapes: d_k, d_v in {32, 64, 128}; chunk in {16, 32, 64}.
+ *     KDA_BF16 with d_k = d_v = 128 and chunk = 64 runs on the tcgen05
+ *     tensor-core path; every other combination runs on the fp32 CUDA-core
+ *     chunked path.  Both are GPU kernels; there is no CPU path.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad cu_seqlens, ... */
+    KDA_ERR_UNSUPPORTED = 2,  /* shape / dtype / chunk combination not built     */
+    KDA_ERR_WORKSPACE = 3,    /* workspace missing, too small or misaligned      */
+    KDA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed             */
+    KDA_ERR_TIMEOUT = 5       /* a kernel gave up waiting (device status only)    */
+} kda_status;
+
+typedef enum kda_dtype {
+    KDA_FP32 = 0,             /* q, k, v and O are float                          */
+    KDA_BF16 = 1              /* q, k, v and O are bfloat16 (raw 16-bit storage)  */
+} kda_dtype;
+
+/*
+ * Bytes of device workspace kda_prefill needs for this problem.  0 means none
+ * (the CUDA-core path).  The figure depends only on the arguments, and it
+ * assumes the worst case of one partial chunk per sequence, so it is valid for
+ * any cu_seqlens with these n_seq and T_total.
+ */
+KDA_API size_t kda_prefill_workspace_size(int n_seq, int T_total, int H, int dk, int dv,
+                                  int chunk, kda_dtype dtype);
+
+/*
+ * Chunked prefill over a packed batch of variable-length sequences.
+ *
+ * Computes, for each sequence n and head h independently, the recurrence above
+ * over the sequence's tokens, starting from S0[n,h], and returns o_t for every
+ * token and the final state.  The chunked matrix form it evaluates is the one
+ * of "Kimi K3: the manos, the mythos, the legendos", section "FlashKDA
+ * Algorithm" (cumulative decay, Q_decay / K_decay / K_restore, the UT
+ * transform U = (I + L)^{-1} Diag(beta)(V - K_decay S_in),
+ * O = Q_decay S_in + M_qk U, S_out = Diag(a_last) S_in + K_restore^T U).
+ *
+ * q, k       [T_total, H, dk]  dtype
+ * v          [T_total, H, dv]  dtype
+ * log_alpha  [T_total, H, dk]  float, natural log of the gate
+ * beta       [T_total, H]      float
+ * S0         [n_seq, H, dk, dv] float, or NULL for zero initial states
+ * cu_seqlens [n_seq + 1] int32 device array of token offsets (0 = cu[0] <=
+ *            cu[1] <= ... <= cu[n_seq] = T_total), or NULL for n_seq
+ *            sequences of equal length T_total / n_seq (which must divide).
+ * cu_seqlens_host  optional host copy of cu_seqlens (same values).  When
+ *            given it is validated and used to size the launch exactly; when
+ *            NULL a device cu_seqlens is trusted (lengths are clamped on the
+ *            device so that no access leaves the arrays).
+ * O          [T_total, H, dv]  dtype, written for every token; must not alias
+ *            an input.
+ * S_final    [n_seq, H, dk, dv] float, or NULL.  May alias S0 exactly.
+ * workspace  device memory of at least kda_prefill_workspace_size(...) bytes,
+ *            256-byte aligned (may be NULL when that size is 0).  Its contents
+ *            on entry do not matter; the call owns it until the work completes.
+ * Sequences of length 0 are allowed (their S_final is S0).
+ */
+KDA_API kda_status kda_prefill(const void* q, const void* k, const void* v,
+                       const float* log_alpha, const float* beta, const float* S0,
+                       const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                       int n_seq, int T_total, int H, int dk, int dv, int chunk,
+                       kda_dtype dtype, void* O, float* S_final,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * One decode step for N independent sequences (one token each), the per-token
+ * form u = beta (v - (D S)^T k), S <- D S + k u^T, o = S^T q of "Kimi K3: the
+ * manos, the mythos, the legendos", section "FlashKDA Algorithm".
+ *
+ * q, k       [N, H, dk] dtype;  v [N, H, dv] dtype
+ * log_alpha  [N, H, dk] float;  beta [N, H] float
+ * S          [N, H, dk, dv] float, read and overwritten in place
+ * o          [N, H, dv] dtype, written; must not alias an input.
+ */
+KDA_API kda_status kda_decode(const void* q, const void* k, const void* v,
+                      const float* log_alpha, const float* beta, float* S,
+                      int N, int H, int dk, int dv, kda_dtype dtype, void* o,
+                      cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word:
+ * KDA_OK, or KDA_ERR_TIMEOUT if a kernel since the last call gave up waiting
+ * (its outputs are then incomplete), or KDA_ERR_CUDA if the synchronisation
+ * itself failed.  The word is per device and shared by all streams.
+ */
+KDA_API kda_status kda_get_last_device_status(cudaStream_t stream);
+
+/*
+ * Tracing hook.  While set, every kda_prefill / kda_decode call made from the
+ * calling host thread records the given CUDA events (cudaEvent_t handles,
+ * created by the caller) on its stream at the boundaries between the kernels
+ * it launches: event 0 before the first kernel, event i after the i-th kernel
+ * (the tensor-core prefill launches [table builder,] chunk prep, state pass;
+ * the CUDA-core prefill and the decode launch one kernel).  Events beyond
+ * n_events are skipped.  Pass (NULL, 0) to stop.  Returns KDA_ERR_INVALID_ARG
+ * for n_events < 0 or a NULL array with n_events > 0.  The array must stay
+ * valid while the hook is set.  This exists so that a benchmark can time each
+ * kernel with CUDA events on the stream the kernel runs on.
+ */
+KDA_API kda_status kda_set_trace_events(void* const* events, int n_events);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+KDA_API const char* kda_status_string(kda_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

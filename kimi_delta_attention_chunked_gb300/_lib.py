@@ -1,0 +1,177 @@
+"""ctypes binding of ``libkda.so`` -- argument marshalling only.
+
+Every function here has the name of the C entry point it calls (see
+``include/kda.h``).  Tensors are passed as raw device pointers; PyTorch is used
+only to allocate outputs and workspaces and to name the current stream.  There
+is no fallback: if the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(6)
+KDA_FP32, KDA_BF16 = 0, 1
+SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_decode", "kda_get_last_device_status",
+           "kda_set_trace_events", "kda_status_string")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {kda_status_string(status)}")
+
+
+def load():
+    """Load libkda.so (built by ``build.build()``); raises if it is not there."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"KDA CUDA library not built: {LIB_PATH} is missing "
+                              "(run python -m kimi_delta_attention_chunked_gb300.build)")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.kda_prefill_workspace_size.argtypes = [I, I, I, I, I, I, I]
+        lib.kda_prefill_workspace_size.restype = Z
+        lib.kda_prefill.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, Z, P]
+        lib.kda_prefill.restype = I
+        lib.kda_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P]
+        lib.kda_decode.restype = I
+        lib.kda_get_last_device_status.argtypes = [P]
+        lib.kda_get_last_device_status.restype = I
+        lib.kda_set_trace_events.argtypes = [P, I]
+        lib.kda_set_trace_events.restype = I
+        lib.kda_status_string.argtypes = [I]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def kda_status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return KDA_BF16
+    if t == torch.float32:
+        return KDA_FP32
+    raise TypeError(f"KDA supports bfloat16 and float32 q/k/v, not {t}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check_dev(name, t, device, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def kda_prefill_workspace_size(n_seq: int, T_total: int, H: int, dk: int, dv: int, chunk: int,
+                               dtype: torch.dtype) -> int:
+    return int(load().kda_prefill_workspace_size(n_seq, T_total, H, dk, dv, chunk, _dtype_code(dtype)))
+
+
+def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, cu_seqlens_host=None, chunk=64,
+                O=None, S_final=None, workspace=None, stream=None, want_state=True):
+    """Chunked prefill; returns (O, S_final).  Shapes as in ``include/kda.h``:
+    q, k, log_alpha [T, H, dk]; v [T, H, dv]; beta [T, H]; S0 [n_seq, H, dk, dv] fp32 or
+    None; cu_seqlens int32 [n_seq+1] on the device or None (one sequence)."""
+    lib = load()
+    dev = q.device
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_dev(name, t, dev, q.dtype)
+    _check_dev("log_alpha", log_alpha, dev, torch.float32)
+    _check_dev("beta", beta, dev, torch.float32)
+    _check_dev("cu_seqlens", cu_seqlens, dev, torch.int32)
+    n_seq = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if S0 is not None:
+        _check_dev("S0", S0, dev, torch.float32)
+    if O is None:
+        O = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    if S_final is None and want_state:
+        S_final = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev)
+    host = None
+    if cu_seqlens_host is not None:
+        host = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+    dt = _dtype_code(q.dtype)
+    need = int(lib.kda_prefill_workspace_size(n_seq, T, H, dk, dv, chunk, dt))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
+                         host, n_seq, T, H, dk, dv, chunk, dt, _ptr(O), _ptr(S_final), _ptr(workspace),
+                         ws_bytes, _stream(stream, dev))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_prefill")
+    return O, S_final
+
+
+def kda_decode(q, k, v, log_alpha, beta, S, o=None, stream=None):
+    """One decode step; S [N, H, dk, dv] fp32 is updated in place; returns o [N, H, dv]."""
+    lib = load()
+    dev = q.device
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_dev(name, t, dev, q.dtype)
+    _check_dev("log_alpha", log_alpha, dev, torch.float32)
+    _check_dev("beta", beta, dev, torch.float32)
+    _check_dev("S", S, dev, torch.float32)
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
+    st = lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S), N, H, dk, dv,
+                        _dtype_code(q.dtype), _ptr(o), _stream(stream, dev))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode")
+    return o
+
+
+_trace_keep = None
+
+
+def kda_set_trace_events(events):
+    """Record these torch.cuda.Event objects at the kernel boundaries of the
+    following calls on this thread (None or [] stops)."""
+    global _trace_keep
+    lib = load()
+    if not events:
+        _trace_keep = None
+        st = lib.kda_set_trace_events(None, 0)
+    else:
+        arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        _trace_keep = (arr, list(events))
+        st = lib.kda_set_trace_events(arr, len(events))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_set_trace_events")
+
+
+def kda_get_last_device_status(stream=None, device=None) -> int:
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    return int(load().kda_get_last_device_status(_stream(stream, dev)))

@@ -1,0 +1,96 @@
+// common.cuh -- small device helpers shared by the KDA kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Device-side status codes (written into the status word by a kernel).
+enum : int { kDevOk = 0, kDevTimeout = 5 };
+
+// Upper bound on how long a kernel waits for an asynchronous event (an
+// mbarrier phase) before it records KDA_ERR_TIMEOUT and gives up: ~2 s at the
+// GB300 boost clock.  A correct launch never gets close.
+constexpr long long kWaitCycles = 4000000000LL;
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+    if (status) atomicCAS(status, kDevOk, code);
+}
+
+template <typename T> struct io;
+template <> struct io<float> {
+    static __device__ __forceinline__ float ld(const float* p) { return *p; }
+    static __device__ __forceinline__ void st(float* p, float x) { *p = x; }
+};
+template <> struct io<__nv_bfloat16> {
+    static __device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+    static __device__ __forceinline__ void st(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
+    return __bfloat1622float2(v);
+}
+
+}  // namespace kda
+
+// Host-side launchers implemented by the kernel translation units.
+namespace kda_host {
+
+struct PrefillArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;
+    const float* beta;
+    const float* S0;
+    const int32_t* cu_seqlens;   // device, or nullptr (equal lengths)
+    int n_seq, T_total, H, dk, dv, chunk;
+    int total_chunks;            // exact when the host knows cu_seqlens, else an upper bound
+    kda_dtype dtype;
+    void* O;
+    float* S_final;
+    void* workspace;
+    size_t workspace_bytes;
+    cudaStream_t stream;
+    int* status;                 // device status word
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;
+    const float* beta;
+    float* S;
+    int N, H, dk, dv;
+    kda_dtype dtype;
+    void* o;
+    cudaStream_t stream;
+};
+
+// Records the next trace event (see kda_set_trace_events) on `stream`.
+void trace_mark(cudaStream_t stream);
+void trace_reset();
+
+cudaError_t launch_decode(const DecodeArgs& a);
+cudaError_t launch_prefill_simt_fp32_c16(const PrefillArgs& a);
+cudaError_t launch_prefill_simt_fp32_c32(const PrefillArgs& a);
+cudaError_t launch_prefill_simt_fp32_c64(const PrefillArgs& a);
+cudaError_t launch_prefill_simt_bf16_c16(const PrefillArgs& a);
+cudaError_t launch_prefill_simt_bf16_c32(const PrefillArgs& a);
+cudaError_t launch_prefill_simt_bf16_c64(const PrefillArgs& a);
+bool tc_supported(int dk, int dv, int chunk, kda_dtype dt);
+size_t tc_workspace_bytes(int n_seq, int T_total, int H, int chunk);
+cudaError_t launch_prefill_tc(const PrefillArgs& a);
+
+}  // namespace kda_host

@@ -1,0 +1,158 @@
+// decode.cu -- fused single-token KDA decode step, fp32 state updated in place.
+//
+// Per (sequence, head) the step is the per-token form of "Kimi K3: the manos,
+// the mythos, the legendos", section "FlashKDA Algorithm":
+//     Sbar = Diag(alpha) S            (alpha = exp(log_alpha), one per key row)
+//     x    = Sbar^T k,   y = Sbar^T q (reductions over the d_k rows)
+//     u    = beta (v - x)
+//     S    = Sbar + k u^T             (written back in place)
+//     o    = S^T q = y + (k^T q) u
+// The pages count ~7 d^2 flops and ~8 d^2 bytes (fp32 state read + write) per
+// head-step (section "Complexity Analysis"), so the step is HBM-bound: the
+// kernel streams each 64 KiB state exactly once, with 16-byte loads and
+// stores marked evict-first, and keeps the whole state tile in registers
+// between the read and the write.
+//
+// Layout: one CTA of 256 threads per (sequence, head).  A row of S (d_v
+// floats) is covered by d_v/4 consecutive threads holding one float4 each;
+// the CTA covers 256/(d_v/4) rows per pass and d_k/(rows per pass) passes.
+// All state loads are issued before anything else so that ~64 KiB per CTA is
+// in flight.
+#include "common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int DK, int DV, typename TIn>
+__global__ void __launch_bounds__(kThreads, 2)
+kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
+                  const TIn* __restrict__ v, const float* __restrict__ log_alpha,
+                  const float* __restrict__ beta, float* __restrict__ S,
+                  TIn* __restrict__ o) {
+    constexpr int LPR = DV / 4;                       // threads per state row
+    constexpr int RPP = kThreads / LPR;               // rows per pass
+    constexpr int NPASS = (DK + RPP - 1) / RPP;
+    static_assert(DV % 4 == 0 && kThreads % LPR == 0, "bad tile");
+
+    __shared__ float s_k[DK], s_q[DK], s_a[DK];
+    __shared__ float4 s_x[RPP][LPR];
+    __shared__ float4 s_y[RPP][LPR];
+
+    const size_t unit = blockIdx.x;                   // n * H + h
+    const int tid = threadIdx.x;
+    const int c4 = tid % LPR;                         // float4 column group
+    const int r0 = tid / LPR;                         // first row of this thread
+    float* Su = S + unit * (size_t)DK * DV;
+
+    // 1. issue every state load first
+    float4 s[NPASS];
+#pragma unroll
+    for (int p = 0; p < NPASS; ++p) {
+        const int i = r0 + p * RPP;
+        if (i < DK) s[p] = __ldcs(reinterpret_cast<const float4*>(Su + (size_t)i * DV) + c4);
+    }
+    // 2. the token's key, query and gate
+    for (int i = tid; i < DK; i += kThreads) {
+        s_k[i] = kda::io<TIn>::ld(k + unit * DK + i);
+        s_q[i] = kda::io<TIn>::ld(q + unit * DK + i);
+        s_a[i] = __expf(log_alpha[unit * DK + i]);
+    }
+    float4 vv;
+    vv.x = kda::io<TIn>::ld(v + unit * DV + 4 * c4 + 0);
+    vv.y = kda::io<TIn>::ld(v + unit * DV + 4 * c4 + 1);
+    vv.z = kda::io<TIn>::ld(v + unit * DV + 4 * c4 + 2);
+    vv.w = kda::io<TIn>::ld(v + unit * DV + 4 * c4 + 3);
+    const float bt = beta[unit];
+    __syncthreads();
+
+    // 3. decay the rows and form the partial reductions x = Sbar^T k, y = Sbar^T q
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+#pragma unroll
+    for (int p = 0; p < NPASS; ++p) {
+        const int i = r0 + p * RPP;
+        if (i < DK) {
+            const float a = s_a[i], ki = s_k[i], qi = s_q[i];
+            s[p].x *= a; s[p].y *= a; s[p].z *= a; s[p].w *= a;
+            x.x = fmaf(s[p].x, ki, x.x); x.y = fmaf(s[p].y, ki, x.y);
+            x.z = fmaf(s[p].z, ki, x.z); x.w = fmaf(s[p].w, ki, x.w);
+            y.x = fmaf(s[p].x, qi, y.x); y.y = fmaf(s[p].y, qi, y.y);
+            y.z = fmaf(s[p].z, qi, y.z); y.w = fmaf(s[p].w, qi, y.w);
+        }
+    }
+    s_x[r0][c4] = x;
+    s_y[r0][c4] = y;
+    __syncthreads();
+
+    // 4. finish the reductions for this thread's 4 columns; u = beta (v - x)
+    float4 X = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int r = 0; r < RPP; ++r) {
+        const float4 t = s_x[r][c4];
+        X.x += t.x; X.y += t.y; X.z += t.z; X.w += t.w;
+    }
+    float4 u;
+    u.x = bt * (vv.x - X.x); u.y = bt * (vv.y - X.y);
+    u.z = bt * (vv.z - X.z); u.w = bt * (vv.w - X.w);
+
+    // 5. write the new state S = Sbar + k u^T
+#pragma unroll
+    for (int p = 0; p < NPASS; ++p) {
+        const int i = r0 + p * RPP;
+        if (i < DK) {
+            const float ki = s_k[i];
+            float4 w;
+            w.x = fmaf(ki, u.x, s[p].x); w.y = fmaf(ki, u.y, s[p].y);
+            w.z = fmaf(ki, u.z, s[p].z); w.w = fmaf(ki, u.w, s[p].w);
+            __stcs(reinterpret_cast<float4*>(Su + (size_t)i * DV) + c4, w);
+        }
+    }
+
+    // 6. read-out o = Sbar^T q + (k^T q) u  (one row of threads writes it)
+    if (r0 == 0) {
+        float4 Y = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < RPP; ++r) {
+            const float4 t = s_y[r][c4];
+            Y.x += t.x; Y.y += t.y; Y.z += t.z; Y.w += t.w;
+        }
+        float kq = 0.f;
+        for (int i = 0; i < DK; ++i) kq = fmaf(s_k[i], s_q[i], kq);
+        TIn* ou = o + unit * DV + 4 * c4;
+        kda::io<TIn>::st(ou + 0, fmaf(kq, u.x, Y.x));
+        kda::io<TIn>::st(ou + 1, fmaf(kq, u.y, Y.y));
+        kda::io<TIn>::st(ou + 2, fmaf(kq, u.z, Y.z));
+        kda::io<TIn>::st(ou + 3, fmaf(kq, u.w, Y.w));
+    }
+}
+
+template <int DK, int DV, typename TIn>
+cudaError_t launch(const kda_host::DecodeArgs& a) {
+    const unsigned units = (unsigned)((size_t)a.N * a.H);
+    if (units == 0) return cudaSuccess;
+    kda_decode_kernel<DK, DV, TIn><<<units, kThreads, 0, a.stream>>>(
+        static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v),
+        a.log_alpha, a.beta, a.S, static_cast<TIn*>(a.o));
+    return cudaGetLastError();
+}
+
+template <typename TIn>
+cudaError_t dispatch_dims(const kda_host::DecodeArgs& a) {
+#define KDA_DECODE_CASE(DK_, DV_) \
+    if (a.dk == DK_ && a.dv == DV_) return launch<DK_, DV_, TIn>(a);
+    KDA_DECODE_CASE(32, 32) KDA_DECODE_CASE(32, 64) KDA_DECODE_CASE(32, 128)
+    KDA_DECODE_CASE(64, 32) KDA_DECODE_CASE(64, 64) KDA_DECODE_CASE(64, 128)
+    KDA_DECODE_CASE(128, 32) KDA_DECODE_CASE(128, 64) KDA_DECODE_CASE(128, 128)
+#undef KDA_DECODE_CASE
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+namespace kda_host {
+
+cudaError_t launch_decode(const DecodeArgs& a) {
+    if (a.dtype == KDA_BF16) return dispatch_dims<__nv_bfloat16>(a);
+    return dispatch_dims<float>(a);
+}
+
+}  // namespace kda_host

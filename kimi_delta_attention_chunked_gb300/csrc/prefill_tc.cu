@@ -1,0 +1,747 @@
+// prefill_tc.cu -- chunked KDA prefill on tcgen05 tensor cores (bf16 inputs,
+// d_k = d_v = 128, chunk C = 64, fp32 state).
+//
+// The chunked form is the one of "Kimi K3: the manos, the mythos, the
+// legendos", section "FlashKDA Algorithm":
+//     B = Diag(beta)(V - K_decay S_in),  L = StrictTril(Diag(beta) K_decay K_inv^T)
+//     U = (I + L)^-1 B,  M_qk = tril(Q_decay K_inv^T)
+//     O = Q_decay S_in + M_qk U,  S_out = Diag(a_last) S_in + K_restore^T U
+// with a = exp(cumsum(log_alpha)) the inclusive cumulative decay of the chunk.
+// Everything that does not depend on S_in is computed for all chunks in
+// parallel; only the state pass is sequential.  Two kernels:
+//
+//  kda_tc_prep   one CTA per (chunk, head), fully parallel.
+//      a1  gate prep: fp32 cumulative log-decay, then bf16 MMA operands.
+//          K_inv = k / a would overflow (|cumsum| reaches 5 * 64 = 320 under
+//          the (-5, 0) log-decay bound of the "LLM architecture at trillion
+//          scale" page), so the Gram matrices are built per 16-row block b with
+//          a reference point p_b = first row of the block:
+//             row factor  q_r exp(G_r - G_pb), k_r exp(G_r - G_pb)   (<= 1)
+//             col factor  k_t exp(G_pb - G_t)  for t < p_b + 16      (<= e^75)
+//          so every exponent stays inside [-75, 75] (fp32/bf16 range) and the
+//          product equals the exact exp(G_r - G_t) weight.
+//      a2  Gram MMAs (tcgen05, M = 128 stacked q/k rows, N = 16(b+1)):
+//          M_qk (diagonal included) and L (strict, beta folded in).
+//      a3  INV = (I + L)^-1 in fp32 (16x16 diagonal blocks by substitution,
+//          then block forward substitution), then one MMA
+//          [INV Diag(beta)] [K_decay | V] -> W, U0.
+//      Writes, per (chunk, head), the MMA-ready operand images the chain
+//      needs: [Q_decay; W], K_restore^T, M_qk, U0, a_last.
+//
+//  kda_tc_chain  one CTA per (sequence, head, 64-column slice of d_v);
+//      a4/a5  for each chunk in order (operands streamed by bulk copies,
+//          two stages deep), with S kept in TMEM in fp32:
+//             P  = [Q_decay; W] S_in                    (MMA, M = 128)
+//             U  = U0 - P_w                             (W S_in = K_decay part)
+//             S  = Diag(a_last) S_in + K_restore^T U    (MMA, accumulate)
+//             P_q += M_qk U  ->  O                      (MMA, accumulate)
+//
+// Precision: MMA operands are bf16 with fp32 accumulation.  The four operands
+// whose rounding dominated the error budget -- INV Diag(beta), M_qk, U0 and U
+// -- are carried as a high and a low bf16 part (U0 as fp32), each product
+// being issued once per part, which leaves the bf16 output rounding as the
+// largest single error term.
+//
+// Every wait on an asynchronous event is bounded; a wait that runs out records
+// KDA_ERR_TIMEOUT in the status word and the kernel runs to completion.
+#include "common.cuh"
+#include "umma.cuh"
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int DK = 128, DV = 128, C = 64;
+constexpr int NT = 64;                       // d_v columns per chain CTA
+constexpr int NTILES = DV / NT;
+
+// ---- per (chunk, head) workspace block: images of shared-memory operands
+constexpr uint32_t WS_A1 = 0;                // [Q_decay; W]  K-major SW128, 128 rows, K = 128 (2 panels)
+constexpr uint32_t WS_KR = 32768;            // K_restore^T   MN-major SW128, K = 64 rows, M = 128 (2 panels)
+constexpr uint32_t WS_MQ = 49152;            // M_qk high and low bf16 parts, each K-major SW128, 64 rows, K = 64
+constexpr uint32_t WS_U0 = 65536;            // U0            fp32 [NTILES][C][NT]
+constexpr uint32_t WS_AL = 98304;            // a_last        fp32 [DK]
+constexpr uint32_t WS_BLOCK = 99328;         // 97 KiB
+constexpr uint32_t COPY_BYTES = 32768 + 16384 + 16384 + C * NT * 4 + DK * 4;
+
+// ---- prep kernel shared memory
+constexpr uint32_t K1_AG = 0;                // Gram A: 128 rows [q~ b0 | k^ b0 | q~ b1 | ...], K = 128
+constexpr uint32_t K1_BG = 32768;            // Gram B tiles, tile b has 16(b+1) rows, K = 128
+constexpr uint32_t K1_BWU = 73728;           // [K_decay | V]: MN-major, K = 64 rows, N = 256 (4 panels)
+constexpr uint32_t K1_TOT = 106496;          // float [4][128] block totals of log-decay
+constexpr uint32_t K1_FIRST = 108544;        // float [4][128] first-row log-decay of each block
+constexpr uint32_t K1_BETA = 110592;         // float [64]
+constexpr uint32_t K1_BAR = 110848;          // mbarrier (8 B) + TMEM address (4 B)
+constexpr uint32_t K1_BYTES = 110912;
+// aliases, valid once the Gram MMAs have completed
+constexpr int LDS_ = 68;                     // row stride (floats) of the fp32 64x64 matrices
+constexpr uint32_t K1_LS = 0;                // L   fp32 [64][68]
+constexpr uint32_t K1_IS = 17408;            // INV fp32 [64][68]
+constexpr uint32_t K1_XS = 34816;            // 3 x 16x16 fp32 scratch blocks
+constexpr uint32_t K1_AI = 38912;            // INV Diag(beta), high bf16 part, K-major SW128, 64 rows, K = 64
+constexpr uint32_t K1_AIL = 55296;           // ... low bf16 part (rows 64..127 of both are never used)
+constexpr uint32_t K1_TMEM_COLS = 256;
+
+// ---- chain kernel shared memory
+constexpr int K2_NS = 2;                     // operand stages in flight
+constexpr uint32_t K2_STAGE = 82944;
+constexpr uint32_t ST_A1 = 0, ST_KR = 32768, ST_MQ = 49152, ST_MQL = 57344, ST_U0 = 65536, ST_AL = 81920;
+constexpr uint32_t K2_SB = K2_NS * K2_STAGE; // S_in bf16, MN-major SW128, K = 128 rows, N = 64
+constexpr uint32_t K2_UB = K2_SB + 16384;    // U high bf16 part, MN-major SW128, K = 64 rows, N = 64
+constexpr uint32_t K2_UBL = K2_UB + 8192;    // U low bf16 part
+constexpr uint32_t K2_BAR = K2_UBL + 8192;   // full[K2_NS], mma, TMEM address
+constexpr uint32_t K2_BYTES = K2_BAR + 64;
+constexpr uint32_t K2_TMEM_COLS = 128;       // S: cols [0, 64), P: cols [64, 128)
+
+static_assert(COPY_BYTES <= K2_STAGE, "stage too small");
+static_assert(ST_MQL + 16384 <= K2_STAGE, "M_qk rows 64..127 must stay inside the stage");
+static_assert(K1_AIL + 16384 <= K1_BWU, "INV rows 64..127 must stay inside the alias region");
+static_assert(K2_BYTES + 1024 <= 232448, "chain smem");
+static_assert(2 * (K1_BYTES + 1024 + 1024) <= 233472, "prep must fit two CTAs per SM");
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void st_shared_u32(uint8_t* p, uint32_t x) { *reinterpret_cast<uint32_t*>(p) = x; }
+
+// x = hi + lo with hi = bf16(x) (returned in place) and lo = bf16(x - hi): the
+// pair carries ~16 significant bits, enough to keep an MMA operand's rounding
+// out of the error budget.
+__device__ __forceinline__ void split8(float* x, float* lo) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const float hi = __bfloat162float(__float2bfloat16_rn(x[u]));
+        lo[u] = x[u] - hi;
+        x[u] = hi;
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+    return make_uint4(kda::pack_bf16x2(f[0], f[1]), kda::pack_bf16x2(f[2], f[3]),
+                      kda::pack_bf16x2(f[4], f[5]), kda::pack_bf16x2(f[6], f[7]));
+}
+
+// ============================================================== schedule
+// cu_seqlens -> per-chunk (token start, rows, sequence) and per-sequence
+// (bos, len, first chunk, chunks).  One block; lengths are clamped so that no
+// later access leaves the arrays even for an inconsistent device cu_seqlens.
+__global__ void __launch_bounds__(1024)
+kda_tc_schedule(const int32_t* __restrict__ cu, int n_seq, int T_total, int slots,
+                int4* __restrict__ chunk_info, int4* __restrict__ seq_info, int* status) {
+    __shared__ int part[1024];
+    __shared__ int total;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (n_seq + nt - 1) / nt;
+    const int s0 = min(tid * per, n_seq), s1 = min(s0 + per, n_seq);
+    int cnt = 0;
+    for (int n = s0; n < s1; ++n) {
+        const int bos = min(max(cu[n], 0), T_total);
+        const int eos = min(max(cu[n + 1], bos), T_total);
+        cnt += (eos - bos + C - 1) / C;
+    }
+    part[tid] = cnt;
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int i = 0; i < nt; ++i) { const int c = part[i]; part[i] = acc; acc += c; }
+        total = min(acc, slots);
+        if (acc > slots) kda::record_status(status, KDA_ERR_INVALID_ARG);
+    }
+    __syncthreads();
+    int first = part[tid];
+    for (int n = s0; n < s1; ++n) {
+        const int bos = min(max(cu[n], 0), T_total);
+        const int eos = min(max(cu[n + 1], bos), T_total);
+        int len = eos - bos;
+        int nch = (len + C - 1) / C;
+        if (first + nch > slots) { nch = max(0, slots - first); len = min(len, nch * C); }
+        seq_info[n] = make_int4(bos, len, first, nch);
+        for (int j = 0; j < nch; ++j) chunk_info[first + j] = make_int4(bos + j * C, min(C, len - j * C), n, 0);
+        first += nch;
+    }
+    for (int s = total + tid; s < slots; s += nt) chunk_info[s] = make_int4(0, 0, -1, 0);
+}
+
+// ============================================================== prep (a1-a3)
+template <int B>
+__device__ __forceinline__ void gram_epilogue(uint32_t tmem, int lane, uint8_t* mq_out, float* LS) {
+    constexpr int N = 16 * (B + 1);
+    constexpr int OFF = 8 * B * (B + 1);
+    float v[N];
+#pragma unroll
+    for (int c = 0; c < N; c += 16) kda::tmem_ld16(tmem + ((uint32_t)(32 * B) << 16) + OFF + c, v + c);
+    kda::tmem_wait_ld();
+    if (lane < 16) {                          // M_qk row, diagonal included
+        const int r = 16 * B + lane;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+            float f[8], lo[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = 8 * cc + u;
+                f[u] = (t < N && t <= r) ? v[t < N ? t : 0] : 0.f;
+            }
+            split8(f, lo);
+            *reinterpret_cast<uint4*>(mq_out + kda::sw128(r, 8 * cc, 64)) = pack8(f);
+            *reinterpret_cast<uint4*>(mq_out + 8192 + kda::sw128(r, 8 * cc, 64)) = pack8(lo);
+        }
+    } else {                                  // L row (beta folded in), strict
+        const int r = 16 * B + lane - 16;
+        float* row = LS + r * LDS_;
+#pragma unroll
+        for (int t4 = 0; t4 < 64; t4 += 4) {
+            float4 x;
+            x.x = (t4 + 0 < N && t4 + 0 < r) ? v[t4 + 0 < N ? t4 + 0 : 0] : 0.f;
+            x.y = (t4 + 1 < N && t4 + 1 < r) ? v[t4 + 1 < N ? t4 + 1 : 0] : 0.f;
+            x.z = (t4 + 2 < N && t4 + 2 < r) ? v[t4 + 2 < N ? t4 + 2 : 0] : 0.f;
+            x.w = (t4 + 3 < N && t4 + 3 < r) ? v[t4 + 3 < N ? t4 + 3 : 0] : 0.f;
+            *reinterpret_cast<float4*>(row + t4) = x;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256, 2)
+kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
+            const float* __restrict__ g, const float* __restrict__ beta, int H, int use_table,
+            int fixed_len, int nch_per_seq, const int4* __restrict__ chunk_info,
+            uint8_t* __restrict__ ws_blocks, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    const int slot = blockIdx.x, h = blockIdx.y;
+    int tok0, nrows;
+    if (!use_table) {
+        const int n = slot / nch_per_seq, j = slot % nch_per_seq;
+        tok0 = n * fixed_len + j * C;
+        nrows = min(C, fixed_len - j * C);
+    } else {
+        const int4 ci = chunk_info[slot];
+        if (ci.z < 0) return;
+        tok0 = ci.x;
+        nrows = ci.y;
+    }
+    if (nrows <= 0) return;
+    uint8_t* blk = ws_blocks + ((size_t)slot * H + h) * WS_BLOCK;
+
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + K1_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + K1_BAR + 8);
+    if (w == 0) {
+        kda::tmem_alloc(tmem_slot, K1_TMEM_COLS);
+        kda::tmem_relinquish();
+    }
+    if (tid == 0) {
+        kda::mbar_init(bar, 1);
+        kda::fence_barrier_init();
+    }
+    kda::tc_fence_before();
+    __syncthreads();
+    kda::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // ---------------- a1: loads and per-block cumulative log-decay
+    const int p = w >> 2, b = w & 3;          // channel panel, row block
+    const int ch = 64 * p + 2 * lane;          // this thread's two channels
+    float G0[16], G1[16], bt[16];
+    uint32_t qv[16], kv[16];
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+        const int r = 16 * b + rr;
+        const bool ok = r < nrows;
+        const size_t tok = (size_t)tok0 + r;
+        const size_t off = (tok * H + h) * DK + ch;
+        float2 gg = ok ? *reinterpret_cast<const float2*>(g + off) : make_float2(0.f, 0.f);
+        G0[rr] = gg.x;
+        G1[rr] = gg.y;
+        qv[rr] = ok ? *reinterpret_cast<const uint32_t*>(q + off) : 0u;
+        kv[rr] = ok ? *reinterpret_cast<const uint32_t*>(k + off) : 0u;
+        bt[rr] = ok ? beta[tok * H + h] : 0.f;
+    }
+    // V slice -> right half of the [K_decay | V] operand (MN-major)
+    for (int e = tid; e < C * (DV / 8); e += 256) {
+        const int t = e >> 4, cc = e & 15;
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (t < nrows) x = *reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + t) * H + h) * DV + 8 * cc);
+        *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) = x;
+    }
+#pragma unroll
+    for (int rr = 1; rr < 16; ++rr) { G0[rr] += G0[rr - 1]; G1[rr] += G1[rr - 1]; }
+    float* tot = reinterpret_cast<float*>(sm + K1_TOT);
+    float* first = reinterpret_cast<float*>(sm + K1_FIRST);
+    float* beta_s = reinterpret_cast<float*>(sm + K1_BETA);
+    tot[b * 128 + ch] = G0[15];
+    tot[b * 128 + ch + 1] = G1[15];
+    first[b * 128 + ch] = G0[0];
+    first[b * 128 + ch + 1] = G1[0];
+    if (p == 0 && lane == 0) {
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) beta_s[16 * b + rr] = bt[rr];
+    }
+    __syncthreads();
+
+    // global cumulative log-decay at each block start (Gs) and at the chunk end
+    float Gs0[4], Gs1[4], acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        Gs0[m] = acc0 + first[m * 128 + ch];
+        Gs1[m] = acc1 + first[m * 128 + ch + 1];
+        acc0 += tot[m * 128 + ch];
+        acc1 += tot[m * 128 + ch + 1];
+    }
+    float myG0 = Gs0[0], myG1 = Gs1[0];
+#pragma unroll
+    for (int m = 1; m < 4; ++m)
+        if (m == b) { myG0 = Gs0[m]; myG1 = Gs1[m]; }
+    const float ap0 = __expf(myG0), ap1 = __expf(myG1);              // a at the block start
+    const float R0 = __expf(acc0 - myG0), R1 = __expf(acc1 - myG1);  // a_last / a(block start)
+    float f0[4], f1[4];                                              // a(p_m) / a(p_b), m > b
+#pragma unroll
+    for (int m = 0; m < 4; ++m) { f0[m] = __expf(Gs0[m] - myG0); f1[m] = __expf(Gs1[m] - myG1); }
+    if (b == 0) {
+        *reinterpret_cast<float2*>(blk + WS_AL + 4 * ch) = make_float2(__expf(acc0), __expf(acc1));
+    }
+
+    // ---------------- a1: operands
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+        const int r = 16 * b + rr;
+        const float e0 = __expf(G0[rr] - G0[0]), e1 = __expf(G1[rr] - G1[0]);   // <= 1
+        const float c0 = __expf(G0[0] - G0[rr]), c1 = __expf(G1[0] - G1[rr]);   // >= 1, <= e^75
+        const float2 qf = kda::unpack_bf16x2(qv[rr]);
+        const float2 kf = kda::unpack_bf16x2(kv[rr]);
+        const float be = bt[rr];
+        const float qt0 = qf.x * e0, qt1 = qf.y * e1;            // q~ (row factor)
+        const float kh0 = be * kf.x * e0, kh1 = be * kf.y * e1;  // k^ = beta k (row factor)
+        const float kt0 = kf.x * c0, kt1 = kf.y * c1;            // k (column factor, own block)
+        st_shared_u32(sm + K1_AG + kda::sw128(32 * b + rr, ch, 128), kda::pack_bf16x2(qt0, qt1));
+        st_shared_u32(sm + K1_AG + kda::sw128(32 * b + 16 + rr, ch, 128), kda::pack_bf16x2(kh0, kh1));
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            if (m >= b) {
+                const uint32_t toff = 2048u * m * (m + 1);
+                const float s0 = (m == b) ? 1.f : f0[m], s1 = (m == b) ? 1.f : f1[m];
+                st_shared_u32(sm + K1_BG + toff + kda::sw128(r, ch, 16 * (m + 1)),
+                              kda::pack_bf16x2(kt0 * s0, kt1 * s1));
+            }
+        }
+        // Q_decay -> rows 0..63 of the [Q_decay; W] image
+        *reinterpret_cast<uint32_t*>(blk + WS_A1 + kda::sw128(r, ch, 128)) = kda::pack_bf16x2(qt0 * ap0, qt1 * ap1);
+        // K_decay -> left half of the [K_decay | V] operand
+        st_shared_u32(sm + K1_BWU + kda::sw128(r, ch, 64),
+                      kda::pack_bf16x2(kf.x * e0 * ap0, kf.y * e1 * ap1));
+        // K_restore -> K_restore^T image (MN-major: row = token, contiguous = channel)
+        *reinterpret_cast<uint32_t*>(blk + WS_KR + kda::sw128(r, ch, 64)) = kda::pack_bf16x2(kt0 * R0, kt1 * R1);
+    }
+    kda::fence_proxy_async_smem();
+    kda::tc_fence_before();
+    __syncthreads();
+
+    // ---------------- a2: Gram MMAs, one per 16-row block
+    if (tid == 0) {
+        kda::tc_fence_after();
+        const uint32_t sAG = kda::smem_u32(sm + K1_AG), sBG = kda::smem_u32(sm + K1_BG);
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+            const uint32_t N = 16 * (bb + 1);
+            const uint32_t idesc = kda::idesc_bf16(128, N, 0, 0);
+            const uint32_t tile = sBG + 2048u * bb * (bb + 1);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t ad = kda::sw128_desc(sAG + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+                const uint64_t bd = kda::sw128_desc(tile + (s >> 2) * (N * 128) + (s & 3) * 32, 16, 1024);
+                kda::umma_bf16(tmem + 8 * bb * (bb + 1), ad, bd, idesc, s > 0 ? 1u : 0u);
+            }
+        }
+        kda::umma_commit(bar);
+    }
+    if (!kda::mbar_wait(bar, 0, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+    kda::tc_fence_after();
+
+    float* LS = reinterpret_cast<float*>(sm + K1_LS);
+    float* IS = reinterpret_cast<float*>(sm + K1_IS);
+    float* XS = reinterpret_cast<float*>(sm + K1_XS);
+    if (w == 0) gram_epilogue<0>(tmem, lane, blk + WS_MQ, LS);
+    else if (w == 1) gram_epilogue<1>(tmem, lane, blk + WS_MQ, LS);
+    else if (w == 2) gram_epilogue<2>(tmem, lane, blk + WS_MQ, LS);
+    else if (w == 3) gram_epilogue<3>(tmem, lane, blk + WS_MQ, LS);
+    kda::tc_fence_before();
+    __syncthreads();
+
+    // ---------------- a3: INV = (I + L)^-1
+    if (w < 4) {
+        if (lane < 16) {                       // diagonal block w, column `lane`
+            const int o = 16 * w, j = lane;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float a = (r == j) ? 1.f : 0.f;
+#pragma unroll
+                for (int t = 0; t < r; ++t) a = fmaf(-LS[(o + r) * LDS_ + o + t], x[t], a);
+                x[r] = a;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) IS[(o + r) * LDS_ + o + j] = x[r];
+        }
+    } else {                                   // zero the blocks above the diagonal
+        for (int e = tid - 128; e < 6 * 256; e += 128) {
+            const int pb = e >> 8, idx = e & 255;
+            const int bi = pb < 3 ? 0 : (pb < 5 ? 1 : 2);
+            const int bj = pb < 3 ? pb + 1 : (pb < 5 ? pb - 1 : 3);
+            IS[(16 * bi + (idx >> 4)) * LDS_ + 16 * bj + (idx & 15)] = 0.f;
+        }
+    }
+    __syncthreads();
+    for (int bb = 1; bb < 4; ++bb) {
+        // X_{bb,j} = sum_{m=j}^{bb-1} L_{bb,m} INV_{m,j}
+        for (int e = tid; e < bb * 256; e += 256) {
+            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            float a = 0.f;
+            for (int m = j; m < bb; ++m) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    a = fmaf(LS[(16 * bb + r) * LDS_ + 16 * m + t], IS[(16 * m + t) * LDS_ + 16 * j + c], a);
+            }
+            XS[e] = a;
+        }
+        __syncthreads();
+        // INV_{bb,j} = -INV_{bb,bb} X_{bb,j}
+        for (int e = tid; e < bb * 256; e += 256) {
+            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            float a = 0.f;
+#pragma unroll
+            for (int s = 0; s < 16; ++s)
+                a = fmaf(IS[(16 * bb + r) * LDS_ + 16 * bb + s], XS[(j << 8) + (s << 4) + c], a);
+            IS[(16 * bb + r) * LDS_ + 16 * j + c] = -a;
+        }
+        __syncthreads();
+    }
+    // INV Diag(beta) -> K-major A operand as high + low bf16 parts
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int e = tid + 256 * it;
+        const int r = e >> 3, cc = e & 7;
+        float f[8], lo[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) f[u] = IS[r * LDS_ + 8 * cc + u] * beta_s[8 * cc + u];
+        split8(f, lo);
+        *reinterpret_cast<uint4*>(sm + K1_AI + kda::sw128(r, 8 * cc, 64)) = pack8(f);
+        *reinterpret_cast<uint4*>(sm + K1_AIL + kda::sw128(r, 8 * cc, 64)) = pack8(lo);
+    }
+    kda::fence_proxy_async_smem();
+    kda::tc_fence_before();
+    __syncthreads();
+
+    // ---------------- a3: [W | U0] = INV Diag(beta) [K_decay | V]  (INV in two bf16 parts)
+    if (tid == 0) {
+        kda::tc_fence_after();
+        const uint32_t sB = kda::smem_u32(sm + K1_BWU);
+        const uint32_t idesc = kda::idesc_bf16(128, 256, 0, 1);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            const uint32_t sAI = kda::smem_u32(sm + (part ? K1_AIL : K1_AI));
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t ad = kda::sw128_desc(sAI + s * 32, 16, 1024);
+                const uint64_t bd = kda::sw128_desc(sB + s * 2048, 8192, 1024);
+                kda::umma_bf16(tmem, ad, bd, idesc, (part | s) ? 1u : 0u);
+            }
+        }
+        kda::umma_commit(bar);
+    }
+    if (!kda::mbar_wait(bar, 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+    kda::tc_fence_after();
+
+    if (w == 0 || w == 1) {                    // W rows -> rows 64..127 of [Q_decay; W]
+        const int r = 32 * w + lane;
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            float x[32];
+            kda::tmem_ld32(tmem + ((uint32_t)(32 * w) << 16) + 32 * cb, x);
+            kda::tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                *reinterpret_cast<uint4*>(blk + WS_A1 + kda::sw128(64 + r, 32 * cb + 8 * u, 128)) = pack8(x + 8 * u);
+        }
+    } else if (w == 4 || w == 5) {             // U0 rows (fp32) -> [tile][row][NT]
+        const int r = 32 * (w - 4) + lane;
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            float x[32];
+            kda::tmem_ld32(tmem + ((uint32_t)(32 * (w - 4)) << 16) + 128 + 32 * cb, x);
+            kda::tmem_wait_ld();
+            const int j = 32 * cb, tile = j / NT;
+            float4* dst = reinterpret_cast<float4*>(blk + WS_U0 + ((size_t)(tile * C + r) * NT + (j % NT)) * 4);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) dst[u] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+        }
+    }
+    kda::tc_fence_before();
+    __syncthreads();
+    if (w == 0) kda::tmem_dealloc(tmem, K1_TMEM_COLS);
+}
+
+// ============================================================== chain (a4, a5)
+__global__ void __launch_bounds__(128, 1)
+kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, int nch_per_seq,
+             const uint8_t* __restrict__ ws_blocks, const float* __restrict__ S0, int H,
+             bf16* __restrict__ O, float* __restrict__ S_final, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    const int tile = blockIdx.x % NTILES, n = blockIdx.x / NTILES, h = blockIdx.y;
+    int bos, len, first, nch;
+    if (!use_table) {
+        bos = n * fixed_len; len = fixed_len; first = n * nch_per_seq; nch = nch_per_seq;
+    } else {
+        const int4 si = seq_info[n];
+        bos = si.x; len = si.y; first = si.z; nch = si.w;
+    }
+    const int tid = threadIdx.x, w = tid >> 5;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + K2_BAR);
+    uint64_t* mbar = full + K2_NS;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + K2_NS + 1);
+    if (w == 0) {
+        kda::tmem_alloc(tmem_slot, K2_TMEM_COLS);
+        kda::tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int s = 0; s < K2_NS; ++s) kda::mbar_init(full + s, 1);
+        kda::mbar_init(mbar, 1);
+        kda::fence_barrier_init();
+    }
+    kda::tc_fence_before();
+    __syncthreads();
+    kda::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_off = (uint32_t)(32 * w) << 16;
+    const uint32_t tS = tmem + lane_off, tP = tmem + lane_off + 64;
+    const int i = tid;                          // TMEM lane = state row (key channel)
+
+    auto issue = [&](int c) {
+        const int st = c % K2_NS;
+        uint8_t* stage = sm + st * K2_STAGE;
+        const uint8_t* src = ws_blocks + ((size_t)(first + c) * H + h) * WS_BLOCK;
+        kda::mbar_arrive_expect_tx(full + st, COPY_BYTES);
+        kda::bulk_g2s(stage + ST_A1, src + WS_A1, 32768, full + st);
+        kda::bulk_g2s(stage + ST_KR, src + WS_KR, 16384, full + st);
+        kda::bulk_g2s(stage + ST_MQ, src + WS_MQ, 16384, full + st);
+        kda::bulk_g2s(stage + ST_U0, src + WS_U0 + (uint32_t)tile * C * NT * 4, C * NT * 4, full + st);
+        kda::bulk_g2s(stage + ST_AL, src + WS_AL, DK * 4, full + st);
+    };
+
+    // initial state slice -> TMEM
+    {
+        float s[64];
+        if (S0) {
+            const float4* src = reinterpret_cast<const float4*>(S0 + (((size_t)n * H + h) * DK + i) * DV + tile * NT);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float4 x = src[u];
+                s[4 * u] = x.x; s[4 * u + 1] = x.y; s[4 * u + 2] = x.z; s[4 * u + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 64; ++u) s[u] = 0.f;
+        }
+        kda::tmem_st32(tS, s);
+        kda::tmem_st32(tS + 32, s + 32);
+        kda::tmem_wait_st();
+    }
+    if (tid == 0)
+        for (int c = 0; c < min(K2_NS, nch); ++c) issue(c);
+    kda::tc_fence_before();
+    __syncthreads();
+    kda::tc_fence_after();
+
+    const uint32_t sSB = kda::smem_u32(sm + K2_SB), sUB = kda::smem_u32(sm + K2_UB);
+    const uint32_t sUBL = kda::smem_u32(sm + K2_UBL);
+    uint32_t mma_phase = 0;
+    for (int c = 0; c < nch; ++c) {
+        const int st = c % K2_NS;
+        uint8_t* stage = sm + st * K2_STAGE;
+        if (!kda::mbar_wait(full + st, (uint32_t)((c / K2_NS) & 1), kda::kWaitCycles))
+            kda::record_status(status, kda::kDevTimeout);
+
+        // S_in -> bf16 operand; TMEM state <- Diag(a_last) S_in
+        {
+            float s[64];
+            kda::tmem_ld32(tS, s);
+            kda::tmem_ld32(tS + 32, s + 32);
+            kda::tmem_wait_ld();
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+                *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(i, 8 * cc, 128)) = pack8(s + 8 * cc);
+            const float al = reinterpret_cast<const float*>(stage + ST_AL)[i];
+#pragma unroll
+            for (int u = 0; u < 64; ++u) s[u] *= al;
+            kda::tmem_st32(tS, s);
+            kda::tmem_st32(tS + 32, s + 32);
+            kda::tmem_wait_st();
+        }
+        kda::fence_proxy_async_smem();
+        kda::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {                         // P = [Q_decay; W] S_in
+            kda::tc_fence_after();
+            const uint32_t sA1 = kda::smem_u32(stage + ST_A1);
+            const uint32_t idesc = kda::idesc_bf16(128, NT, 0, 1);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t ad = kda::sw128_desc(sA1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+                const uint64_t bd = kda::sw128_desc(sSB + s * 2048, 16384, 1024);
+                kda::umma_bf16(tmem + 64, ad, bd, idesc, s > 0 ? 1u : 0u);
+            }
+            kda::umma_commit(mbar);
+        }
+        if (!kda::mbar_wait(mbar, mma_phase, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        mma_phase ^= 1;
+        kda::tc_fence_after();
+
+        if (w >= 2) {                            // U = U0 - W S_in -> high + low bf16 operands
+            const int r = tid - 64;
+            float pw[64];
+            kda::tmem_ld32(tP, pw);
+            kda::tmem_ld32(tP + 32, pw + 32);
+            kda::tmem_wait_ld();
+            const float4* u0 = reinterpret_cast<const float4*>(stage + ST_U0 + r * NT * 4);
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                const float4 x0 = u0[2 * cc], x1 = u0[2 * cc + 1];
+                float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w}, lo[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) f[u] -= pw[8 * cc + u];
+                split8(f, lo);
+                *reinterpret_cast<uint4*>(sm + K2_UB + kda::sw128(r, 8 * cc, 64)) = pack8(f);
+                *reinterpret_cast<uint4*>(sm + K2_UBL + kda::sw128(r, 8 * cc, 64)) = pack8(lo);
+            }
+        }
+        kda::fence_proxy_async_smem();
+        kda::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            kda::tc_fence_after();
+            const uint32_t sKR = kda::smem_u32(stage + ST_KR);
+            const uint32_t sMQ = kda::smem_u32(stage + ST_MQ), sMQL = kda::smem_u32(stage + ST_MQL);
+            const uint32_t id_s = kda::idesc_bf16(128, NT, 1, 1);
+            const uint32_t id_o = kda::idesc_bf16(128, NT, 0, 1);
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {   // S += K_restore^T (U_hi + U_lo)
+                const uint32_t sU = part ? sUBL : sUB;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ad = kda::sw128_desc(sKR + s * 2048, 8192, 1024);
+                    const uint64_t bd = kda::sw128_desc(sU + s * 2048, 8192, 1024);
+                    kda::umma_bf16(tmem, ad, bd, id_s, 1u);
+                }
+            }
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {   // P_q += M_hi U_hi + M_hi U_lo + M_lo U_hi
+                const uint32_t sA = part == 2 ? sMQL : sMQ;
+                const uint32_t sU = part == 1 ? sUBL : sUB;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ad = kda::sw128_desc(sA + s * 32, 16, 1024);
+                    const uint64_t bd = kda::sw128_desc(sU + s * 2048, 8192, 1024);
+                    kda::umma_bf16(tmem + 64, ad, bd, id_o, 1u);
+                }
+            }
+            kda::umma_commit(mbar);
+        }
+        if (!kda::mbar_wait(mbar, mma_phase, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        mma_phase ^= 1;
+        kda::tc_fence_after();
+        if (tid == 0 && c + K2_NS < nch) issue(c + K2_NS);   // this stage is free again
+
+        if (w < 2) {                             // O rows of this chunk
+            const int r = tid;
+            float o[64];
+            kda::tmem_ld32(tP, o);
+            kda::tmem_ld32(tP + 32, o + 32);
+            kda::tmem_wait_ld();
+            if (r < len - c * C) {
+                uint4* dst = reinterpret_cast<uint4*>(O + ((size_t)(bos + c * C + r) * H + h) * DV + tile * NT);
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) dst[cc] = pack8(o + 8 * cc);
+            }
+        }
+        kda::tc_fence_before();
+    }
+    __syncthreads();
+    kda::tc_fence_after();
+    if (S_final) {
+        float s[64];
+        kda::tmem_ld32(tS, s);
+        kda::tmem_ld32(tS + 32, s + 32);
+        kda::tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(S_final + (((size_t)n * H + h) * DK + i) * DV + tile * NT);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) dst[u] = make_float4(s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]);
+    }
+    kda::tc_fence_before();
+    __syncthreads();
+    if (w == 0) kda::tmem_dealloc(tmem, K2_TMEM_COLS);
+}
+
+size_t header_bytes(int n_seq, long long slots) {
+    const size_t raw = 16u * (size_t)slots + 16u * (size_t)n_seq;
+    return (raw + 1023) & ~size_t(1023);
+}
+
+long long slot_bound(int n_seq, int T_total) { return (long long)T_total / C + n_seq; }
+
+}  // namespace
+
+namespace kda_host {
+
+bool tc_supported(int dk, int dv, int chunk, kda_dtype dt) {
+    return dt == KDA_BF16 && dk == DK && dv == DV && chunk == C;
+}
+
+size_t tc_workspace_bytes(int n_seq, int T_total, int H, int chunk) {
+    (void)chunk;
+    const long long ub = slot_bound(n_seq, T_total);
+    return header_bytes(n_seq, ub) + (size_t)ub * H * WS_BLOCK;
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a) {
+    if (a.n_seq == 0) return cudaSuccess;
+    const long long ub = slot_bound(a.n_seq, a.T_total);
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    int4* chunk_info = reinterpret_cast<int4*>(ws);
+    int4* seq_info = reinterpret_cast<int4*>(ws + 16 * (size_t)ub);
+    uint8_t* blocks = ws + header_bytes(a.n_seq, ub);
+
+    // Equal-length batches map chunks to sequences arithmetically; packed
+    // varlen batches go through the chunk table built on the device.
+    const int use_table = a.cu_seqlens != nullptr;
+    const int fixed_len = use_table ? 0 : a.T_total / a.n_seq;
+    const int nch_per = use_table ? 0 : (fixed_len + C - 1) / C;
+    if (use_table) {
+        kda_tc_schedule<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.n_seq, a.T_total, (int)ub, chunk_info,
+                                                  seq_info, a.status);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        trace_mark(a.stream);
+    }
+    const int prep_smem = (int)(K1_BYTES + 1024);
+    const int chain_smem = (int)(K2_BYTES + 1024);
+    cudaError_t e = cudaFuncSetAttribute(kda_tc_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kda_tc_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
+    if (e != cudaSuccess) return e;
+    if (a.total_chunks > 0) {
+        kda_tc_prep<<<dim3(a.total_chunks, a.H), 256, prep_smem, a.stream>>>(
+            static_cast<const bf16*>(a.q), static_cast<const bf16*>(a.k), static_cast<const bf16*>(a.v),
+            a.log_alpha, a.beta, a.H, use_table, fixed_len, nch_per, chunk_info, blocks, a.status);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        trace_mark(a.stream);
+    }
+    kda_tc_chain<<<dim3(NTILES * a.n_seq, a.H), 128, chain_smem, a.stream>>>(
+        seq_info, use_table, fixed_len, nch_per, blocks, a.S0, a.H, static_cast<bf16*>(a.O), a.S_final,
+        a.status);
+    e = cudaGetLastError();
+    trace_mark(a.stream);
+    return e;
+}
+
+}  // namespace kda_host

@@ -1,0 +1,151 @@
+"""Chunked prefill: CUDA kernels vs the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import kimi_delta_attention_chunked_gb300 as kda
+from kimi_delta_attention_chunked_gb300 import inputs
+from _gpu import need_gpu, rel_err, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(w, dev, lengths=None, seed=0, heads=None, host_cu=True, check=True, alias_state=False):
+    d = inputs.make_prefill(w, device=dev, seed=seed, lengths=lengths)
+    S0 = d["S0"]
+    kw = {}
+    if alias_state and S0 is not None:
+        state = S0.clone()                     # S0 and S_final are the same buffer
+        kw["S_final"] = state
+        S_in = state
+    else:
+        S_in = S0
+    O, Sf = kda.kda_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=S_in,
+                            cu_seqlens=d["cu_seqlens"], cu_seqlens_host=d["cu_seqlens_host"] if host_cu else None,
+                            chunk=w.chunk, **kw)
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_device_status() == 0
+    if not check:
+        return d, O, Sf, None, None
+    h0, h1 = heads if heads else (0, w.H)
+    sl = slice(h0, h1)
+    s0 = None if S0 is None else S0[:, sl].contiguous()
+    O_ref, Sf_ref = oracle.prefill(d["q"][:, sl].contiguous(), d["k"][:, sl].contiguous(), d["v"][:, sl].contiguous(),
+                                   d["log_alpha"][:, sl].contiguous(), d["beta"][:, sl].contiguous(),
+                                   cu_seqlens=d["cu_seqlens_host"], S0=s0)
+    eo = rel_err(O[:, sl], O_ref)
+    es = rel_err(Sf[:, sl], Sf_ref)
+    return d, O, Sf, eo, es
+
+
+# ------------------------------------------------------------- CUDA-core path
+def test_tiny_fp32_workload():
+    """B=1, H=2, T=64, d=32, chunk 16, fp32: the 1e-4 correctness case."""
+    dev = need_gpu()
+    w = inputs.WORKLOADS["tiny_fp32_T64_H2_D32"]
+    _, _, _, eo, es = run_case(w, dev)
+    assert eo <= 1e-4 and es <= 1e-4, (eo, es)
+
+
+@pytest.mark.parametrize("dk,dv,chunk", [(32, 32, 16), (64, 32, 32), (128, 64, 64), (32, 128, 16), (64, 64, 64)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_simt_path_varlen(dk, dv, chunk, dtype):
+    """Ragged varlen batches (empty, shorter than a chunk, several chunks + tail)."""
+    dev = need_gpu()
+    w = inputs.Workload("simt", "prefill", H=3, dk=dk, dv=dv, dtype=dtype, chunk=chunk, s0_std=0.02)
+    _, _, _, eo, es = run_case(w, dev, lengths=[0, 1, chunk - 1, 2 * chunk + 5, 3 * chunk], seed=dk + chunk)
+    assert eo <= tol_for(dtype), eo
+    assert es <= tol_for(dtype), es
+
+
+def test_chunk_size_invariance_fp32():
+    """The chunk form is exact for any chunk size: C = 16, 32, 64 agree (fp32)."""
+    dev = need_gpu()
+    outs = []
+    for C in (16, 32, 64):
+        w = inputs.Workload("inv", "prefill", H=2, dk=64, dv=64, dtype=torch.float32, chunk=C, s0_std=0.02)
+        d, O, Sf, _, _ = run_case(w, dev, lengths=[150, 37], seed=5, check=False)
+        outs.append((O.double().cpu().numpy(), Sf.double().cpu().numpy()))
+    for O, Sf in outs[1:]:
+        assert rel_err(torch.from_numpy(O), outs[0][0]) < 1e-5
+        assert rel_err(torch.from_numpy(Sf), outs[0][1]) < 1e-5
+
+
+# ------------------------------------------------------------- tensor-core path
+TC = dict(H=4, dk=128, dv=128, dtype=torch.bfloat16, chunk=64)
+
+
+@pytest.mark.parametrize("lengths", [[1], [17], [64], [65], [200], [64 * 5], [0, 130, 1, 64, 63, 129]])
+def test_tc_path_lengths(lengths):
+    dev = need_gpu()
+    w = inputs.Workload("tc", "prefill", s0_std=0.02, **TC)
+    _, _, _, eo, es = run_case(w, dev, lengths=lengths, seed=len(lengths) + sum(lengths))
+    assert eo <= 5e-3, eo
+    assert es <= 5e-3, es
+
+
+def test_tc_path_zero_state_and_device_only_cu_seqlens():
+    dev = need_gpu()
+    w = inputs.Workload("tc", "prefill", **TC)
+    _, _, _, eo, es = run_case(w, dev, lengths=[300, 77, 640], seed=11, host_cu=False)
+    assert eo <= 5e-3 and es <= 5e-3, (eo, es)
+
+
+def test_tc_path_equal_lengths_without_cu_seqlens():
+    """cu_seqlens = NULL: n_seq = 1 sequence covering all tokens."""
+    dev = need_gpu()
+    w = inputs.Workload("tc", "prefill", T=333, B=1, **TC)
+    d = inputs.make_prefill(w, device=dev, seed=12)
+    O, Sf = kda.kda_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"])
+    O_ref, Sf_ref = oracle.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"])
+    assert rel_err(O, O_ref) <= 5e-3
+    assert rel_err(Sf, Sf_ref) <= 5e-3
+
+
+def test_tc_state_aliasing():
+    dev = need_gpu()
+    w = inputs.Workload("tc", "prefill", s0_std=0.02, **TC)
+    _, _, _, eo, es = run_case(w, dev, lengths=[100, 250], seed=13, alias_state=True)
+    assert eo <= 5e-3 and es <= 5e-3, (eo, es)
+
+
+def test_tc_split_prefill_equals_one_prefill():
+    """Prefill of T1 then T2 from the carried state == one prefill of T1 + T2."""
+    dev = need_gpu()
+    w = inputs.Workload("tc", "prefill", T=448, B=1, s0_std=0.02, **TC)
+    d = inputs.make_prefill(w, device=dev, seed=14)
+    a = lambda x, s: x[s].contiguous()
+    O, Sf = kda.kda_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=d["S0"])
+    s1, s2 = slice(0, 192), slice(192, 448)
+    O1, S1 = kda.kda_prefill(a(d["q"], s1), a(d["k"], s1), a(d["v"], s1), a(d["log_alpha"], s1), a(d["beta"], s1),
+                             S0=d["S0"])
+    O2, S2 = kda.kda_prefill(a(d["q"], s2), a(d["k"], s2), a(d["v"], s2), a(d["log_alpha"], s2), a(d["beta"], s2),
+                             S0=S1)
+    assert rel_err(torch.cat([O1, O2]), O.double().cpu().numpy()) < 5e-3
+    assert rel_err(S2, Sf.double().cpu().numpy()) < 5e-3
+
+
+# ------------------------------------------------------------- full-size workloads
+def test_full_prefill_8k():
+    """B=1, H=32, T=8192, d=128, chunk 64, bf16: every output vs the oracle."""
+    dev = need_gpu()
+    _, _, _, eo, es = run_case(inputs.WORKLOADS["prefill_bf16_T8192_H32_D128"], dev)
+    assert eo <= 5e-3 and es <= 5e-3, (eo, es)
+
+
+def test_full_varlen_sampled_heads():
+    """8 packed sequences of 1K..32K tokens with random S0; heads 0, 31 vs the oracle."""
+    dev = need_gpu()
+    w = inputs.WORKLOADS["varlen_bf16_8seq_1K_32K_H32_D128"]
+    for heads in [(0, 1), (31, 32)]:
+        _, _, _, eo, es = run_case(w, dev, heads=heads)
+        assert eo <= 5e-3 and es <= 5e-3, (heads, eo, es)
+
+
+@pytest.mark.slow
+def test_full_long_context_sampled_head():
+    """T = 1,048,576, H = 32, strong decay: head 7 vs the oracle (O and final state)."""
+    dev = need_gpu()
+    _, _, _, eo, es = run_case(inputs.WORKLOADS["long_bf16_T1M_H32_D128"], dev, heads=(7, 8))
+    assert eo <= 5e-3 and es <= 5e-3, (eo, es)
