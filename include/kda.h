@@ -119,6 +119,39 @@ KDA_API kda_status kda_prefill(const void* q, const void* k, const void* v,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Size of the fixed device array that kda_prefill_noalloc uses as its
+ * workspace (bytes).  Every GPU that loads the library holds it until exit.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * kda_prefill without a caller-provided workspace.  The paper has no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory -- runtimes that own all device memory through their own fixed pool
+ * and do not let libraries call cudaMalloc, plugin interfaces that give a
+ * library only its inputs and outputs, and deployments whose memory footprint
+ * is fixed at start-up.
+ *
+ * Same arguments and results as kda_prefill, minus (workspace,
+ * workspace_bytes).  The workspace is a file-scope device array of
+ * KDA_NOALLOC_SCRATCH_BYTES; the call allocates nothing.
+ *   - Returns KDA_ERR_WORKSPACE, before launching anything, when
+ *     kda_prefill_workspace_size(...) for the problem exceeds
+ *     KDA_NOALLOC_SCRATCH_BYTES (e.g. more than about 640 chunk-head slots
+ *     on the tensor-core path: H = 32 heads of ~1280 tokens).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls that overlap
+ *     on the GPU race on it: order them on one stream.
+ */
+KDA_API kda_status kda_prefill_noalloc(const void* q, const void* k, const void* v,
+                               const float* log_alpha, const float* beta, const float* S0,
+                               const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                               int n_seq, int T_total, int H, int dk, int dv, int chunk,
+                               kda_dtype dtype, void* O, float* S_final, cudaStream_t stream);
+
+/*
  * One decode step for N independent sequences (one token each), the per-token
  * form u = beta (v - (D S)^T k), S <- D S + k u^T, o = S^T q of "Kimi K3: the
  * manos, the mythos, the legendos", section "FlashKDA Algorithm".

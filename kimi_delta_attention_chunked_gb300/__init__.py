@@ -5,7 +5,8 @@ in ``include/kda.h``); this package only builds it and marshals arguments to
 it.  ``inputs`` holds the seeded synthetic workloads.
 """
 from ._lib import (KDAError, kda_decode, kda_get_last_device_status, kda_prefill,  # noqa: F401
-                   kda_prefill_workspace_size, kda_set_trace_events, kda_status_string, load)
+                   kda_prefill_noalloc, kda_prefill_workspace_size, kda_set_trace_events, kda_status_string,
+                   load)
 
-__all__ = ["KDAError", "kda_decode", "kda_get_last_device_status", "kda_prefill",
+__all__ = ["KDAError", "kda_decode", "kda_get_last_device_status", "kda_prefill", "kda_prefill_noalloc",
            "kda_prefill_workspace_size", "kda_set_trace_events", "kda_status_string", "load"]

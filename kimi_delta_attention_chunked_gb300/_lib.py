@@ -18,8 +18,9 @@ LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(6)
 KDA_FP32, KDA_BF16 = 0, 1
-SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_decode", "kda_get_last_device_status",
-           "kda_set_trace_events", "kda_status_string")
+SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_noalloc", "kda_decode",
+           "kda_get_last_device_status", "kda_set_trace_events", "kda_status_string")
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -46,6 +47,8 @@ def load():
         lib.kda_prefill_workspace_size.restype = Z
         lib.kda_prefill.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, Z, P]
         lib.kda_prefill.restype = I
+        lib.kda_prefill_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
+        lib.kda_prefill_noalloc.restype = I
         lib.kda_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P]
         lib.kda_decode.restype = I
         lib.kda_get_last_device_status.argtypes = [P]
@@ -130,6 +133,39 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, cu_seqlens_h
                          ws_bytes, _stream(stream, dev))
     if st != KDA_OK:
         raise KDAError(st, "kda_prefill")
+    return O, S_final
+
+
+def kda_prefill_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, cu_seqlens_host=None, chunk=64,
+                        O=None, S_final=None, stream=None):
+    """kda_prefill with the library's fixed device scratch array as workspace,
+    for callers that cannot allocate device memory (see include/kda.h).
+    Outputs O and S_final must be passed in by such callers; allocating them
+    here is only a convenience of this binding.  Returns (O, S_final)."""
+    lib = load()
+    dev = q.device
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_dev(name, t, dev, q.dtype)
+    _check_dev("log_alpha", log_alpha, dev, torch.float32)
+    _check_dev("beta", beta, dev, torch.float32)
+    _check_dev("cu_seqlens", cu_seqlens, dev, torch.int32)
+    n_seq = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if S0 is not None:
+        _check_dev("S0", S0, dev, torch.float32)
+    if O is None:
+        O = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    if S_final is None:
+        S_final = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev)
+    host = None
+    if cu_seqlens_host is not None:
+        host = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+    st = lib.kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                                 _ptr(cu_seqlens), host, n_seq, T, H, dk, dv, chunk, _dtype_code(q.dtype),
+                                 _ptr(O), _ptr(S_final), _stream(stream, dev))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_prefill_noalloc")
     return O, S_final
 
 
