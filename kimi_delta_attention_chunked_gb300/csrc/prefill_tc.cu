@@ -20,10 +20,11 @@
 //             col factor  k_t exp(G_pb - G_t)  for t < p_b + 16      (<= e^75)
 //          so every exponent stays inside [-75, 75] (fp32/bf16 range) and the
 //          product equals the exact exp(G_r - G_t) weight.
-//      a2  Gram MMAs (tcgen05, M = 128 stacked q/k rows, N = 16(b+1)):
-//          M_qk (diagonal included) and L (strict, beta folded in).
+//      a2  Gram MMAs (tcgen05, M = 128 stacked q/k rows; the four blocks'
+//          column operands stacked along N = 160): M_qk (diagonal included)
+//          and L (strict, beta folded in).
 //      a3  INV = (I + L)^-1 in fp32 (16x16 diagonal blocks by substitution,
-//          then block forward substitution), then one MMA
+//          then two levels of 2x2 block merges done warp by warp), then one MMA
 //          [INV Diag(beta)] [K_decay | V] -> W, U0.
 //      Writes, per (chunk, head), the MMA-ready operand images the chain
 //      needs: [Q_decay; W], K_restore^T, M_qk, U0, a_last.
@@ -66,7 +67,8 @@ constexpr uint32_t COPY_BYTES = 32768 + 16384 + 16384 + C * NT * 4 + DK * 4;
 
 // ---- prep kernel shared memory
 constexpr uint32_t K1_AG = 0;                // Gram A: 128 rows [q~ b0 | k^ b0 | q~ b1 | ...], K = 128
-constexpr uint32_t K1_BG = 32768;            // Gram B tiles, tile b has 16(b+1) rows, K = 128
+constexpr uint32_t K1_BG = 32768;            // Gram B: tiles b = 0..3 (16(b+1) rows each) stacked along N
+                                             // at row 8b(b+1): one 160-row K-major tile, K = 128
 constexpr uint32_t K1_BWU = 73728;           // [K_decay | V]: MN-major, K = 64 rows, N = 256 (4 panels)
 constexpr uint32_t K1_TOT = 106496;          // float [4][128] block totals of log-decay
 constexpr uint32_t K1_FIRST = 108544;        // float [4][128] first-row log-decay of each block
@@ -77,7 +79,7 @@ constexpr uint32_t K1_BYTES = 110912;
 constexpr int LDS_ = 68;                     // row stride (floats) of the fp32 64x64 matrices
 constexpr uint32_t K1_LS = 0;                // L   fp32 [64][68]
 constexpr uint32_t K1_IS = 17408;            // INV fp32 [64][68]
-constexpr uint32_t K1_XS = 34816;            // 3 x 16x16 fp32 scratch blocks
+constexpr uint32_t K1_XS = 34816;            // 4 x 16x16 fp32 scratch blocks (dense)
 constexpr uint32_t K1_AI = 38912;            // INV Diag(beta), high bf16 part, K-major SW128, 64 rows, K = 64
 constexpr uint32_t K1_AIL = 55296;           // ... low bf16 part (rows 64..127 of both are never used)
 constexpr uint32_t K1_TMEM_COLS = 256;
@@ -89,9 +91,9 @@ constexpr uint32_t ST_A1 = 0, ST_KR = 32768, ST_MQ = 49152, ST_MQL = 57344, ST_U
 constexpr uint32_t K2_SB = K2_NS * K2_STAGE; // S_in bf16, MN-major SW128, K = 128 rows, N = 64
 constexpr uint32_t K2_UB = K2_SB + 16384;    // U high bf16 part, MN-major SW128, K = 64 rows, N = 64
 constexpr uint32_t K2_UBL = K2_UB + 8192;    // U low bf16 part
-constexpr uint32_t K2_BAR = K2_UBL + 8192;   // full[K2_NS], mma, TMEM address
+constexpr uint32_t K2_BAR = K2_UBL + 8192;   // full[K2_NS], p, s, o, TMEM address
 constexpr uint32_t K2_BYTES = K2_BAR + 64;
-constexpr uint32_t K2_TMEM_COLS = 128;       // S: cols [0, 64), P: cols [64, 128)
+constexpr uint32_t K2_TMEM_COLS = 256;       // S: cols [0, 64), P double buffer: [64, 128), [128, 192)
 
 static_assert(COPY_BYTES <= K2_STAGE, "stage too small");
 static_assert(ST_MQL + 16384 <= K2_STAGE, "M_qk rows 64..127 must stay inside the stage");
@@ -115,6 +117,39 @@ __device__ __forceinline__ void split8(float* x, float* lo) {
         lo[u] = x[u] - hi;
         x[u] = hi;
     }
+}
+
+// One warp: acc (+)= A * B for 16x16 fp32 blocks in shared memory (row-major,
+// leading dimensions lda / ldb).  Lane l owns row l / 2, columns 8 (l % 2) .. +7.
+__device__ __forceinline__ void mm16(float (&acc)[8], const float* A, int lda, const float* B, int ldb, int lane,
+                                     bool accumulate) {
+    const int r = lane >> 1, c0 = 8 * (lane & 1);
+    if (!accumulate) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    }
+#pragma unroll
+    for (int k4 = 0; k4 < 16; k4 += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(A + r * lda + k4);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float4 b0 = *reinterpret_cast<const float4*>(B + (k4 + kk) * ldb + c0);
+            const float4 b1 = *reinterpret_cast<const float4*>(B + (k4 + kk) * ldb + c0 + 4);
+            acc[0] = fmaf(av[kk], b0.x, acc[0]); acc[1] = fmaf(av[kk], b0.y, acc[1]);
+            acc[2] = fmaf(av[kk], b0.z, acc[2]); acc[3] = fmaf(av[kk], b0.w, acc[3]);
+            acc[4] = fmaf(av[kk], b1.x, acc[4]); acc[5] = fmaf(av[kk], b1.y, acc[5]);
+            acc[6] = fmaf(av[kk], b1.z, acc[6]); acc[7] = fmaf(av[kk], b1.w, acc[7]);
+        }
+    }
+}
+
+__device__ __forceinline__ void st16(float* D, int ldd, const float (&acc)[8], int lane, float scale) {
+    const int r = lane >> 1, c0 = 8 * (lane & 1);
+    *reinterpret_cast<float4*>(D + r * ldd + c0) =
+        make_float4(scale * acc[0], scale * acc[1], scale * acc[2], scale * acc[3]);
+    *reinterpret_cast<float4*>(D + r * ldd + c0 + 4) =
+        make_float4(scale * acc[4], scale * acc[5], scale * acc[6], scale * acc[7]);
 }
 
 __device__ __forceinline__ uint4 pack8(const float* f) {
@@ -318,9 +353,8 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             if (m >= b) {
-                const uint32_t toff = 2048u * m * (m + 1);
                 const float s0 = (m == b) ? 1.f : f0[m], s1 = (m == b) ? 1.f : f1[m];
-                st_shared_u32(sm + K1_BG + toff + kda::sw128(r, ch, 16 * (m + 1)),
+                st_shared_u32(sm + K1_BG + kda::sw128(8 * m * (m + 1) + r, ch, 160),
                               kda::pack_bf16x2(kt0 * s0, kt1 * s1));
             }
         }
@@ -336,21 +370,17 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
     kda::tc_fence_before();
     __syncthreads();
 
-    // ---------------- a2: Gram MMAs, one per 16-row block
+    // ---------------- a2: Gram MMAs: all 128 rows against the 160 stacked B rows
+    // (row block b's products sit in columns [8b(b+1), 8b(b+1) + 16(b+1)))
     if (tid == 0) {
         kda::tc_fence_after();
         const uint32_t sAG = kda::smem_u32(sm + K1_AG), sBG = kda::smem_u32(sm + K1_BG);
+        const uint32_t idesc = kda::idesc_bf16(128, 160, 0, 0);
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-            const uint32_t N = 16 * (bb + 1);
-            const uint32_t idesc = kda::idesc_bf16(128, N, 0, 0);
-            const uint32_t tile = sBG + 2048u * bb * (bb + 1);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint64_t ad = kda::sw128_desc(sAG + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
-                const uint64_t bd = kda::sw128_desc(tile + (s >> 2) * (N * 128) + (s & 3) * 32, 16, 1024);
-                kda::umma_bf16(tmem + 8 * bb * (bb + 1), ad, bd, idesc, s > 0 ? 1u : 0u);
-            }
+        for (int s = 0; s < 8; ++s) {
+            const uint64_t ad = kda::sw128_desc(sAG + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+            const uint64_t bd = kda::sw128_desc(sBG + (s >> 2) * 20480 + (s & 3) * 32, 16, 1024);
+            kda::umma_bf16(tmem, ad, bd, idesc, s > 0 ? 1u : 0u);
         }
         kda::umma_commit(bar);
     }
@@ -367,7 +397,8 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
     kda::tc_fence_before();
     __syncthreads();
 
-    // ---------------- a3: INV = (I + L)^-1
+    // ---------------- a3: INV = (I + L)^-1, by 16x16 blocks
+    // (1) diagonal blocks D_b by forward substitution (warps 0-3); zero the blocks above
     if (w < 4) {
         if (lane < 16) {                       // diagonal block w, column `lane`
             const int o = 16 * w, j = lane;
@@ -382,7 +413,7 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
 #pragma unroll
             for (int r = 0; r < 16; ++r) IS[(o + r) * LDS_ + o + j] = x[r];
         }
-    } else {                                   // zero the blocks above the diagonal
+    } else {
         for (int e = tid - 128; e < 6 * 256; e += 128) {
             const int pb = e >> 8, idx = e & 255;
             const int bi = pb < 3 ? 0 : (pb < 5 ? 1 : 2);
@@ -391,30 +422,45 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
         }
     }
     __syncthreads();
-    for (int bb = 1; bb < 4; ++bb) {
-        // X_{bb,j} = sum_{m=j}^{bb-1} L_{bb,m} INV_{m,j}
-        for (int e = tid; e < bb * 256; e += 256) {
-            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            float a = 0.f;
-            for (int m = j; m < bb; ++m) {
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    a = fmaf(LS[(16 * bb + r) * LDS_ + 16 * m + t], IS[(16 * m + t) * LDS_ + 16 * j + c], a);
-            }
-            XS[e] = a;
-        }
-        __syncthreads();
-        // INV_{bb,j} = -INV_{bb,bb} X_{bb,j}
-        for (int e = tid; e < bb * 256; e += 256) {
-            const int j = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            float a = 0.f;
-#pragma unroll
-            for (int s = 0; s < 16; ++s)
-                a = fmaf(IS[(16 * bb + r) * LDS_ + 16 * bb + s], XS[(j << 8) + (s << 4) + c], a);
-            IS[(16 * bb + r) * LDS_ + 16 * j + c] = -a;
-        }
-        __syncthreads();
+    auto blkL = [&](int bi, int bj) { return LS + (16 * bi) * LDS_ + 16 * bj; };
+    auto blkI = [&](int bi, int bj) { return IS + (16 * bi) * LDS_ + 16 * bj; };
+    // (2) INV_10 = -D1 (L10 D0), INV_32 = -D3 (L32 D2)   (warps 0, 1)
+    if (w < 2) {
+        const int b0 = 2 * w;
+        float acc[8];
+        mm16(acc, blkL(b0 + 1, b0), LDS_, blkI(b0, b0), LDS_, lane, false);
+        st16(XS + 256 * w, 16, acc, lane, 1.f);
+        __syncwarp();
+        mm16(acc, blkI(b0 + 1, b0 + 1), LDS_, XS + 256 * w, 16, lane, false);
+        st16(blkI(b0 + 1, b0), LDS_, acc, lane, -1.f);
     }
+    __syncthreads();
+    // (3) X = L_[23][01] D_[01]:  X_i0 = L_{2+i,0} D0 + L_{2+i,1} INV_10,  X_i1 = L_{2+i,1} D1   (warps 0-3)
+    if (w < 4) {
+        const int xi = w >> 1, xj = w & 1;
+        float acc[8];
+        if (xj == 0) {
+            mm16(acc, blkL(2 + xi, 0), LDS_, blkI(0, 0), LDS_, lane, false);
+            mm16(acc, blkL(2 + xi, 1), LDS_, blkI(1, 0), LDS_, lane, true);
+        } else {
+            mm16(acc, blkL(2 + xi, 1), LDS_, blkI(1, 1), LDS_, lane, false);
+        }
+        st16(XS + 256 * w, 16, acc, lane, 1.f);
+    }
+    __syncthreads();
+    // (4) INV_[23][01] = -D_[23] X:  Y_0j = D2 X_0j,  Y_1j = INV_32 X_0j + D3 X_1j   (warps 0-3)
+    if (w < 4) {
+        const int yi = w >> 1, yj = w & 1;
+        float acc[8];
+        if (yi == 0) {
+            mm16(acc, blkI(2, 2), LDS_, XS + 256 * yj, 16, lane, false);
+        } else {
+            mm16(acc, blkI(3, 2), LDS_, XS + 256 * yj, 16, lane, false);
+            mm16(acc, blkI(3, 3), LDS_, XS + 256 * (2 + yj), 16, lane, true);
+        }
+        st16(blkI(2 + yi, yj), LDS_, acc, lane, -1.f);
+    }
+    __syncthreads();
     // INV Diag(beta) -> K-major A operand as high + low bf16 parts
 #pragma unroll
     for (int it = 0; it < 2; ++it) {
@@ -481,7 +527,24 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
 }
 
 // ============================================================== chain (a4, a5)
-__global__ void __launch_bounds__(128, 1)
+// Warp roles (NT = 64 columns of d_v per CTA):
+//   warps 0-7  conversion warps; warp w reads TMEM lanes 32 (w % 4) .. +31 and
+//              columns 32 (w / 4) .. +31 of each 64-wide TMEM tile.
+//              - all 8: S_in -> bf16 operand, S <- Diag(a_last) S_in   (chunk c)
+//              - lanes 64..127 (warps 2, 3, 6, 7): U = U0 - W S_in     (chunk c)
+//              - lanes 0..63   (warps 0, 1, 4, 5): O rows              (chunk c - 1)
+//   warp 8     lane 0 issues every MMA and bulk copy.
+// MMA order per chunk: P[c&1] = [Q_decay; W] S_in -> commit(p);
+// S += K_restore^T U -> commit(s); P[c&1] += M_qk U -> commit(o).  The O
+// product and the O stores run while the next chunk's state is converted.
+constexpr int K2_THREADS = 288;
+constexpr int K2_ISSUER_WARP = 8;
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__global__ void __launch_bounds__(K2_THREADS, 1)
 kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, int nch_per_seq,
              const uint8_t* __restrict__ ws_blocks, const float* __restrict__ S0, int H,
              bf16* __restrict__ O, float* __restrict__ S_final, int* status) {
@@ -495,26 +558,33 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         const int4 si = seq_info[n];
         bos = si.x; len = si.y; first = si.z; nch = si.w;
     }
-    const int tid = threadIdx.x, w = tid >> 5;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + K2_BAR);
-    uint64_t* mbar = full + K2_NS;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + K2_NS + 1);
+    uint64_t* bar_p = full + K2_NS;
+    uint64_t* bar_s = bar_p + 1;
+    uint64_t* bar_o = bar_p + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_p + 3);
     if (w == 0) {
         kda::tmem_alloc(tmem_slot, K2_TMEM_COLS);
         kda::tmem_relinquish();
     }
     if (tid == 0) {
         for (int s = 0; s < K2_NS; ++s) kda::mbar_init(full + s, 1);
-        kda::mbar_init(mbar, 1);
+        kda::mbar_init(bar_p, 1);
+        kda::mbar_init(bar_s, 1);
+        kda::mbar_init(bar_o, 1);
         kda::fence_barrier_init();
     }
     kda::tc_fence_before();
     __syncthreads();
     kda::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_off = (uint32_t)(32 * w) << 16;
-    const uint32_t tS = tmem + lane_off, tP = tmem + lane_off + 64;
-    const int i = tid;                          // TMEM lane = state row (key channel)
+    const bool issuer = (w == K2_ISSUER_WARP);
+    const int quad = w & 3, half = (w >> 2) & 1;
+    const int row = 32 * quad + lane;                       // TMEM lane = state row / P row
+    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+    const uint32_t tS = tmem + lane_off + 32 * half;        // this warp's 32 state columns
+    const uint32_t tP0 = tmem + lane_off + 64 + 32 * half;  // P buffer 0 (P buffer 1 at +64)
 
     auto issue = [&](int c) {
         const int st = c % K2_NS;
@@ -527,154 +597,171 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         kda::bulk_g2s(stage + ST_U0, src + WS_U0 + (uint32_t)tile * C * NT * 4, C * NT * 4, full + st);
         kda::bulk_g2s(stage + ST_AL, src + WS_AL, DK * 4, full + st);
     };
+    auto wait = [&](uint64_t* b, uint32_t parity) {
+        if (!kda::mbar_wait(b, parity, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+    };
 
-    // initial state slice -> TMEM
-    {
-        float s[64];
+    // initial state slice -> TMEM; first stages in flight
+    if (!issuer) {
+        float s[32];
         if (S0) {
-            const float4* src = reinterpret_cast<const float4*>(S0 + (((size_t)n * H + h) * DK + i) * DV + tile * NT);
+            const float4* src =
+                reinterpret_cast<const float4*>(S0 + (((size_t)n * H + h) * DK + row) * DV + tile * NT + 32 * half);
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const float4 x = src[u];
                 s[4 * u] = x.x; s[4 * u + 1] = x.y; s[4 * u + 2] = x.z; s[4 * u + 3] = x.w;
             }
         } else {
 #pragma unroll
-            for (int u = 0; u < 64; ++u) s[u] = 0.f;
+            for (int u = 0; u < 32; ++u) s[u] = 0.f;
         }
         kda::tmem_st32(tS, s);
-        kda::tmem_st32(tS + 32, s + 32);
         kda::tmem_wait_st();
-    }
-    if (tid == 0)
+    } else if (lane == 0) {
         for (int c = 0; c < min(K2_NS, nch); ++c) issue(c);
+    }
     kda::tc_fence_before();
     __syncthreads();
     kda::tc_fence_after();
 
     const uint32_t sSB = kda::smem_u32(sm + K2_SB), sUB = kda::smem_u32(sm + K2_UB);
     const uint32_t sUBL = kda::smem_u32(sm + K2_UBL);
-    uint32_t mma_phase = 0;
+    auto o_epilogue = [&](int c) {                          // warps 0, 1, 4, 5: rows 0..63
+        wait(bar_o, (uint32_t)(c & 1));
+        kda::tc_fence_after();
+        float o[32];
+        kda::tmem_ld32(tP0 + 64 * (c & 1), o);
+        kda::tmem_wait_ld();
+        if (row < len - c * C) {
+            uint4* dst = reinterpret_cast<uint4*>(O + ((size_t)(bos + c * C + row) * H + h) * DV + tile * NT +
+                                                  32 * half);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) dst[cc] = pack8(o + 8 * cc);
+        }
+    };
+
     for (int c = 0; c < nch; ++c) {
         const int st = c % K2_NS;
         uint8_t* stage = sm + st * K2_STAGE;
-        if (!kda::mbar_wait(full + st, (uint32_t)((c / K2_NS) & 1), kda::kWaitCycles))
-            kda::record_status(status, kda::kDevTimeout);
-
-        // S_in -> bf16 operand; TMEM state <- Diag(a_last) S_in
-        {
-            float s[64];
+        if (!issuer) {
+            // ---- S_in -> bf16 operand; TMEM state <- Diag(a_last) S_in
+            wait(full + st, (uint32_t)((c / K2_NS) & 1));
+            if (c > 0) wait(bar_s, (uint32_t)((c - 1) & 1));
+            kda::tc_fence_after();
+            float s[32];
             kda::tmem_ld32(tS, s);
-            kda::tmem_ld32(tS + 32, s + 32);
             kda::tmem_wait_ld();
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-                *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(i, 8 * cc, 128)) = pack8(s + 8 * cc);
-            const float al = reinterpret_cast<const float*>(stage + ST_AL)[i];
+            for (int cc = 0; cc < 4; ++cc)
+                *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(row, 32 * half + 8 * cc, 128)) = pack8(s + 8 * cc);
+            const float al = reinterpret_cast<const float*>(stage + ST_AL)[row];
 #pragma unroll
-            for (int u = 0; u < 64; ++u) s[u] *= al;
+            for (int u = 0; u < 32; ++u) s[u] *= al;
             kda::tmem_st32(tS, s);
-            kda::tmem_st32(tS + 32, s + 32);
             kda::tmem_wait_st();
-        }
-        kda::fence_proxy_async_smem();
-        kda::tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {                         // P = [Q_decay; W] S_in
-            kda::tc_fence_after();
-            const uint32_t sA1 = kda::smem_u32(stage + ST_A1);
-            const uint32_t idesc = kda::idesc_bf16(128, NT, 0, 1);
+            kda::fence_proxy_async_smem();
+            kda::tc_fence_before();
+            named_bar_sync(1, K2_THREADS);
+            if (quad >= 2) {
+                // ---- U = U0 - W S_in -> high + low bf16 operands (rows 64..127 of P)
+                const int r = row - 64;
+                wait(bar_p, (uint32_t)(c & 1));
+                kda::tc_fence_after();
+                float pw[32];
+                kda::tmem_ld32(tP0 + 64 * (c & 1), pw);
+                kda::tmem_wait_ld();
+                const float4* u0 = reinterpret_cast<const float4*>(stage + ST_U0 + (r * NT + 32 * half) * 4);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint64_t ad = kda::sw128_desc(sA1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
-                const uint64_t bd = kda::sw128_desc(sSB + s * 2048, 16384, 1024);
-                kda::umma_bf16(tmem + 64, ad, bd, idesc, s > 0 ? 1u : 0u);
+                for (int cc = 0; cc < 4; ++cc) {
+                    const float4 x0 = u0[2 * cc], x1 = u0[2 * cc + 1];
+                    float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w}, lo[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) f[u] -= pw[8 * cc + u];
+                    split8(f, lo);
+                    const uint32_t off = kda::sw128(r, 32 * half + 8 * cc, 64);
+                    *reinterpret_cast<uint4*>(sm + K2_UB + off) = pack8(f);
+                    *reinterpret_cast<uint4*>(sm + K2_UBL + off) = pack8(lo);
+                }
+                kda::fence_proxy_async_smem();
+                kda::tc_fence_before();
+            } else if (c > 0) {
+                o_epilogue(c - 1);                          // overlaps the U conversion
+                kda::tc_fence_before();
             }
-            kda::umma_commit(mbar);
-        }
-        if (!kda::mbar_wait(mbar, mma_phase, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
-        mma_phase ^= 1;
-        kda::tc_fence_after();
-
-        if (w >= 2) {                            // U = U0 - W S_in -> high + low bf16 operands
-            const int r = tid - 64;
-            float pw[64];
-            kda::tmem_ld32(tP, pw);
-            kda::tmem_ld32(tP + 32, pw + 32);
-            kda::tmem_wait_ld();
-            const float4* u0 = reinterpret_cast<const float4*>(stage + ST_U0 + r * NT * 4);
+            // all conversion warps: the O warps must have waited for bar_o(c - 1)
+            // before bar_o(c) can be committed (a parity wait cannot skip a phase)
+            named_bar_sync(2, K2_THREADS);
+        } else {
+            named_bar_sync(1, K2_THREADS);
+            if (lane == 0) {                                // P = [Q_decay; W] S_in
+                wait(full + st, (uint32_t)((c / K2_NS) & 1));
+                kda::tc_fence_after();
+                const uint32_t sA1 = kda::smem_u32(stage + ST_A1);
+                const uint32_t idesc = kda::idesc_bf16(128, NT, 0, 1);
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                const float4 x0 = u0[2 * cc], x1 = u0[2 * cc + 1];
-                float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w}, lo[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) f[u] -= pw[8 * cc + u];
-                split8(f, lo);
-                *reinterpret_cast<uint4*>(sm + K2_UB + kda::sw128(r, 8 * cc, 64)) = pack8(f);
-                *reinterpret_cast<uint4*>(sm + K2_UBL + kda::sw128(r, 8 * cc, 64)) = pack8(lo);
-            }
-        }
-        kda::fence_proxy_async_smem();
-        kda::tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            kda::tc_fence_after();
-            const uint32_t sKR = kda::smem_u32(stage + ST_KR);
-            const uint32_t sMQ = kda::smem_u32(stage + ST_MQ), sMQL = kda::smem_u32(stage + ST_MQL);
-            const uint32_t id_s = kda::idesc_bf16(128, NT, 1, 1);
-            const uint32_t id_o = kda::idesc_bf16(128, NT, 0, 1);
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {   // S += K_restore^T (U_hi + U_lo)
-                const uint32_t sU = part ? sUBL : sUB;
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t ad = kda::sw128_desc(sKR + s * 2048, 8192, 1024);
-                    const uint64_t bd = kda::sw128_desc(sU + s * 2048, 8192, 1024);
-                    kda::umma_bf16(tmem, ad, bd, id_s, 1u);
+                for (int s = 0; s < 8; ++s) {
+                    const uint64_t ad = kda::sw128_desc(sA1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+                    const uint64_t bd = kda::sw128_desc(sSB + s * 2048, 16384, 1024);
+                    kda::umma_bf16(tmem + 64 + 64 * (c & 1), ad, bd, idesc, s > 0 ? 1u : 0u);
+                }
+                kda::umma_commit(bar_p);
+                // the previous chunk's stage is free once its last MMA (the O product) is done
+                if (c >= 1) {
+                    wait(bar_o, (uint32_t)((c - 1) & 1));
+                    if (c - 1 + K2_NS < nch) issue(c - 1 + K2_NS);
                 }
             }
+            __syncwarp();
+            named_bar_sync(2, K2_THREADS);
+            if (lane == 0) {
+                kda::tc_fence_after();
+                const uint32_t sKR = kda::smem_u32(stage + ST_KR);
+                const uint32_t sMQ = kda::smem_u32(stage + ST_MQ), sMQL = kda::smem_u32(stage + ST_MQL);
+                const uint32_t id_s = kda::idesc_bf16(128, NT, 1, 1);
+                const uint32_t id_o = kda::idesc_bf16(128, NT, 0, 1);
 #pragma unroll
-            for (int part = 0; part < 3; ++part) {   // P_q += M_hi U_hi + M_hi U_lo + M_lo U_hi
-                const uint32_t sA = part == 2 ? sMQL : sMQ;
-                const uint32_t sU = part == 1 ? sUBL : sUB;
+                for (int part = 0; part < 2; ++part) {      // S += K_restore^T (U_hi + U_lo)
+                    const uint32_t sU = part ? sUBL : sUB;
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t ad = kda::sw128_desc(sA + s * 32, 16, 1024);
-                    const uint64_t bd = kda::sw128_desc(sU + s * 2048, 8192, 1024);
-                    kda::umma_bf16(tmem + 64, ad, bd, id_o, 1u);
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t ad = kda::sw128_desc(sKR + s * 2048, 8192, 1024);
+                        const uint64_t bd = kda::sw128_desc(sU + s * 2048, 8192, 1024);
+                        kda::umma_bf16(tmem, ad, bd, id_s, 1u);
+                    }
                 }
-            }
-            kda::umma_commit(mbar);
-        }
-        if (!kda::mbar_wait(mbar, mma_phase, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
-        mma_phase ^= 1;
-        kda::tc_fence_after();
-        if (tid == 0 && c + K2_NS < nch) issue(c + K2_NS);   // this stage is free again
-
-        if (w < 2) {                             // O rows of this chunk
-            const int r = tid;
-            float o[64];
-            kda::tmem_ld32(tP, o);
-            kda::tmem_ld32(tP + 32, o + 32);
-            kda::tmem_wait_ld();
-            if (r < len - c * C) {
-                uint4* dst = reinterpret_cast<uint4*>(O + ((size_t)(bos + c * C + r) * H + h) * DV + tile * NT);
+                kda::umma_commit(bar_s);
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) dst[cc] = pack8(o + 8 * cc);
+                for (int part = 0; part < 3; ++part) {      // P_q += M_hi U_hi + M_hi U_lo + M_lo U_hi
+                    const uint32_t sA = part == 2 ? sMQL : sMQ;
+                    const uint32_t sU = part == 1 ? sUBL : sUB;
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        const uint64_t ad = kda::sw128_desc(sA + s * 32, 16, 1024);
+                        const uint64_t bd = kda::sw128_desc(sU + s * 2048, 8192, 1024);
+                        kda::umma_bf16(tmem + 64 + 64 * (c & 1), ad, bd, id_o, 1u);
+                    }
+                }
+                kda::umma_commit(bar_o);
             }
+            __syncwarp();
         }
-        kda::tc_fence_before();
     }
-    __syncthreads();
-    kda::tc_fence_after();
-    if (S_final) {
-        float s[64];
-        kda::tmem_ld32(tS, s);
-        kda::tmem_ld32(tS + 32, s + 32);
-        kda::tmem_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(S_final + (((size_t)n * H + h) * DK + i) * DV + tile * NT);
+    if (!issuer) {
+        if (quad < 2 && nch > 0) {
+            o_epilogue(nch - 1);
+        }
+        if (nch > 0) wait(bar_s, (uint32_t)((nch - 1) & 1));
+        kda::tc_fence_after();
+        if (S_final) {
+            float s[32];
+            kda::tmem_ld32(tS, s);
+            kda::tmem_wait_ld();
+            float4* dst = reinterpret_cast<float4*>(S_final + (((size_t)n * H + h) * DK + row) * DV + tile * NT +
+                                                    32 * half);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) dst[u] = make_float4(s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]);
+            for (int u = 0; u < 8; ++u) dst[u] = make_float4(s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]);
+        }
     }
     kda::tc_fence_before();
     __syncthreads();
@@ -736,7 +823,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         if (e != cudaSuccess) return e;
         trace_mark(a.stream);
     }
-    kda_tc_chain<<<dim3(NTILES * a.n_seq, a.H), 128, chain_smem, a.stream>>>(
+    kda_tc_chain<<<dim3(NTILES * a.n_seq, a.H), K2_THREADS, chain_smem, a.stream>>>(
         seq_info, use_table, fixed_len, nch_per, blocks, a.S0, a.H, static_cast<bf16*>(a.O), a.S_final,
         a.status);
     e = cudaGetLastError();
