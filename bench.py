@@ -104,12 +104,19 @@ def dist_env():
 
 
 def barrier_max(t, world, device):
+    """Max of a per-rank time over all ranks (the job is as slow as its slowest replica)."""
     if world == 1:
         return t
     import torch.distributed as dist
     x = torch.tensor([t], dtype=torch.float64, device=device)
     dist.all_reduce(x, op=dist.ReduceOp.MAX)
     return float(x.item())
+
+
+def replica_throughput(units_per_rank, steps, world, max_ms):
+    """Whole-job throughput of N independent replicas: every rank processes
+    units_per_rank units per step; the job takes the slowest rank's time."""
+    return units_per_rank * world * steps / (max_ms / 1e3)
 
 
 def sync_barrier(world):
@@ -286,7 +293,7 @@ def run_gpu(args):
     e2e_steps = max(3, args.steps // 4)
 
     tok_per_step = T * world
-    value = tok_per_step * args.steps / (ms / 1e3)
+    value = replica_throughput(T, args.steps, world, ms)
     ms_step = ms / args.steps
     # roofline of the dominant prefill kernel (compulsory bytes that kernel moves)
     prep_bytes = T * H * (3 * 256 + 512 + 4)               # q, k, v, log_alpha, beta read once
@@ -313,13 +320,13 @@ def run_gpu(args):
                           "frac": step_bytes / (ms_step / 1e3) / 1e9 / hbm,
                           "tflops": T * H * FLOPS_TOKEN_HEAD / (ms_step / 1e3) / 1e12,
                           "kernel_ms": {"kda_tc_prep": prep_ms, "kda_tc_chain": chain_ms}},
-        "decode": {"workload": DECODE, "value": dsteps * world / (dms / 1e3), "unit": "steps/s",
+        "decode": {"workload": DECODE, "value": replica_throughput(1, dsteps, world, dms), "unit": "steps/s",
                    "steps": dsteps, "ms_per_step": dec_ms_step,
                    "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": dec_achieved,
                                 "peak": hbm, "unit": "GB/s", "frac": dec_achieved / hbm, "traffic": None,
                                 "bytes_per_launch": dec_bytes_step},
                    "l2": "fp32 state 537 MB > L2; fresh token set per step"},
-        "e2e": {"value": tok_per_step * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": replica_throughput(T, e2e_steps, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * world,
         "clocks": clk.summary(),
