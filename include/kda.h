@@ -28,7 +28,10 @@
  *     allocates device memory and never synchronises the stream, except in
  *     kda_get_last_device_status.
  *   - Work is enqueued on `stream` (0 = the legacy default stream).  A call
- *     returns once the work is enqueued.
+ *     returns once the work is enqueued.  A long tensor-core prefill forks
+ *     part of its work onto an internal high-priority stream of the library
+ *     (created once per device, kept until exit) and joins it back into
+ *     `stream` with events before returning, so ordering on `stream` holds.
  *   - Arguments are checked before anything is launched; a failed check
  *     returns an error and launches nothing.  A launch failure returns
  *     KDA_ERR_CUDA.  Faults detected inside a kernel (a wait that ran out of
@@ -178,9 +181,11 @@ KDA_API kda_status kda_get_last_device_status(cudaStream_t stream);
  * Tracing hook.  While set, every kda_prefill / kda_decode call made from the
  * calling host thread records the given CUDA events (cudaEvent_t handles,
  * created by the caller) on its stream at the boundaries between the kernels
- * it launches: event 0 before the first kernel, event i after the i-th kernel
- * (the tensor-core prefill launches [table builder,] chunk prep, state pass;
- * the CUDA-core prefill and the decode launch one kernel).  Events beyond
+ * it launches, all on the caller's stream: event 0 before the first kernel;
+ * for the tensor-core prefill, event 1 once every chunk-prep kernel has run
+ * and event 2 when the state pass (which may run partly on an internal
+ * stream, overlapped with later chunk preps) has joined back; for the
+ * CUDA-core prefill and the decode, event 1 after their one kernel.  Events beyond
  * n_events are skipped.  Pass (NULL, 0) to stop.  Returns KDA_ERR_INVALID_ARG
  * for n_events < 0 or a NULL array with n_events > 0.  The array must stay
  * valid while the hook is set.  This exists so that a benchmark can time each

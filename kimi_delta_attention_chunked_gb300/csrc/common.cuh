@@ -56,6 +56,7 @@ struct PrefillArgs {
     const int32_t* cu_seqlens;   // device, or nullptr (equal lengths)
     int n_seq, T_total, H, dk, dv, chunk;
     int total_chunks;            // exact when the host knows cu_seqlens, else an upper bound
+    int max_chunks;              // chunks of the longest sequence (host-known lengths), else 0
     kda_dtype dtype;
     void* O;
     float* S_final;

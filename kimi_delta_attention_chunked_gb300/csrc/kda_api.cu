@@ -3,6 +3,7 @@
 // Nothing here computes any part of KDA; it validates the call, chooses the
 // kernel for the (dtype, d_k, d_v, chunk) combination and enqueues it on the
 // caller's stream.  See include/kda.h for the contract of each entry point.
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 
@@ -86,7 +87,7 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
         if (cu_seqlens_host) return KDA_ERR_INVALID_ARG;       // host copy of nothing
         if (T_total % n_seq != 0) return KDA_ERR_INVALID_ARG;
     }
-    int total_chunks = 0;
+    int total_chunks = 0, max_chunks = 0;
     if (cu_seqlens_host) {
         if (cu_seqlens_host[0] != 0 || cu_seqlens_host[n_seq] != T_total) return KDA_ERR_INVALID_ARG;
         long long tc = 0;
@@ -94,6 +95,7 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
             const int len = cu_seqlens_host[n + 1] - cu_seqlens_host[n];
             if (len < 0) return KDA_ERR_INVALID_ARG;
             tc += (len + chunk - 1) / chunk;
+            max_chunks = std::max(max_chunks, (len + chunk - 1) / chunk);
         }
         total_chunks = (int)tc;
     } else if (!cu_seqlens) {
@@ -111,7 +113,8 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
     kda_host::PrefillArgs a{};
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.S0 = S0;
     a.cu_seqlens = cu_seqlens; a.n_seq = n_seq; a.T_total = T_total; a.H = H; a.dk = dk;
-    a.dv = dv; a.chunk = chunk; a.total_chunks = total_chunks; a.dtype = dtype; a.O = O;
+    a.dv = dv; a.chunk = chunk; a.total_chunks = total_chunks; a.max_chunks = max_chunks; a.dtype = dtype;
+    a.O = O;
     a.S_final = S_final; a.workspace = workspace; a.workspace_bytes = workspace_bytes;
     a.stream = stream;
 

@@ -45,6 +45,9 @@
 //
 // Every wait on an asynchronous event is bounded; a wait that runs out records
 // KDA_ERR_TIMEOUT in the status word and the kernel runs to completion.
+#include <algorithm>
+#include <mutex>
+
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -240,18 +243,26 @@ __global__ void __launch_bounds__(256, 2)
 kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
             const float* __restrict__ g, const float* __restrict__ beta, int H, int use_table,
             int fixed_len, int nch_per_seq, const int4* __restrict__ chunk_info,
+            const int4* __restrict__ seq_info, int j_begin, int j_count,
             uint8_t* __restrict__ ws_blocks, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
-    const int slot = blockIdx.x, h = blockIdx.y;
-    int tok0, nrows;
+    // this launch covers chunks j_begin .. j_begin + j_count - 1 of every sequence:
+    // equal lengths -> grid.x = n_seq * j_count; chunk table -> grid.x = chunk slots
+    const int h = blockIdx.y;
+    int tok0, nrows, slot;
     if (!use_table) {
-        const int n = slot / nch_per_seq, j = slot % nch_per_seq;
+        const int n = blockIdx.x / j_count, j = j_begin + blockIdx.x % j_count;
+        if (j >= nch_per_seq) return;
+        slot = n * nch_per_seq + j;
         tok0 = n * fixed_len + j * C;
         nrows = min(C, fixed_len - j * C);
     } else {
+        slot = blockIdx.x;
         const int4 ci = chunk_info[slot];
         if (ci.z < 0) return;
+        const int j = slot - seq_info[ci.z].z;
+        if (j < j_begin || j >= j_begin + j_count) return;
         tok0 = ci.x;
         nrows = ci.y;
     }
@@ -546,7 +557,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 
 __global__ void __launch_bounds__(K2_THREADS, 1)
 kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, int nch_per_seq,
-             const uint8_t* __restrict__ ws_blocks, const float* __restrict__ S0, int H,
+             int c_begin, int c_end, const uint8_t* __restrict__ ws_blocks, const float* __restrict__ S0, int H,
              bf16* __restrict__ O, float* __restrict__ S_final, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
@@ -558,6 +569,10 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         const int4 si = seq_info[n];
         bos = si.x; len = si.y; first = si.z; nch = si.w;
     }
+    // this launch runs chunks [c_begin, c_end) of the sequence; locally they are
+    // numbered 0 .. nloc - 1 (stage and barrier parities use the local number)
+    const int cb = min(c_begin, nch);
+    const int nloc = max(0, min(c_end, nch) - cb);
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + K2_BAR);
     uint64_t* bar_p = full + K2_NS;
@@ -589,7 +604,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     auto issue = [&](int c) {
         const int st = c % K2_NS;
         uint8_t* stage = sm + st * K2_STAGE;
-        const uint8_t* src = ws_blocks + ((size_t)(first + c) * H + h) * WS_BLOCK;
+        const uint8_t* src = ws_blocks + ((size_t)(first + cb + c) * H + h) * WS_BLOCK;
         kda::mbar_arrive_expect_tx(full + st, COPY_BYTES);
         kda::bulk_g2s(stage + ST_A1, src + WS_A1, 32768, full + st);
         kda::bulk_g2s(stage + ST_KR, src + WS_KR, 16384, full + st);
@@ -619,7 +634,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         kda::tmem_st32(tS, s);
         kda::tmem_wait_st();
     } else if (lane == 0) {
-        for (int c = 0; c < min(K2_NS, nch); ++c) issue(c);
+        for (int c = 0; c < min(K2_NS, nloc); ++c) issue(c);
     }
     kda::tc_fence_before();
     __syncthreads();
@@ -633,15 +648,15 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         float o[32];
         kda::tmem_ld32(tP0 + 64 * (c & 1), o);
         kda::tmem_wait_ld();
-        if (row < len - c * C) {
-            uint4* dst = reinterpret_cast<uint4*>(O + ((size_t)(bos + c * C + row) * H + h) * DV + tile * NT +
+        if (row < len - (cb + c) * C) {
+            uint4* dst = reinterpret_cast<uint4*>(O + ((size_t)(bos + (cb + c) * C + row) * H + h) * DV + tile * NT +
                                                   32 * half);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) dst[cc] = pack8(o + 8 * cc);
         }
     };
 
-    for (int c = 0; c < nch; ++c) {
+    for (int c = 0; c < nloc; ++c) {
         const int st = c % K2_NS;
         uint8_t* stage = sm + st * K2_STAGE;
         if (!issuer) {
@@ -709,7 +724,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 // the previous chunk's stage is free once its last MMA (the O product) is done
                 if (c >= 1) {
                     wait(bar_o, (uint32_t)((c - 1) & 1));
-                    if (c - 1 + K2_NS < nch) issue(c - 1 + K2_NS);
+                    if (c - 1 + K2_NS < nloc) issue(c - 1 + K2_NS);
                 }
             }
             __syncwarp();
@@ -748,10 +763,10 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         }
     }
     if (!issuer) {
-        if (quad < 2 && nch > 0) {
-            o_epilogue(nch - 1);
+        if (quad < 2 && nloc > 0) {
+            o_epilogue(nloc - 1);
         }
-        if (nch > 0) wait(bar_s, (uint32_t)((nch - 1) & 1));
+        if (nloc > 0) wait(bar_s, (uint32_t)((nloc - 1) & 1));
         kda::tc_fence_after();
         if (S_final) {
             float s[32];
@@ -773,7 +788,45 @@ size_t header_bytes(int n_seq, long long slots) {
     return (raw + 1023) & ~size_t(1023);
 }
 
+size_t state_bytes(int n_seq, int H) { return (size_t)n_seq * H * DK * DV * sizeof(float); }
+
 long long slot_bound(int n_seq, int T_total) { return (long long)T_total / C + n_seq; }
+
+// ---- stream overlap: the prep of a later slice of chunks runs while the
+// state pass works through the previous slice.  Per device: one
+// high-priority stream for the state pass and a pool of events, created on
+// first use and kept for the life of the process.
+constexpr int kMaxSlices = 8;
+constexpr int kMaxDevices = 64;
+struct OverlapRes {
+    cudaStream_t chain = nullptr;
+    cudaEvent_t ev[kMaxSlices + 2] = {};
+    bool ok = false;
+};
+std::mutex g_overlap_mutex;
+OverlapRes g_overlap[kMaxDevices];
+
+cudaError_t overlap_resources(OverlapRes** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorNotSupported;
+    OverlapRes& r = g_overlap[dev];
+    if (!r.ok) {
+        int lo = 0, hi = 0;
+        e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+        if (e != cudaSuccess) return e;
+        e = cudaStreamCreateWithPriority(&r.chain, cudaStreamNonBlocking, hi);
+        if (e != cudaSuccess) return e;
+        for (auto& ev : r.ev) {
+            e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) return e;
+        }
+        r.ok = true;
+    }
+    *out = &r;
+    return cudaSuccess;
+}
 
 }  // namespace
 
@@ -786,7 +839,7 @@ bool tc_supported(int dk, int dv, int chunk, kda_dtype dt) {
 size_t tc_workspace_bytes(int n_seq, int T_total, int H, int chunk) {
     (void)chunk;
     const long long ub = slot_bound(n_seq, T_total);
-    return header_bytes(n_seq, ub) + (size_t)ub * H * WS_BLOCK;
+    return header_bytes(n_seq, ub) + state_bytes(n_seq, H) + (size_t)ub * H * WS_BLOCK;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a) {
@@ -795,19 +848,33 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     int4* chunk_info = reinterpret_cast<int4*>(ws);
     int4* seq_info = reinterpret_cast<int4*>(ws + 16 * (size_t)ub);
-    uint8_t* blocks = ws + header_bytes(a.n_seq, ub);
+    float* S_mid = reinterpret_cast<float*>(ws + header_bytes(a.n_seq, ub));
+    uint8_t* blocks = ws + header_bytes(a.n_seq, ub) + state_bytes(a.n_seq, a.H);
 
     // Equal-length batches map chunks to sequences arithmetically; packed
     // varlen batches go through the chunk table built on the device.
     const int use_table = a.cu_seqlens != nullptr;
     const int fixed_len = use_table ? 0 : a.T_total / a.n_seq;
     const int nch_per = use_table ? 0 : (fixed_len + C - 1) / C;
+    // longest sequence in chunks (the device-only cu_seqlens case is not sliced)
+    const int max_chunks = use_table ? (a.max_chunks > 0 ? a.max_chunks : (int)min(ub, (long long)INT32_MAX))
+                                     : nch_per;
+    // Overlap only pays when the state pass is the long pole, i.e. when its
+    // CTAs leave most SMs to the chunk preps (few sequences x heads).
+    int dev = 0, n_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) !=
+                                                   cudaSuccess)
+        return cudaGetLastError();
+    const long long chain_ctas = (long long)NTILES * a.n_seq * a.H;
+    const bool overlap = chain_ctas * 4 <= n_sm && !(use_table && a.max_chunks <= 0);
+    const int n_slices = overlap ? std::max(1, std::min(kMaxSlices, max_chunks / 16)) : 1;
+    const int slice = n_slices > 1 ? (max_chunks + n_slices - 1) / n_slices : max_chunks;
+
     if (use_table) {
         kda_tc_schedule<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.n_seq, a.T_total, (int)ub, chunk_info,
                                                   seq_info, a.status);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        trace_mark(a.stream);
     }
     const int prep_smem = (int)(K1_BYTES + 1024);
     const int chain_smem = (int)(K2_BYTES + 1024);
@@ -815,20 +882,52 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kda_tc_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
     if (e != cudaSuccess) return e;
-    if (a.total_chunks > 0) {
-        kda_tc_prep<<<dim3(a.total_chunks, a.H), 256, prep_smem, a.stream>>>(
+
+    auto prep = [&](int j0, int jn, cudaStream_t st) {
+        if (jn <= 0 || a.total_chunks <= 0) return cudaSuccess;
+        const unsigned gx = use_table ? (unsigned)a.total_chunks : (unsigned)(a.n_seq * jn);
+        kda_tc_prep<<<dim3(gx, a.H), 256, prep_smem, st>>>(
             static_cast<const bf16*>(a.q), static_cast<const bf16*>(a.k), static_cast<const bf16*>(a.v),
-            a.log_alpha, a.beta, a.H, use_table, fixed_len, nch_per, chunk_info, blocks, a.status);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+            a.log_alpha, a.beta, a.H, use_table, fixed_len, nch_per, chunk_info, seq_info, j0, jn, blocks,
+            a.status);
+        return cudaGetLastError();
+    };
+    auto chain = [&](int c0, int c1, const float* s_in, float* s_out, cudaStream_t st) {
+        kda_tc_chain<<<dim3(NTILES * a.n_seq, a.H), K2_THREADS, chain_smem, st>>>(
+            seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
+            a.status);
+        return cudaGetLastError();
+    };
+
+    if (n_slices == 1) {
+        if ((e = prep(0, max_chunks, a.stream)) != cudaSuccess) return e;
         trace_mark(a.stream);
+        if ((e = chain(0, max_chunks, a.S0, a.S_final, a.stream)) != cudaSuccess) return e;
+        trace_mark(a.stream);
+        return cudaSuccess;
     }
-    kda_tc_chain<<<dim3(NTILES * a.n_seq, a.H), K2_THREADS, chain_smem, a.stream>>>(
-        seq_info, use_table, fixed_len, nch_per, blocks, a.S0, a.H, static_cast<bf16*>(a.O), a.S_final,
-        a.status);
-    e = cudaGetLastError();
+    // prep slices on the caller's stream, state-pass slices on the internal
+    // stream, slice k of the state pass waiting for slice k of the prep; the
+    // state is carried between slices in S_mid; the caller's stream joins at the end.
+    std::lock_guard<std::mutex> lock(g_overlap_mutex);
+    OverlapRes* r = nullptr;
+    if ((e = overlap_resources(&r)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(r->ev[n_slices], a.stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(r->chain, r->ev[n_slices], 0)) != cudaSuccess) return e;
+    for (int k = 0; k < n_slices; ++k) {
+        const int c0 = k * slice, c1 = std::min(max_chunks, (k + 1) * slice);
+        if ((e = prep(c0, c1 - c0, a.stream)) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(r->ev[k], a.stream)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(r->chain, r->ev[k], 0)) != cudaSuccess) return e;
+        const bool last = (k == n_slices - 1);
+        if ((e = chain(c0, c1, k == 0 ? a.S0 : S_mid, last ? a.S_final : S_mid, r->chain)) != cudaSuccess)
+            return e;
+    }
+    trace_mark(a.stream);                       // every prep slice enqueued
+    if ((e = cudaEventRecord(r->ev[n_slices + 1], r->chain)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(a.stream, r->ev[n_slices + 1], 0)) != cudaSuccess) return e;
     trace_mark(a.stream);
-    return e;
+    return cudaSuccess;
 }
 
 }  // namespace kda_host

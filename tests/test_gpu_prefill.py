@@ -126,6 +126,16 @@ def test_tc_split_prefill_equals_one_prefill():
     assert rel_err(S2, Sf.double().cpu().numpy()) < 5e-3
 
 
+def test_tc_overlapped_slices_few_heads():
+    """Few chains and many chunks: the prep of later chunk slices overlaps the
+    state pass of earlier ones (two streams); the state crosses slice borders."""
+    dev = need_gpu()
+    w = inputs.Workload("tc", "prefill", H=2, dk=128, dv=128, dtype=torch.bfloat16, chunk=64, s0_std=0.02)
+    for lengths in ([64 * 64], [64 * 40 + 17, 3000]):
+        _, _, _, eo, es = run_case(w, dev, lengths=lengths, seed=15)
+        assert eo <= 5e-3 and es <= 5e-3, (lengths, eo, es)
+
+
 # ------------------------------------------------------------- full-size workloads
 def test_full_prefill_8k():
     """B=1, H=32, T=8192, d=128, chunk 64, bf16: every output vs the oracle."""
