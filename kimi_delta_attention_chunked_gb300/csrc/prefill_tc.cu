@@ -123,36 +123,63 @@ __device__ __forceinline__ void split8(float* x, float* lo) {
 }
 
 // One warp: acc (+)= A * B for 16x16 fp32 blocks in shared memory (row-major,
-// leading dimensions lda / ldb).  Lane l owns row l / 2, columns 8 (l % 2) .. +7.
+// leading dimensions lda / ldb), on the tensor cores with mma.sync m16n8k8
+// TF32 and a three-product big/small split of every operand (x = big + small,
+// big = tf32(x), small = tf32(x - big); big*big + big*small + small*big), which
+// keeps the product at about fp32 accuracy.  The accumulator is the m16n8
+// fragment of the two 8-column halves: acc[4 h + i] holds row
+// (lane / 4) + 8 (i / 2), column 8 h + 2 (lane % 4) + (i % 2).
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void split_tf32(float x, uint32_t& big, uint32_t& small) {
+    big = tf32_rna(x);
+    small = tf32_rna(x - __uint_as_float(big));
+}
+__device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint32_t* b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
 __device__ __forceinline__ void mm16(float (&acc)[8], const float* A, int lda, const float* B, int ldb, int lane,
                                      bool accumulate) {
-    const int r = lane >> 1, c0 = 8 * (lane & 1);
+    const int g = lane >> 2, t = lane & 3;
     if (!accumulate) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.f;
     }
 #pragma unroll
-    for (int k4 = 0; k4 < 16; k4 += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(A + r * lda + k4);
-        const float av[4] = {a.x, a.y, a.z, a.w};
+    for (int kk = 0; kk < 16; kk += 8) {
+        uint32_t ab[4], as[4];
+        split_tf32(A[g * lda + kk + t], ab[0], as[0]);
+        split_tf32(A[(g + 8) * lda + kk + t], ab[1], as[1]);
+        split_tf32(A[g * lda + kk + t + 4], ab[2], as[2]);
+        split_tf32(A[(g + 8) * lda + kk + t + 4], ab[3], as[3]);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const float4 b0 = *reinterpret_cast<const float4*>(B + (k4 + kk) * ldb + c0);
-            const float4 b1 = *reinterpret_cast<const float4*>(B + (k4 + kk) * ldb + c0 + 4);
-            acc[0] = fmaf(av[kk], b0.x, acc[0]); acc[1] = fmaf(av[kk], b0.y, acc[1]);
-            acc[2] = fmaf(av[kk], b0.z, acc[2]); acc[3] = fmaf(av[kk], b0.w, acc[3]);
-            acc[4] = fmaf(av[kk], b1.x, acc[4]); acc[5] = fmaf(av[kk], b1.y, acc[5]);
-            acc[6] = fmaf(av[kk], b1.z, acc[6]); acc[7] = fmaf(av[kk], b1.w, acc[7]);
+        for (int h = 0; h < 2; ++h) {
+            uint32_t bb[2], bs[2];
+            split_tf32(B[(kk + t) * ldb + 8 * h + g], bb[0], bs[0]);
+            split_tf32(B[(kk + t + 4) * ldb + 8 * h + g], bb[1], bs[1]);
+            mma_tf32(acc + 4 * h, as, bb);
+            mma_tf32(acc + 4 * h, ab, bs);
+            mma_tf32(acc + 4 * h, ab, bb);
         }
     }
 }
 
 __device__ __forceinline__ void st16(float* D, int ldd, const float (&acc)[8], int lane, float scale) {
-    const int r = lane >> 1, c0 = 8 * (lane & 1);
-    *reinterpret_cast<float4*>(D + r * ldd + c0) =
-        make_float4(scale * acc[0], scale * acc[1], scale * acc[2], scale * acc[3]);
-    *reinterpret_cast<float4*>(D + r * ldd + c0 + 4) =
-        make_float4(scale * acc[4], scale * acc[5], scale * acc[6], scale * acc[7]);
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        *reinterpret_cast<float2*>(D + g * ldd + 8 * h + 2 * t) =
+            make_float2(scale * acc[4 * h], scale * acc[4 * h + 1]);
+        *reinterpret_cast<float2*>(D + (g + 8) * ldd + 8 * h + 2 * t) =
+            make_float2(scale * acc[4 * h + 2], scale * acc[4 * h + 3]);
+    }
 }
 
 __device__ __forceinline__ uint4 pack8(const float* f) {
@@ -352,7 +379,7 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
     for (int rr = 0; rr < 16; ++rr) {
         const int r = 16 * b + rr;
         const float e0 = __expf(G0[rr] - G0[0]), e1 = __expf(G1[rr] - G1[0]);   // <= 1
-        const float c0 = __expf(G0[0] - G0[rr]), c1 = __expf(G1[0] - G1[rr]);   // >= 1, <= e^75
+        const float c0 = __fdividef(1.f, e0), c1 = __fdividef(1.f, e1);         // >= 1, <= e^75
         const float2 qf = kda::unpack_bf16x2(qv[rr]);
         const float2 kf = kda::unpack_bf16x2(kv[rr]);
         const float be = bt[rr];
@@ -415,11 +442,11 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
             const int o = 16 * w, j = lane;
             float x[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float a = (r == j) ? 1.f : 0.f;
+            for (int r = 0; r < 16; ++r) {              // four partial sums shorten the FMA chain
+                float a[4] = {(r == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int t = 0; t < r; ++t) a = fmaf(-LS[(o + r) * LDS_ + o + t], x[t], a);
-                x[r] = a;
+                for (int t = 0; t < r; ++t) a[t & 3] = fmaf(-LS[(o + r) * LDS_ + o + t], x[t], a[t & 3]);
+                x[r] = (a[0] + a[1]) + (a[2] + a[3]);
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) IS[(o + r) * LDS_ + o + j] = x[r];
