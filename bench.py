@@ -221,6 +221,30 @@ def time_decode(kda, w, inputs, steps, warmup, stream, dev, seed=0):
     return start.elapsed_time(end), steps
 
 
+def time_verify(kda, inputs, steps, warmup, stream, dev, K=8, N=256, H=32, D=128, seed=0):
+    """Multi-token verify: K proposed tokens per sequence, all committed."""
+    w = inputs.Workload("verify", "prefill", H=H, dk=D, dv=D, dtype=torch.bfloat16, T=K, B=N)
+    d = inputs.make_prefill(w, device=dev, seed=seed, lengths=[K] * N)
+    rs = lambda x, last: x.view(N, K, H, last).contiguous()
+    q, k, v, g = rs(d["q"], D), rs(d["k"], D), rs(d["v"], D), rs(d["log_alpha"], D)
+    b = d["beta"].view(N, K, H).contiguous()
+    S = (torch.randn((N, H, D, D), device=dev, dtype=torch.float32) * 0.02).contiguous()
+    o = torch.empty((N, K, H, D), dtype=torch.bfloat16, device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            kda.kda_decode_multi(q, k, v, g, b, S, o=o, stream=stream)
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            kda.kda_decode_multi(q, k, v, g, b, S, o=o, stream=stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    bytes_call = N * H * (8 * D * D + K * (3 * 2 * D + 4 * D + 4 + 2 * D))
+    return ms, bytes_call
+
+
 def time_e2e(kda, d, steps, stream, dev):
     """Through the C ABI from pinned host buffers: H2D inputs, prefill, D2H O and S_final."""
     names = ("q", "k", "v", "log_alpha", "beta")
@@ -286,8 +310,10 @@ def run_gpu(args):
         wd = inputs.WORKLOADS[DECODE]
         dec_steps = max(args.steps, args.decode_steps)
         dms, dsteps = time_decode(kda, wd, inputs, dec_steps, args.warmup, stream, dev, seed=rank)
+        vms, vbytes = time_verify(kda, inputs, max(args.steps, 50), args.warmup, stream, dev, seed=rank)
     ms = barrier_max(ms, world, dev)
     dms = barrier_max(dms, world, dev)
+    vms = barrier_max(vms, world, dev)
     e2e_ms, h2d, d2h = time_e2e(kda, d, max(3, args.steps // 4), stream, dev)
     e2e_ms = barrier_max(e2e_ms, world, dev)
     e2e_steps = max(3, args.steps // 4)
@@ -327,6 +353,12 @@ def run_gpu(args):
                                 "peak": hbm, "unit": "GB/s", "frac": dec_achieved / hbm, "traffic": None,
                                 "bytes_per_launch": dec_bytes_step},
                    "l2": "fp32 state 537 MB > L2; fresh token set per step"},
+        "verify": {"workload": "verify_bf16_N256_K8_H32_D128", "value": replica_throughput(1, 1, world, vms),
+                   "unit": "calls/s", "ms_per_call": vms,
+                   "roofline": {"bound": "hbm", "kernel": "kda_decode_multi_kernel",
+                                "achieved": vbytes / (vms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                                "frac": vbytes / (vms / 1e3) / 1e9 / hbm, "traffic": None,
+                                "bytes_per_launch": vbytes}},
         "e2e": {"value": replica_throughput(T, e2e_steps, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * world,

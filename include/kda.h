@@ -170,6 +170,29 @@ KDA_API kda_status kda_decode(const void* q, const void* k, const void* v,
                       cudaStream_t stream);
 
 /*
+ * Multi-token verify step for speculative decoding: the "LLM architecture at
+ * trillion scale" page (section "6. Deep dive: what this means for serving")
+ * has a draft model propose up to 7 tokens that the big model then checks.
+ * For each of N sequences, K proposed tokens (K <= 16) are run through the
+ * recurrence from the state S, every o_t is returned, and S is overwritten
+ * with the state after the first commit_len[n] tokens only (0 leaves S as
+ * it was; the rest of the proposal is not committed).
+ *
+ * q, k       [N, K, H, dk] dtype;  v [N, K, H, dv] dtype
+ * log_alpha  [N, K, H, dk] float;  beta [N, K, H] float
+ * S          [N, H, dk, dv] float, read, and written after commit_len tokens
+ * commit_len [N] int32 device array, values clamped to [0, K]; NULL = K
+ * o          [N, K, H, dv] dtype, or NULL to skip the outputs
+ * A typical use calls it twice: once with commit_len all 0 to get the
+ * outputs, then, once the accepted lengths are known, with o = NULL and
+ * commit_len = the accepted lengths.
+ */
+KDA_API kda_status kda_decode_multi(const void* q, const void* k, const void* v,
+                            const float* log_alpha, const float* beta, float* S,
+                            const int32_t* commit_len, int N, int K, int H, int dk, int dv,
+                            kda_dtype dtype, void* o, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word:
  * KDA_OK, or KDA_ERR_TIMEOUT if a kernel since the last call gave up waiting
  * (its outputs are then incomplete), or KDA_ERR_CUDA if the synchronisation

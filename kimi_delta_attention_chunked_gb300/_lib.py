@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(6)
 KDA_FP32, KDA_BF16 = 0, 1
-SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_noalloc", "kda_decode",
+SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_noalloc", "kda_decode", "kda_decode_multi",
            "kda_get_last_device_status", "kda_set_trace_events", "kda_status_string")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -51,6 +51,8 @@ def load():
         lib.kda_prefill_noalloc.restype = I
         lib.kda_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P]
         lib.kda_decode.restype = I
+        lib.kda_decode_multi.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P]
+        lib.kda_decode_multi.restype = I
         lib.kda_get_last_device_status.argtypes = [P]
         lib.kda_get_last_device_status.restype = I
         lib.kda_set_trace_events.argtypes = [P, I]
@@ -186,6 +188,29 @@ def kda_decode(q, k, v, log_alpha, beta, S, o=None, stream=None):
                         _dtype_code(q.dtype), _ptr(o), _stream(stream, dev))
     if st != KDA_OK:
         raise KDAError(st, "kda_decode")
+    return o
+
+
+def kda_decode_multi(q, k, v, log_alpha, beta, S, commit_len=None, o=None, want_o=True, stream=None):
+    """Verify K proposed tokens per sequence: q, k, log_alpha [N, K, H, dk]; v [N, K, H, dv];
+    beta [N, K, H]; S [N, H, dk, dv] fp32 (written after commit_len[n] tokens; int32 [N] on
+    the device or None = all K).  Returns o [N, K, H, dv] (None if want_o is False)."""
+    lib = load()
+    dev = q.device
+    N, K, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_dev(name, t, dev, q.dtype)
+    _check_dev("log_alpha", log_alpha, dev, torch.float32)
+    _check_dev("beta", beta, dev, torch.float32)
+    _check_dev("S", S, dev, torch.float32)
+    _check_dev("commit_len", commit_len, dev, torch.int32)
+    if o is None and want_o:
+        o = torch.empty((N, K, H, dv), dtype=q.dtype, device=dev)
+    st = lib.kda_decode_multi(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S), _ptr(commit_len),
+                              N, K, H, dk, dv, _dtype_code(q.dtype), _ptr(o), _stream(stream, dev))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_multi")
     return o
 
 

@@ -84,6 +84,8 @@ void trace_mark(cudaStream_t stream);
 void trace_reset();
 
 cudaError_t launch_decode(const DecodeArgs& a);
+int decode_multi_max_tokens();
+cudaError_t launch_decode_multi(const DecodeArgs& a, int K, const int32_t* commit_len);
 cudaError_t launch_prefill_simt_fp32_c16(const PrefillArgs& a);
 cudaError_t launch_prefill_simt_fp32_c32(const PrefillArgs& a);
 cudaError_t launch_prefill_simt_fp32_c64(const PrefillArgs& a);

@@ -125,6 +125,122 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     }
 }
 
+// Multi-token verify step: K tokens per sequence applied to a register-resident
+// state, every o_t produced, the state written back after commit_len[n] of them.
+// Same thread layout as the single-token kernel; the K tokens' q, k, v, gates
+// are staged in shared memory first.
+constexpr int kMaxVerify = 16;
+
+template <int DK, int DV, typename TIn>
+__global__ void __launch_bounds__(kThreads, 2)
+kda_decode_multi_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn* __restrict__ v,
+                        const float* __restrict__ log_alpha, const float* __restrict__ beta,
+                        float* __restrict__ S, const int32_t* __restrict__ commit_len, int K, int H,
+                        TIn* __restrict__ o) {
+    constexpr int LPR = DV / 4;
+    constexpr int RPP = kThreads / LPR;
+    constexpr int NPASS = (DK + RPP - 1) / RPP;
+    __shared__ float s_k[kMaxVerify][DK], s_q[kMaxVerify][DK], s_a[kMaxVerify][DK];
+    __shared__ float s_v[kMaxVerify][DV];
+    __shared__ float s_b[kMaxVerify];
+    __shared__ float4 s_x[RPP][LPR];
+    __shared__ float4 s_y[RPP][LPR];
+
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    const size_t unit = blockIdx.x;                   // n * H + h
+    const int tid = threadIdx.x;
+    const int c4 = tid % LPR, r0 = tid / LPR;
+    float* Su = S + unit * (size_t)DK * DV;
+    int commit = commit_len ? commit_len[n] : K;
+    commit = min(max(commit, 0), K);
+
+    float4 s[NPASS];
+#pragma unroll
+    for (int p = 0; p < NPASS; ++p) {
+        const int i = r0 + p * RPP;
+        if (i < DK) s[p] = __ldcs(reinterpret_cast<const float4*>(Su + (size_t)i * DV) + c4);
+    }
+    for (int e = tid; e < K * DK; e += kThreads) {
+        const int t = e / DK, i = e % DK;
+        const size_t off = (((size_t)n * K + t) * H + h) * DK + i;
+        s_k[t][i] = kda::io<TIn>::ld(k + off);
+        s_q[t][i] = kda::io<TIn>::ld(q + off);
+        s_a[t][i] = __expf(log_alpha[off]);
+    }
+    for (int e = tid; e < K * DV; e += kThreads) {
+        const int t = e / DV, j = e % DV;
+        s_v[t][j] = kda::io<TIn>::ld(v + (((size_t)n * K + t) * H + h) * DV + j);
+    }
+    for (int t = tid; t < K; t += kThreads) s_b[t] = beta[((size_t)n * K + t) * H + h];
+    __syncthreads();
+
+    for (int t = 0; t < K; ++t) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+#pragma unroll
+        for (int p = 0; p < NPASS; ++p) {
+            const int i = r0 + p * RPP;
+            if (i < DK) {
+                const float a = s_a[t][i], ki = s_k[t][i], qi = s_q[t][i];
+                s[p].x *= a; s[p].y *= a; s[p].z *= a; s[p].w *= a;
+                x.x = fmaf(s[p].x, ki, x.x); x.y = fmaf(s[p].y, ki, x.y);
+                x.z = fmaf(s[p].z, ki, x.z); x.w = fmaf(s[p].w, ki, x.w);
+                y.x = fmaf(s[p].x, qi, y.x); y.y = fmaf(s[p].y, qi, y.y);
+                y.z = fmaf(s[p].z, qi, y.z); y.w = fmaf(s[p].w, qi, y.w);
+            }
+        }
+        s_x[r0][c4] = x;
+        s_y[r0][c4] = y;
+        __syncthreads();
+        float4 X = make_float4(0.f, 0.f, 0.f, 0.f), Y = X;
+#pragma unroll 8
+        for (int r = 0; r < RPP; ++r) {
+            const float4 a = s_x[r][c4], b = s_y[r][c4];
+            X.x += a.x; X.y += a.y; X.z += a.z; X.w += a.w;
+            Y.x += b.x; Y.y += b.y; Y.z += b.z; Y.w += b.w;
+        }
+        const float bt = s_b[t];
+        float4 u;
+        u.x = bt * (s_v[t][4 * c4 + 0] - X.x); u.y = bt * (s_v[t][4 * c4 + 1] - X.y);
+        u.z = bt * (s_v[t][4 * c4 + 2] - X.z); u.w = bt * (s_v[t][4 * c4 + 3] - X.w);
+#pragma unroll
+        for (int p = 0; p < NPASS; ++p) {
+            const int i = r0 + p * RPP;
+            if (i < DK) {
+                const float ki = s_k[t][i];
+                s[p].x = fmaf(ki, u.x, s[p].x); s[p].y = fmaf(ki, u.y, s[p].y);
+                s[p].z = fmaf(ki, u.z, s[p].z); s[p].w = fmaf(ki, u.w, s[p].w);
+            }
+        }
+        if (o && r0 == 0) {
+            float kq = 0.f;
+            for (int i = 0; i < DK; ++i) kq = fmaf(s_k[t][i], s_q[t][i], kq);
+            TIn* ou = o + (((size_t)n * K + t) * H + h) * DV + 4 * c4;
+            kda::io<TIn>::st(ou + 0, fmaf(kq, u.x, Y.x));
+            kda::io<TIn>::st(ou + 1, fmaf(kq, u.y, Y.y));
+            kda::io<TIn>::st(ou + 2, fmaf(kq, u.z, Y.z));
+            kda::io<TIn>::st(ou + 3, fmaf(kq, u.w, Y.w));
+        }
+        if (t + 1 == commit) {                         // the accepted prefix ends here
+#pragma unroll
+            for (int p = 0; p < NPASS; ++p) {
+                const int i = r0 + p * RPP;
+                if (i < DK) __stcs(reinterpret_cast<float4*>(Su + (size_t)i * DV) + c4, s[p]);
+            }
+        }
+        __syncthreads();                               // s_x / s_y are reused by the next token
+    }
+}
+
+template <int DK, int DV, typename TIn>
+cudaError_t launch_multi(const kda_host::DecodeArgs& a, int K, const int32_t* commit_len) {
+    const unsigned units = (unsigned)((size_t)a.N * a.H);
+    if (units == 0 || K == 0) return cudaSuccess;
+    kda_decode_multi_kernel<DK, DV, TIn><<<units, kThreads, 0, a.stream>>>(
+        static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v), a.log_alpha,
+        a.beta, a.S, commit_len, K, a.H, static_cast<TIn*>(a.o));
+    return cudaGetLastError();
+}
+
 template <int DK, int DV, typename TIn>
 cudaError_t launch(const kda_host::DecodeArgs& a) {
     const unsigned units = (unsigned)((size_t)a.N * a.H);
@@ -146,6 +262,17 @@ cudaError_t dispatch_dims(const kda_host::DecodeArgs& a) {
     return cudaErrorNotSupported;
 }
 
+template <typename TIn>
+cudaError_t dispatch_multi(const kda_host::DecodeArgs& a, int K, const int32_t* cl) {
+#define KDA_MULTI_CASE(DK_, DV_) \
+    if (a.dk == DK_ && a.dv == DV_) return launch_multi<DK_, DV_, TIn>(a, K, cl);
+    KDA_MULTI_CASE(32, 32) KDA_MULTI_CASE(32, 64) KDA_MULTI_CASE(32, 128)
+    KDA_MULTI_CASE(64, 32) KDA_MULTI_CASE(64, 64) KDA_MULTI_CASE(64, 128)
+    KDA_MULTI_CASE(128, 32) KDA_MULTI_CASE(128, 64) KDA_MULTI_CASE(128, 128)
+#undef KDA_MULTI_CASE
+    return cudaErrorNotSupported;
+}
+
 }  // namespace
 
 namespace kda_host {
@@ -153,6 +280,13 @@ namespace kda_host {
 cudaError_t launch_decode(const DecodeArgs& a) {
     if (a.dtype == KDA_BF16) return dispatch_dims<__nv_bfloat16>(a);
     return dispatch_dims<float>(a);
+}
+
+int decode_multi_max_tokens() { return kMaxVerify; }
+
+cudaError_t launch_decode_multi(const DecodeArgs& a, int K, const int32_t* commit_len) {
+    if (a.dtype == KDA_BF16) return dispatch_multi<__nv_bfloat16>(a, K, commit_len);
+    return dispatch_multi<float>(a, K, commit_len);
 }
 
 }  // namespace kda_host

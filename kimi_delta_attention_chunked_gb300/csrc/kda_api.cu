@@ -159,6 +159,26 @@ kda_status kda_decode(const void* q, const void* k, const void* v, const float* 
     return from_cuda(e);
 }
 
+kda_status kda_decode_multi(const void* q, const void* k, const void* v, const float* log_alpha,
+                            const float* beta, float* S, const int32_t* commit_len, int N, int K, int H, int dk,
+                            int dv, kda_dtype dtype, void* o, cudaStream_t stream) {
+    if (N < 0 || H <= 0 || K < 0) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return KDA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (K > kda_host::decode_multi_max_tokens()) return KDA_ERR_UNSUPPORTED;
+    if ((long long)N * H >= (1LL << 31)) return KDA_ERR_UNSUPPORTED;
+    if (N == 0 || K == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !S) return KDA_ERR_INVALID_ARG;
+    if (o && (o == q || o == k || o == v || o == (void*)S)) return KDA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(S) % 16 != 0) return KDA_ERR_INVALID_ARG;
+    kda_host::DecodeArgs a{q, k, v, log_alpha, beta, S, N, H, dk, dv, dtype, o, stream};
+    kda_host::trace_reset();
+    kda_host::trace_mark(stream);
+    const cudaError_t e = kda_host::launch_decode_multi(a, K, commit_len);
+    kda_host::trace_mark(stream);
+    return from_cuda(e);
+}
+
 kda_status kda_get_last_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return KDA_ERR_CUDA;
     int h = 0;

@@ -59,3 +59,61 @@ def test_decode_matches_prefill_of_same_tokens():
     o = torch.cat(outs)
     assert rel_err(o, O.double().cpu().numpy()) < 1e-5
     assert rel_err(S, Sf.double().cpu().numpy()) < 1e-5
+
+
+@pytest.mark.parametrize("K", [1, 3, 8])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_verify_multi_token(K, dtype):
+    """K proposed tokens per sequence: every output vs the oracle; the state is
+    committed after commit_len[n] tokens (0 .. K, drawn per sequence)."""
+    dev = need_gpu()
+    N, H, D = 16, 4, 128
+    w = inputs.Workload("verify", "prefill", H=H, dk=D, dv=D, dtype=dtype, chunk=64, T=K, B=N, s0_std=0.02)
+    d = inputs.make_prefill(w, device=dev, seed=K, lengths=[K] * N)
+    rs = lambda x, last: x.view(N, K, H, last).contiguous()
+    q, k, v, g = rs(d["q"], D), rs(d["k"], D), rs(d["v"], D), rs(d["log_alpha"], D)
+    b = d["beta"].view(N, K, H).contiguous()
+    S = d["S0"].clone()
+    commit = torch.tensor([(7 * n) % (K + 1) for n in range(N)], dtype=torch.int32, device=dev)
+    o = kda.kda_decode_multi(q, k, v, g, b, S, commit_len=commit)
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_device_status() == 0
+    O_ref, _ = oracle.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], cu_seqlens=d["cu_seqlens_host"],
+                              S0=d["S0"])
+    assert rel_err(o.view(N * K, H, D), O_ref) <= tol_for(dtype)
+    for n in range(N):
+        c = int(commit[n])
+        if c == 0:
+            ref = d["S0"][n].double().cpu().numpy()
+        else:
+            sl = slice(n * K, n * K + c)
+            _, Sf = oracle.prefill(d["q"][sl], d["k"][sl], d["v"][sl], d["log_alpha"][sl], d["beta"][sl],
+                                   S0=d["S0"][n:n + 1])
+            ref = Sf[0]
+        assert rel_err(S[n], ref) <= tol_for(dtype), n
+
+
+def test_verify_outputs_only_then_commit():
+    """The two-call pattern: outputs with nothing committed, then a commit-only call."""
+    dev = need_gpu()
+    N, K, H, D = 8, 5, 2, 64
+    w = inputs.Workload("verify2", "prefill", H=H, dk=D, dv=D, dtype=torch.float32, chunk=64, T=K, B=N, s0_std=0.02)
+    d = inputs.make_prefill(w, device=dev, seed=99, lengths=[K] * N)
+    rs = lambda x: x.view(N, K, H, D).contiguous()
+    b = d["beta"].view(N, K, H).contiguous()
+    S = d["S0"].clone()
+    zero = torch.zeros(N, dtype=torch.int32, device=dev)
+    o = kda.kda_decode_multi(rs(d["q"]), rs(d["k"]), rs(d["v"]), rs(d["log_alpha"]), b, S, commit_len=zero)
+    assert torch.equal(S, d["S0"])                    # nothing committed
+    acc = torch.tensor([K, 0, 1, 2, 3, 4, K, 1], dtype=torch.int32, device=dev)
+    assert kda.kda_decode_multi(rs(d["q"]), rs(d["k"]), rs(d["v"]), rs(d["log_alpha"]), b, S, commit_len=acc,
+                                want_o=False) is None
+    for n in range(N):
+        c = int(acc[n])
+        if c:
+            sl = slice(n * K, n * K + c)
+            _, Sf = oracle.prefill(d["q"][sl], d["k"][sl], d["v"][sl], d["log_alpha"][sl], d["beta"][sl],
+                                   S0=d["S0"][n:n + 1])
+            assert rel_err(S[n], Sf[0]) <= 1e-4
+        else:
+            assert torch.equal(S[n], d["S0"][n])

@@ -36,6 +36,8 @@ def run_case(w, dev, lengths=None, seed=0, heads=None, host_cu=True, check=True,
                                    cu_seqlens=d["cu_seqlens_host"], S0=s0)
     eo = rel_err(O[:, sl], O_ref)
     es = rel_err(Sf[:, sl], Sf_ref)
+    print(f"PARITY {w.name} dtype={w.dtype} lengths={lengths if lengths else d['lengths'][:3]} heads={h0}:{h1} "
+          f"O={eo:.3e} S={es:.3e}")
     return d, O, Sf, eo, es
 
 
