@@ -122,6 +122,34 @@ KDA_API kda_status kda_prefill(const void* q, const void* k, const void* v,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * kda_prefill that also saves the recurrent state at coarse positions, for
+ * prefix caching: a linear-attention layer can only resume a cached prefix
+ * from a stored state, so serving stacks keep the state every so many tokens
+ * ("Kimi K3: the manos, the mythos, the legendos", section "KDA Prefix Cache
+ * Management"; the "LLM architecture at trillion scale" page, section "6. Deep
+ * dive: what this means for serving").
+ *
+ * Arguments as kda_prefill, plus:
+ * ckpt_every     positive multiple of chunk: a checkpoint is the state after
+ *                the first m * ckpt_every tokens of a sequence (m = 1, 2, ...,
+ *                as long as m * ckpt_every <= its length)
+ * ckpt           [ckpt_capacity, H, dk, dv] float device array; checkpoint m of
+ *                sequence n goes to index sum_{n' < n} floor(len_n' /
+ *                ckpt_every) + m - 1
+ * ckpt_capacity  number of checkpoints ckpt holds; when the lengths are known
+ *                on the host (cu_seqlens_host, or equal lengths) a smaller
+ *                capacity than needed is KDA_ERR_INVALID_ARG, otherwise
+ *                checkpoints past the capacity are not written.
+ */
+KDA_API kda_status kda_prefill_ckpt(const void* q, const void* k, const void* v,
+                            const float* log_alpha, const float* beta, const float* S0,
+                            const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                            int n_seq, int T_total, int H, int dk, int dv, int chunk,
+                            kda_dtype dtype, void* O, float* S_final, int ckpt_every,
+                            float* ckpt, int ckpt_capacity, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Size of the fixed device array that kda_prefill_noalloc uses as its
  * workspace (bytes).  Every GPU that loads the library holds it until exit.
  */

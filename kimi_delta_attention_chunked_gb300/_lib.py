@@ -18,8 +18,8 @@ LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(6)
 KDA_FP32, KDA_BF16 = 0, 1
-SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_noalloc", "kda_decode", "kda_decode_multi",
-           "kda_get_last_device_status", "kda_set_trace_events", "kda_status_string")
+SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_ckpt", "kda_prefill_noalloc", "kda_decode",
+           "kda_decode_multi", "kda_get_last_device_status", "kda_set_trace_events", "kda_status_string")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lock = threading.Lock()
@@ -47,6 +47,8 @@ def load():
         lib.kda_prefill_workspace_size.restype = Z
         lib.kda_prefill.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, Z, P]
         lib.kda_prefill.restype = I
+        lib.kda_prefill_ckpt.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, I, P, I, P, Z, P]
+        lib.kda_prefill_ckpt.restype = I
         lib.kda_prefill_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
         lib.kda_prefill_noalloc.restype = I
         lib.kda_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P]
@@ -136,6 +138,60 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, cu_seqlens_h
     if st != KDA_OK:
         raise KDAError(st, "kda_prefill")
     return O, S_final
+
+
+def checkpoint_count(seq_lens, ckpt_every: int) -> int:
+    """Number of checkpoints kda_prefill_ckpt writes for these sequence lengths."""
+    return sum(int(n) // ckpt_every for n in seq_lens)
+
+
+def kda_prefill_ckpt(q, k, v, log_alpha, beta, ckpt_every, S0=None, cu_seqlens=None, cu_seqlens_host=None,
+                     chunk=64, O=None, S_final=None, ckpt=None, workspace=None, stream=None):
+    """kda_prefill that also returns the state after every ``ckpt_every`` tokens
+    of each sequence: (O, S_final, ckpt), ckpt [n_ckpt, H, dk, dv] fp32 with the
+    checkpoints of sequence 0 first, in position order.  Without a ``ckpt``
+    buffer the lengths must be known here (``cu_seqlens_host``, or one sequence)."""
+    lib = load()
+    dev = q.device
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_dev(name, t, dev, q.dtype)
+    _check_dev("log_alpha", log_alpha, dev, torch.float32)
+    _check_dev("beta", beta, dev, torch.float32)
+    _check_dev("cu_seqlens", cu_seqlens, dev, torch.int32)
+    n_seq = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if S0 is not None:
+        _check_dev("S0", S0, dev, torch.float32)
+    if ckpt is None:
+        if cu_seqlens is None:
+            lens = [T]
+        elif cu_seqlens_host is not None:
+            b = [int(x) for x in cu_seqlens_host]
+            lens = [b[i + 1] - b[i] for i in range(n_seq)]
+        else:
+            raise ValueError("kda_prefill_ckpt: pass ckpt or cu_seqlens_host")
+        ckpt = torch.empty((checkpoint_count(lens, ckpt_every), H, dk, dv), dtype=torch.float32, device=dev)
+    _check_dev("ckpt", ckpt, dev, torch.float32)
+    if O is None:
+        O = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    if S_final is None:
+        S_final = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev)
+    host = None
+    if cu_seqlens_host is not None:
+        host = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+    dt = _dtype_code(q.dtype)
+    need = int(lib.kda_prefill_workspace_size(n_seq, T, H, dk, dv, chunk, dt))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kda_prefill_ckpt(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                              _ptr(cu_seqlens), host, n_seq, T, H, dk, dv, chunk, dt, _ptr(O), _ptr(S_final),
+                              int(ckpt_every), _ptr(ckpt), ckpt.shape[0] if ckpt.numel() else 0,
+                              _ptr(workspace), ws_bytes, _stream(stream, dev))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_prefill_ckpt")
+    return O, S_final, ckpt
 
 
 def kda_prefill_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, cu_seqlens_host=None, chunk=64,

@@ -41,6 +41,26 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
     return __bfloat1622float2(v);
 }
 
+// Index of the first checkpoint of sequence n: sum over earlier sequences of
+// floor(len / every).  Block-wide sum; every thread of the block must call it.
+// lens_of(m) returns the length of sequence m.
+template <typename LenFn>
+__device__ __forceinline__ int ckpt_base(int n, int every, LenFn lens_of) {
+    __shared__ int red[32];
+    int part = 0;
+    for (int m = threadIdx.x; m < n; m += blockDim.x) part += lens_of(m) / every;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    const int w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[w] = part;
+    __syncthreads();
+    int tot = 0;
+    for (int i = 0; i < nw; ++i) tot += red[i];
+    __syncthreads();
+    return tot;
+}
+
 }  // namespace kda
 
 // Host-side launchers implemented by the kernel translation units.
@@ -64,6 +84,9 @@ struct PrefillArgs {
     size_t workspace_bytes;
     cudaStream_t stream;
     int* status;                 // device status word
+    int ckpt_every;              // 0: no checkpoints; else a multiple of chunk (tokens)
+    float* ckpt;                 // [ckpt_cap, H, dk, dv]
+    int ckpt_cap;
 };
 
 struct DecodeArgs {

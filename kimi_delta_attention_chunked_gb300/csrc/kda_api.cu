@@ -72,11 +72,16 @@ size_t kda_prefill_workspace_size(int n_seq, int T_total, int H, int dk, int dv,
     return kda_host::tc_workspace_bytes(n_seq, T_total, H, chunk);
 }
 
-kda_status kda_prefill(const void* q, const void* k, const void* v, const float* log_alpha,
-                       const float* beta, const float* S0, const int32_t* cu_seqlens,
-                       const int32_t* cu_seqlens_host, int n_seq, int T_total, int H, int dk,
-                       int dv, int chunk, kda_dtype dtype, void* O, float* S_final,
-                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+kda_status prefill_impl(const void* q, const void* k, const void* v, const float* log_alpha,
+                        const float* beta, const float* S0, const int32_t* cu_seqlens,
+                        const int32_t* cu_seqlens_host, int n_seq, int T_total, int H, int dk, int dv,
+                        int chunk, kda_dtype dtype, void* O, float* S_final, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream, int ckpt_every, float* ckpt,
+                        int ckpt_cap) {
     if (n_seq < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return KDA_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk)) return KDA_ERR_UNSUPPORTED;
@@ -116,7 +121,7 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
     a.dv = dv; a.chunk = chunk; a.total_chunks = total_chunks; a.max_chunks = max_chunks; a.dtype = dtype;
     a.O = O;
     a.S_final = S_final; a.workspace = workspace; a.workspace_bytes = workspace_bytes;
-    a.stream = stream;
+    a.stream = stream; a.ckpt_every = ckpt_every; a.ckpt = ckpt; a.ckpt_cap = ckpt_cap;
 
     if (kda_host::tc_supported(dk, dv, chunk, dtype)) {
         const size_t need = kda_host::tc_workspace_bytes(n_seq, T_total, H, chunk);
@@ -138,6 +143,42 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
          kda_host::launch_prefill_simt_bf16_c64}};
     const int ci = chunk == 16 ? 0 : (chunk == 32 ? 1 : 2);
     return from_cuda(simt[dtype == KDA_BF16 ? 1 : 0][ci](a));
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill(const void* q, const void* k, const void* v, const float* log_alpha,
+                       const float* beta, const float* S0, const int32_t* cu_seqlens,
+                       const int32_t* cu_seqlens_host, int n_seq, int T_total, int H, int dk,
+                       int dv, int chunk, kda_dtype dtype, void* O, float* S_final,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return prefill_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, n_seq, T_total, H, dk, dv,
+                        chunk, dtype, O, S_final, workspace, workspace_bytes, stream, 0, nullptr, 0);
+}
+
+kda_status kda_prefill_ckpt(const void* q, const void* k, const void* v, const float* log_alpha,
+                            const float* beta, const float* S0, const int32_t* cu_seqlens,
+                            const int32_t* cu_seqlens_host, int n_seq, int T_total, int H, int dk, int dv,
+                            int chunk, kda_dtype dtype, void* O, float* S_final, int ckpt_every,
+                            float* ckpt, int ckpt_capacity, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+    if (!chunk_ok(chunk)) return KDA_ERR_UNSUPPORTED;
+    if (ckpt_every <= 0 || ckpt_every % chunk != 0 || ckpt_capacity < 0) return KDA_ERR_INVALID_ARG;
+    if (ckpt_capacity > 0 && !ckpt) return KDA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ckpt) % 16 != 0) return KDA_ERR_INVALID_ARG;   // vector stores
+    if (cu_seqlens_host && n_seq > 0) {                 // the caller's buffer must hold every checkpoint
+        long long need = 0;
+        for (int n = 0; n < n_seq; ++n)
+            need += (long long)std::max(0, cu_seqlens_host[n + 1] - cu_seqlens_host[n]) / ckpt_every;
+        if (need > ckpt_capacity) return KDA_ERR_INVALID_ARG;
+    } else if (!cu_seqlens && n_seq > 0) {
+        if ((long long)n_seq * ((T_total / n_seq) / ckpt_every) > ckpt_capacity) return KDA_ERR_INVALID_ARG;
+    }
+    return prefill_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, n_seq, T_total, H, dk, dv,
+                        chunk, dtype, O, S_final, workspace, workspace_bytes, stream, ckpt_every, ckpt,
+                        ckpt_capacity);
 }
 
 kda_status kda_decode(const void* q, const void* k, const void* v, const float* log_alpha,

@@ -54,7 +54,8 @@ kda_prefill_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                         const TIn* __restrict__ v, const float* __restrict__ log_alpha,
                         const float* __restrict__ beta, const float* __restrict__ S0,
                         const int32_t* __restrict__ cu_seqlens, int T_total, int H,
-                        int seq_len_fixed, TIn* __restrict__ O, float* __restrict__ S_final) {
+                        int seq_len_fixed, TIn* __restrict__ O, float* __restrict__ S_final,
+                        int ckpt_every, float* __restrict__ ckpt, int ckpt_cap) {
     constexpr int DVT = DV < 32 ? DV : 32;
     using Sm = SimtSmem<DK, DVT, C>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -78,6 +79,23 @@ kda_prefill_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         eos = bos + seq_len_fixed;
     }
 
+    // state checkpoints: index of this sequence's first one (block-wide sum)
+    int ck_base = 0;
+    if (ckpt_every > 0) {
+        ck_base = cu_seqlens ? kda::ckpt_base(n, ckpt_every,
+                                              [&](int m) {
+                                                  const int b0 = min(max(cu_seqlens[m], 0), T_total);
+                                                  return min(max(cu_seqlens[m + 1], b0), T_total) - b0;
+                                              })
+                             : n * (seq_len_fixed / ckpt_every);
+    }
+    auto put_ckpt = [&](int idx) {             // every thread stores its elements of the slice
+        if (idx < 0 || idx >= ckpt_cap) return;
+        for (int e = tid; e < DK * DVT; e += kThreads) {
+            const int i = e / DVT, j = e % DVT;
+            ckpt[(((size_t)idx * H + h) * DK + i) * DV + j0 + j] = sm.s[i][j];
+        }
+    };
     // initial state slice
     for (int e = tid; e < DK * DVT; e += kThreads) {
         const int i = e / DVT, j = e % DVT;
@@ -87,6 +105,7 @@ kda_prefill_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     for (int c0 = bos; c0 < eos; c0 += C) {
         const int nr = min(C, eos - c0);         // valid rows of this chunk
         __syncthreads();                         // previous chunk fully consumed
+        if (ckpt_every > 0 && c0 > bos && (c0 - bos) % ckpt_every == 0) put_ckpt(ck_base + (c0 - bos) / ckpt_every - 1);
         // ---- load q, k, log-decay, the v slice and beta (rows >= nr zero)
         for (int e = tid; e < C * DK; e += kThreads) {
             const int r = e / DK, i = e % DK;
@@ -226,6 +245,7 @@ kda_prefill_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         }
     }
     __syncthreads();
+    if (ckpt_every > 0 && eos > bos && (eos - bos) % ckpt_every == 0) put_ckpt(ck_base + (eos - bos) / ckpt_every - 1);
     if (S_final) {
         for (int e = tid; e < DK * DVT; e += kThreads) {
             const int i = e / DVT, j = e % DVT;
@@ -247,7 +267,7 @@ cudaError_t launch(const kda_host::PrefillArgs& a) {
     kern<<<grid, kThreads, smem, a.stream>>>(
         static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v),
         a.log_alpha, a.beta, a.S0, a.cu_seqlens, a.T_total, a.H, fixed,
-        static_cast<TIn*>(a.O), a.S_final);
+        static_cast<TIn*>(a.O), a.S_final, a.ckpt_every, a.ckpt, a.ckpt_cap);
     const cudaError_t err = cudaGetLastError();
     kda_host::trace_mark(a.stream);
     return err;

@@ -585,7 +585,8 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 __global__ void __launch_bounds__(K2_THREADS, 1)
 kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, int nch_per_seq,
              int c_begin, int c_end, const uint8_t* __restrict__ ws_blocks, const float* __restrict__ S0, int H,
-             bf16* __restrict__ O, float* __restrict__ S_final, int* status) {
+             bf16* __restrict__ O, float* __restrict__ S_final, int ckpt_every, float* __restrict__ ckpt,
+             int ckpt_cap, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     const int tile = blockIdx.x % NTILES, n = blockIdx.x / NTILES, h = blockIdx.y;
@@ -600,6 +601,18 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     // numbered 0 .. nloc - 1 (stage and barrier parities use the local number)
     const int cb = min(c_begin, nch);
     const int nloc = max(0, min(c_end, nch) - cb);
+    // state checkpoints: index of this sequence's first one (block-wide sum)
+    int ck_base = 0;
+    if (ckpt_every > 0)
+        ck_base = use_table ? kda::ckpt_base(n, ckpt_every, [&](int m) { return seq_info[m].y; })
+                            : n * (fixed_len / ckpt_every);
+    // store this thread's 32 state values as checkpoint `idx` (if it fits)
+    auto put_ckpt = [&](int idx, const float* v32, int row_, int col0) {
+        if (idx < 0 || idx >= ckpt_cap) return;
+        float4* dst = reinterpret_cast<float4*>(ckpt + (((size_t)idx * H + h) * DK + row_) * DV + tile * NT + col0);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dst[u] = make_float4(v32[4 * u], v32[4 * u + 1], v32[4 * u + 2], v32[4 * u + 3]);
+    };
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + K2_BAR);
     uint64_t* bar_p = full + K2_NS;
@@ -694,6 +707,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             float s[32];
             kda::tmem_ld32(tS, s);
             kda::tmem_wait_ld();
+            if (ckpt_every > 0 && cb + c > 0 && ((cb + c) * C) % ckpt_every == 0)   // state after (cb + c) chunks
+                put_ckpt(ck_base + (cb + c) * C / ckpt_every - 1, s, row, 32 * half);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
                 *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(row, 32 * half + 8 * cc, 128)) = pack8(s + 8 * cc);
@@ -795,14 +810,19 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         }
         if (nloc > 0) wait(bar_s, (uint32_t)((nloc - 1) & 1));
         kda::tc_fence_after();
-        if (S_final) {
+        const bool end_ckpt = ckpt_every > 0 && nloc > 0 && cb + nloc == nch && len % ckpt_every == 0;
+        if (S_final || end_ckpt) {
             float s[32];
             kda::tmem_ld32(tS, s);
             kda::tmem_wait_ld();
-            float4* dst = reinterpret_cast<float4*>(S_final + (((size_t)n * H + h) * DK + row) * DV + tile * NT +
-                                                    32 * half);
+            if (end_ckpt) put_ckpt(ck_base + len / ckpt_every - 1, s, row, 32 * half);
+            if (S_final) {
+                float4* dst = reinterpret_cast<float4*>(S_final + (((size_t)n * H + h) * DK + row) * DV +
+                                                        tile * NT + 32 * half);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) dst[u] = make_float4(s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]);
+                for (int u = 0; u < 8; ++u)
+                    dst[u] = make_float4(s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]);
+            }
         }
     }
     kda::tc_fence_before();
@@ -922,7 +942,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     auto chain = [&](int c0, int c1, const float* s_in, float* s_out, cudaStream_t st) {
         kda_tc_chain<<<dim3(NTILES * a.n_seq, a.H), K2_THREADS, chain_smem, st>>>(
             seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
-            a.status);
+            a.ckpt_every, a.ckpt, a.ckpt_cap, a.status);
         return cudaGetLastError();
     };
 

@@ -100,6 +100,32 @@ def test_prefill_argument_checks(lib):
     assert _prefill_raw(lib, ws=ctypes.c_void_p(0x100010), ws_bytes=need, **tc) == E.KDA_ERR_WORKSPACE
 
 
+def test_prefill_ckpt_argument_checks(lib):
+    """Checkpoint arguments are checked on the host, before any device work."""
+    E = _lib
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+
+    def call(every=16, ck=P(0x5000), cap=4, n_seq=1, T=64, cu=None, cuh=None, chunk=16):
+        return lib.kda_prefill_ckpt(fake, fake, fake, fake, fake, None, cu, cuh, n_seq, T, 2, 32, 32, chunk,
+                                    _lib.KDA_FP32, P(0x2000), None, every, ck, cap, None, 0, None)
+    assert call(every=0) == E.KDA_ERR_INVALID_ARG
+    assert call(every=24) == E.KDA_ERR_INVALID_ARG                 # not a multiple of the chunk
+    assert call(cap=-1) == E.KDA_ERR_INVALID_ARG
+    assert call(ck=None) == E.KDA_ERR_INVALID_ARG                  # capacity without a buffer
+    assert call(ck=P(0x5004)) == E.KDA_ERR_INVALID_ARG             # not 16-byte aligned
+    assert call(cap=3) == E.KDA_ERR_INVALID_ARG                    # 64 / 16 = 4 checkpoints needed
+    assert call(every=32, cap=1) == E.KDA_ERR_INVALID_ARG
+    assert call(every=16, chunk=128) == E.KDA_ERR_UNSUPPORTED
+    cuh = (ctypes.c_int32 * 3)(0, 40, 64)                          # 40 // 16 + 24 // 16 = 3
+    assert call(n_seq=2, cu=P(0x3000), cuh=cuh, cap=2) == E.KDA_ERR_INVALID_ARG
+    assert call(n_seq=0, T=0, cap=0, ck=None) == E.KDA_OK
+
+
+def test_checkpoint_count():
+    assert _lib.checkpoint_count([0, 15, 16, 40, 64], 16) == 0 + 0 + 1 + 2 + 4
+
+
 def test_decode_argument_checks(lib):
     P = ctypes.c_void_p
     f = P(0x1000)
