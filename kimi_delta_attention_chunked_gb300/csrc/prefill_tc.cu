@@ -39,9 +39,8 @@
 //
 // Precision: MMA operands are bf16 with fp32 accumulation.  The four operands
 // whose rounding dominated the error budget -- INV Diag(beta), M_qk, U0 and U
-// -- are carried as a high and a low bf16 part (U0 as fp32), each product
-// being issued once per part, which leaves the bf16 output rounding as the
-// largest single error term.
+// -- are carried as a high and a low bf16 part (U0 as fp32), which leaves the
+// bf16 output rounding as the largest single error term.
 //
 // Every wait on an asynchronous event is bounded; a wait that runs out records
 // KDA_ERR_TIMEOUT in the status word and the kernel runs to completion.
@@ -63,7 +62,7 @@ constexpr int NTILES = DV / NT;
 constexpr uint32_t WS_A1 = 0;                // [Q_decay; W]  K-major SW128, 128 rows, K = 128 (2 panels)
 constexpr uint32_t WS_KR = 32768;            // K_restore^T   MN-major SW128, K = 64 rows, M = 128 (2 panels)
 constexpr uint32_t WS_MQ = 49152;            // M_qk high and low bf16 parts, each K-major SW128, 64 rows, K = 64
-constexpr uint32_t WS_U0 = 65536;            // U0            fp32 [NTILES][C][NT]
+constexpr uint32_t WS_U0 = 65536;            // U0            fp32 [NTILES][C][NT], 16-byte chunk j of row r at j ^ (r % 8)
 constexpr uint32_t WS_AL = 98304;            // a_last        fp32 [DK]
 constexpr uint32_t WS_BLOCK = 99328;         // 97 KiB
 constexpr uint32_t COPY_BYTES = 32768 + 16384 + 16384 + C * NT * 4 + DK * 4;
@@ -91,15 +90,16 @@ constexpr uint32_t K1_TMEM_COLS = 256;
 constexpr int K2_NS = 2;                     // operand stages in flight
 constexpr uint32_t K2_STAGE = 82944;
 constexpr uint32_t ST_A1 = 0, ST_KR = 32768, ST_MQ = 49152, ST_MQL = 57344, ST_U0 = 65536, ST_AL = 81920;
-constexpr uint32_t K2_SB = K2_NS * K2_STAGE; // S_in bf16, MN-major SW128, K = 128 rows, N = 64
-constexpr uint32_t K2_UB = K2_SB + 16384;    // U high bf16 part, MN-major SW128, K = 64 rows, N = 64
-constexpr uint32_t K2_UBL = K2_UB + 8192;    // U low bf16 part
-constexpr uint32_t K2_BAR = K2_UBL + 8192;   // full[K2_NS], p, s, o, TMEM address
+constexpr uint32_t K2_SB = K2_NS * K2_STAGE; // S_in bf16, MN-major SW128, K = 128 rows, N = 64 (16 KiB used)
+constexpr uint32_t K2_UB = K2_SB + 32768;    // [U_hi | U_lo] bf16, MN-major SW128, K = 64 rows, N = 2 x 64
+constexpr uint32_t K2_XO = K2_UB + 16384;    // M_lo U share of O, bf16 SW128 [64 rows][64]
+constexpr uint32_t K2_BAR = K2_XO + 8192;    // full[K2_NS], p, s, o, TMEM address
 constexpr uint32_t K2_BYTES = K2_BAR + 64;
-constexpr uint32_t K2_TMEM_COLS = 256;       // S: cols [0, 64), P double buffer: [64, 128), [128, 192)
+constexpr uint32_t K2_TMEM_COLS = 512;       // S [0, 64), X [64, 128), P buffers [128, 256), [256, 384)
 
 static_assert(COPY_BYTES <= K2_STAGE, "stage too small");
-static_assert(ST_MQL + 16384 <= K2_STAGE, "M_qk rows 64..127 must stay inside the stage");
+static_assert(ST_MQL == ST_MQ + 8192, "[M_hi; M_lo] is one 128-row operand");
+static_assert(K2_SB % 1024 == 0, "SW128 operands are 1024-byte aligned");
 static_assert(K1_AIL + 16384 <= K1_BWU, "INV rows 64..127 must stay inside the alias region");
 static_assert(K2_BYTES + 1024 <= 232448, "chain smem");
 static_assert(2 * (K1_BYTES + 1024 + 1024) <= 233472, "prep must fit two CTAs per SM");
@@ -554,9 +554,10 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
             kda::tmem_ld32(tmem + ((uint32_t)(32 * (w - 4)) << 16) + 128 + 32 * cb, x);
             kda::tmem_wait_ld();
             const int j = 32 * cb, tile = j / NT;
-            float4* dst = reinterpret_cast<float4*>(blk + WS_U0 + ((size_t)(tile * C + r) * NT + (j % NT)) * 4);
+            float4* dst = reinterpret_cast<float4*>(blk + WS_U0 + (size_t)(tile * C + r) * NT * 4);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) dst[u] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+            for (int u = 0; u < 8; ++u)
+                dst[((j % NT) / 4 + u) ^ (r & 7)] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
         }
     }
     kda::tc_fence_before();
@@ -565,21 +566,41 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
 }
 
 // ============================================================== chain (a4, a5)
-// Warp roles (NT = 64 columns of d_v per CTA):
+// Per CTA: one (sequence, head) pair and NT = 64 columns of d_v.  The high
+// and low bf16 parts of U sit side by side along N where the product allows
+// it.  TMEM columns:
+//   [0, 64)      S, the fp32 state slice (TMEM lane = key channel)
+//   [64, 128)    X, the low-part share K_restore^T U_lo of the state update,
+//                folded into S when the state is next read
+//   [128, 256), [256, 384)  P buffers (chunk parity)
+// MMAs per chunk (20 instructions):
+//   P[:, 0:64]   = [Q_decay; W] S_in              K = 128, N = 64   -> commit(p)
+//   [S | X]     += K_restore^T [U_hi | U_lo]     K = 64,  N = 128  -> commit(s)
+//   P[:, 0:64]  += [M_hi; M_lo] U_hi             K = 64,  N = 64
+//   P[:, 64:128] = [M_hi; M_lo] U_lo             K = 64,  N = 64   -> commit(o)
+// The W rows of P are zeroed once U has been formed, so after the last
+// product lanes 0..63 of P hold Q_decay S + M_hi U and lanes 64..127 hold
+// M_lo U: output row r is the sum of the two 64-column blocks of lanes r and
+// 64 + r.
+// Warp roles:
 //   warps 0-7  conversion warps; warp w reads TMEM lanes 32 (w % 4) .. +31 and
-//              columns 32 (w / 4) .. +31 of each 64-wide TMEM tile.
-//              - all 8: S_in -> bf16 operand, S <- Diag(a_last) S_in   (chunk c)
-//              - lanes 64..127 (warps 2, 3, 6, 7): U = U0 - W S_in     (chunk c)
-//              - lanes 0..63   (warps 0, 1, 4, 5): O rows              (chunk c - 1)
+//              columns 32 (w / 4) .. +31 of each 64-wide block.
+//              - all 8: S_in = S + X -> bf16 operand, S <- Diag(a_last) S_in, X <- 0  (chunk c)
+//              - lanes 64..127 (warps 2, 3, 6, 7): M_lo U share of O (chunk c - 1) -> shared
+//                memory; U = U0 - W S_in -> high/low bf16 operand; W rows of P <- 0           (chunk c)
+//              - lanes 0..63 (warps 0, 1, 4, 5): O rows                                       (chunk c - 1)
 //   warp 8     lane 0 issues every MMA and bulk copy.
-// MMA order per chunk: P[c&1] = [Q_decay; W] S_in -> commit(p);
-// S += K_restore^T U -> commit(s); P[c&1] += M_qk U -> commit(o).  The O
-// product and the O stores run while the next chunk's state is converted.
+// Named barriers: 1 = everyone; 2 = conversion warps arrive, issuer waits
+// (U ready); 3 = lanes 64..127 warps arrive, lanes 0..63 warps wait (O share);
+// 4 = conversion warps, once, before the last chunk's O.
 constexpr int K2_THREADS = 288;
 constexpr int K2_ISSUER_WARP = 8;
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __global__ void __launch_bounds__(K2_THREADS, 1)
@@ -638,8 +659,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     const int quad = w & 3, half = (w >> 2) & 1;
     const int row = 32 * quad + lane;                       // TMEM lane = state row / P row
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-    const uint32_t tS = tmem + lane_off + 32 * half;        // this warp's 32 state columns
-    const uint32_t tP0 = tmem + lane_off + 64 + 32 * half;  // P buffer 0 (P buffer 1 at +64)
+    const uint32_t tS = tmem + lane_off + 32 * half;        // this warp's 32 state columns (X at +64)
+    auto tP = [&](int c) { return tmem + lane_off + 128 + 128 * (c & 1) + 32 * half; };   // S_hi part; S_lo at +64
 
     auto issue = [&](int c) {
         const int st = c % K2_NS;
@@ -656,7 +677,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         if (!kda::mbar_wait(b, parity, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
     };
 
-    // initial state slice -> TMEM; first stages in flight
+    // initial state slice -> TMEM (X = 0); first stages in flight
     if (!issuer) {
         float s[32];
         if (S0) {
@@ -672,6 +693,9 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             for (int u = 0; u < 32; ++u) s[u] = 0.f;
         }
         kda::tmem_st32(tS, s);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) s[u] = 0.f;
+        kda::tmem_st32(tS + 64, s);
         kda::tmem_wait_st();
     } else if (lane == 0) {
         for (int c = 0; c < min(K2_NS, nloc); ++c) issue(c);
@@ -681,18 +705,49 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     kda::tc_fence_after();
 
     const uint32_t sSB = kda::smem_u32(sm + K2_SB), sUB = kda::smem_u32(sm + K2_UB);
-    const uint32_t sUBL = kda::smem_u32(sm + K2_UBL);
-    auto o_epilogue = [&](int c) {                          // warps 0, 1, 4, 5: rows 0..63
-        wait(bar_o, (uint32_t)(c & 1));
+    // O of chunk c, lanes 64..127 (after bar_o(c)): M_lo U -> shared memory (bf16;
+    // it is a low-order correction), then release the lanes 0..63 warps
+    auto o_low_share = [&](int c) {
         kda::tc_fence_after();
-        float o[32];
-        kda::tmem_ld32(tP0 + 64 * (c & 1), o);
+        float a[32], b[32];
+        kda::tmem_ld32(tP(c), a);
+        kda::tmem_ld32(tP(c) + 64, b);
         kda::tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 32; ++u) a[u] += b[u];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+            *reinterpret_cast<uint4*>(sm + K2_XO + kda::sw128(row - 64, 32 * half + 8 * cc, 64)) = pack8(a + 8 * cc);
+        kda::tc_fence_before();
+        named_bar_arrive(3, 256);
+    };
+    // O of chunk c, lanes 0..63 (after bar_o(c)): both blocks + the M_lo U share
+    auto o_rows = [&](int c) {
+        kda::tc_fence_after();
+        float a[32], b[32];
+        kda::tmem_ld32(tP(c), a);
+        kda::tmem_ld32(tP(c) + 64, b);
+        kda::tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 32; ++u) a[u] += b[u];
+        kda::tc_fence_before();
+        named_bar_sync(3, 256);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const uint4 x = *reinterpret_cast<const uint4*>(sm + K2_XO + kda::sw128(row, 32 * half + 8 * cc, 64));
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = kda::unpack_bf16x2(xs[u]);
+                a[8 * cc + 2 * u] += f.x;
+                a[8 * cc + 2 * u + 1] += f.y;
+            }
+        }
         if (row < len - (cb + c) * C) {
             uint4* dst = reinterpret_cast<uint4*>(O + ((size_t)(bos + (cb + c) * C + row) * H + h) * DV + tile * NT +
                                                   32 * half);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) dst[cc] = pack8(o + 8 * cc);
+            for (int cc = 0; cc < 4; ++cc) dst[cc] = pack8(a + 8 * cc);
         }
     };
 
@@ -700,55 +755,67 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         const int st = c % K2_NS;
         uint8_t* stage = sm + st * K2_STAGE;
         if (!issuer) {
-            // ---- S_in -> bf16 operand; TMEM state <- Diag(a_last) S_in
+            // ---- S_in = S + X -> bf16 operand; S <- Diag(a_last) S_in, X <- 0
             wait(full + st, (uint32_t)((c / K2_NS) & 1));
             if (c > 0) wait(bar_s, (uint32_t)((c - 1) & 1));
             kda::tc_fence_after();
-            float s[32];
+            float s[32], x[32];
             kda::tmem_ld32(tS, s);
+            kda::tmem_ld32(tS + 64, x);
             kda::tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) s[u] += x[u];
             if (ckpt_every > 0 && cb + c > 0 && ((cb + c) * C) % ckpt_every == 0)   // state after (cb + c) chunks
                 put_ckpt(ck_base + (cb + c) * C / ckpt_every - 1, s, row, 32 * half);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
                 *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(row, 32 * half + 8 * cc, 128)) = pack8(s + 8 * cc);
-            const float al = reinterpret_cast<const float*>(stage + ST_AL)[row];
-#pragma unroll
-            for (int u = 0; u < 32; ++u) s[u] *= al;
-            kda::tmem_st32(tS, s);
-            kda::tmem_wait_st();
             kda::fence_proxy_async_smem();
             kda::tc_fence_before();
             named_bar_sync(1, K2_THREADS);
+            // S <- Diag(a_last) S_in, X <- 0 while the P product runs (done before barrier 2)
+            const float al = reinterpret_cast<const float*>(stage + ST_AL)[row];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) { s[u] *= al; x[u] = 0.f; }
+            kda::tmem_st32(tS, s);
+            kda::tmem_st32(tS + 64, x);
+            kda::tmem_wait_st();
+            // bar_o(c - 1) is observed by every conversion warp before barrier 2
+            // lets bar_o(c) be committed (a parity wait cannot skip a phase)
+            if (c > 0) wait(bar_o, (uint32_t)((c - 1) & 1));
             if (quad >= 2) {
-                // ---- U = U0 - W S_in -> high + low bf16 operands (rows 64..127 of P)
+                // ---- U = U0 - W S_in -> high/low bf16 operand; W rows of P <- 0
                 const int r = row - 64;
                 wait(bar_p, (uint32_t)(c & 1));
                 kda::tc_fence_after();
-                float pw[32];
-                kda::tmem_ld32(tP0 + 64 * (c & 1), pw);
+                float ph[32];
+                kda::tmem_ld32(tP(c), ph);
                 kda::tmem_wait_ld();
-                const float4* u0 = reinterpret_cast<const float4*>(stage + ST_U0 + (r * NT + 32 * half) * 4);
+                const float4* u0 = reinterpret_cast<const float4*>(stage + ST_U0 + r * NT * 4);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    const float4 x0 = u0[2 * cc], x1 = u0[2 * cc + 1];
+                    const float4 x0 = u0[(8 * half + 2 * cc) ^ (r & 7)], x1 = u0[(8 * half + 2 * cc + 1) ^ (r & 7)];
                     float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w}, lo[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) f[u] -= pw[8 * cc + u];
+                    for (int u = 0; u < 8; ++u) f[u] -= ph[8 * cc + u];
                     split8(f, lo);
                     const uint32_t off = kda::sw128(r, 32 * half + 8 * cc, 64);
                     *reinterpret_cast<uint4*>(sm + K2_UB + off) = pack8(f);
-                    *reinterpret_cast<uint4*>(sm + K2_UBL + off) = pack8(lo);
+                    *reinterpret_cast<uint4*>(sm + K2_UB + 8192 + off) = pack8(lo);
                 }
+#pragma unroll
+                for (int u = 0; u < 32; ++u) ph[u] = 0.f;
+                kda::tmem_st32(tP(c), ph);
+                kda::tmem_wait_st();
                 kda::fence_proxy_async_smem();
                 kda::tc_fence_before();
-            } else if (c > 0) {
-                o_epilogue(c - 1);                          // overlaps the U conversion
+                named_bar_arrive(2, K2_THREADS);
+                if (c > 0) o_low_share(c - 1);              // O of chunk c - 1: M_lo U share
+            } else {
                 kda::tc_fence_before();
+                named_bar_arrive(2, K2_THREADS);
+                if (c > 0) o_rows(c - 1);                   // O of chunk c - 1 (overlaps the U conversion)
             }
-            // all conversion warps: the O warps must have waited for bar_o(c - 1)
-            // before bar_o(c) can be committed (a parity wait cannot skip a phase)
-            named_bar_sync(2, K2_THREADS);
         } else {
             named_bar_sync(1, K2_THREADS);
             if (lane == 0) {                                // P = [Q_decay; W] S_in
@@ -760,7 +827,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 for (int s = 0; s < 8; ++s) {
                     const uint64_t ad = kda::sw128_desc(sA1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
                     const uint64_t bd = kda::sw128_desc(sSB + s * 2048, 16384, 1024);
-                    kda::umma_bf16(tmem + 64 + 64 * (c & 1), ad, bd, idesc, s > 0 ? 1u : 0u);
+                    kda::umma_bf16(tmem + 128 + 128 * (c & 1), ad, bd, idesc, s > 0 ? 1u : 0u);
                 }
                 kda::umma_commit(bar_p);
                 // the previous chunk's stage is free once its last MMA (the O product) is done
@@ -773,30 +840,24 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             named_bar_sync(2, K2_THREADS);
             if (lane == 0) {
                 kda::tc_fence_after();
-                const uint32_t sKR = kda::smem_u32(stage + ST_KR);
-                const uint32_t sMQ = kda::smem_u32(stage + ST_MQ), sMQL = kda::smem_u32(stage + ST_MQL);
-                const uint32_t id_s = kda::idesc_bf16(128, NT, 1, 1);
+                const uint32_t sKR = kda::smem_u32(stage + ST_KR), sMQ = kda::smem_u32(stage + ST_MQ);
+                const uint32_t id_s = kda::idesc_bf16(128, 2 * NT, 1, 1);
                 const uint32_t id_o = kda::idesc_bf16(128, NT, 0, 1);
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {      // S += K_restore^T (U_hi + U_lo)
-                    const uint32_t sU = part ? sUBL : sUB;
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const uint64_t ad = kda::sw128_desc(sKR + s * 2048, 8192, 1024);
-                        const uint64_t bd = kda::sw128_desc(sU + s * 2048, 8192, 1024);
-                        kda::umma_bf16(tmem, ad, bd, id_s, 1u);
-                    }
+                for (int s = 0; s < 4; ++s) {               // [S | X] += K_restore^T [U_hi | U_lo]
+                    const uint64_t ad = kda::sw128_desc(sKR + s * 2048, 8192, 1024);
+                    const uint64_t bd = kda::sw128_desc(sUB + s * 2048, 8192, 1024);
+                    kda::umma_bf16(tmem, ad, bd, id_s, 1u);
                 }
                 kda::umma_commit(bar_s);
 #pragma unroll
-                for (int part = 0; part < 3; ++part) {      // P_q += M_hi U_hi + M_hi U_lo + M_lo U_hi
-                    const uint32_t sA = part == 2 ? sMQL : sMQ;
-                    const uint32_t sU = part == 1 ? sUBL : sUB;
+                for (int part = 0; part < 2; ++part) {      // P += [M_hi; M_lo] U_hi;  P' = [M_hi; M_lo] U_lo
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
-                        const uint64_t ad = kda::sw128_desc(sA + s * 32, 16, 1024);
-                        const uint64_t bd = kda::sw128_desc(sU + s * 2048, 8192, 1024);
-                        kda::umma_bf16(tmem + 64 + 64 * (c & 1), ad, bd, id_o, 1u);
+                        const uint64_t ad = kda::sw128_desc(sMQ + s * 32, 16, 1024);
+                        const uint64_t bd = kda::sw128_desc(sUB + part * 8192 + s * 2048, 8192, 1024);
+                        kda::umma_bf16(tmem + 128 + 128 * (c & 1) + 64 * part, ad, bd, id_o,
+                                       (part == 0 || s > 0) ? 1u : 0u);
                     }
                 }
                 kda::umma_commit(bar_o);
@@ -805,16 +866,24 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         }
     }
     if (!issuer) {
-        if (quad < 2 && nloc > 0) {
-            o_epilogue(nloc - 1);
+        if (nloc > 0) {
+            // barrier 3 must not see two arrivals of the lanes 64..127 warps before
+            // the lanes 0..63 warps have passed it for chunk nloc - 2
+            named_bar_sync(4, 256);
+            wait(bar_o, (uint32_t)((nloc - 1) & 1));
+            if (quad >= 2) o_low_share(nloc - 1);
+            else o_rows(nloc - 1);
+            wait(bar_s, (uint32_t)((nloc - 1) & 1));
         }
-        if (nloc > 0) wait(bar_s, (uint32_t)((nloc - 1) & 1));
         kda::tc_fence_after();
         const bool end_ckpt = ckpt_every > 0 && nloc > 0 && cb + nloc == nch && len % ckpt_every == 0;
         if (S_final || end_ckpt) {
-            float s[32];
+            float s[32], x[32];
             kda::tmem_ld32(tS, s);
+            kda::tmem_ld32(tS + 64, x);
             kda::tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) s[u] += x[u];
             if (end_ckpt) put_ckpt(ck_base + len / ckpt_every - 1, s, row, 32 * half);
             if (S_final) {
                 float4* dst = reinterpret_cast<float4*>(S_final + (((size_t)n * H + h) * DK + row) * DV +
