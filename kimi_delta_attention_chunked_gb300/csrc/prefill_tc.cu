@@ -10,7 +10,7 @@
 // Everything that does not depend on S_in is computed for all chunks in
 // parallel; only the state pass is sequential.  Two kernels:
 //
-//  kda_tc_prep   one CTA per (chunk, head), fully parallel.
+//  kda_tc_prep   persistent, two CTAs per SM, one (chunk, head) item at a time.
 //      a1  gate prep: fp32 cumulative log-decay, then bf16 MMA operands.
 //          K_inv = k / a would overflow (|cumsum| reaches 5 * 64 = 320 under
 //          the (-5, 0) log-decay bound of the "LLM architecture at trillion
@@ -270,31 +270,35 @@ __global__ void __launch_bounds__(256, 2)
 kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
             const float* __restrict__ g, const float* __restrict__ beta, int H, int use_table,
             int fixed_len, int nch_per_seq, const int4* __restrict__ chunk_info,
-            const int4* __restrict__ seq_info, int j_begin, int j_count,
+            const int4* __restrict__ seq_info, int j_begin, int j_count, int n_x,
             uint8_t* __restrict__ ws_blocks, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
-    // this launch covers chunks j_begin .. j_begin + j_count - 1 of every sequence:
-    // equal lengths -> grid.x = n_seq * j_count; chunk table -> grid.x = chunk slots
-    const int h = blockIdx.y;
-    int tok0, nrows, slot;
-    if (!use_table) {
-        const int n = blockIdx.x / j_count, j = j_begin + blockIdx.x % j_count;
-        if (j >= nch_per_seq) return;
-        slot = n * nch_per_seq + j;
-        tok0 = n * fixed_len + j * C;
-        nrows = min(C, fixed_len - j * C);
-    } else {
-        slot = blockIdx.x;
-        const int4 ci = chunk_info[slot];
-        if (ci.z < 0) return;
-        const int j = slot - seq_info[ci.z].z;
-        if (j < j_begin || j >= j_begin + j_count) return;
-        tok0 = ci.x;
-        nrows = ci.y;
-    }
-    if (nrows <= 0) return;
-    uint8_t* blk = ws_blocks + ((size_t)slot * H + h) * WS_BLOCK;
+    // Persistent: this CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ... of
+    // the n_x * H (chunk, head) items, head fastest.  The launch covers chunks
+    // j_begin .. j_begin + j_count - 1 of every sequence: equal lengths ->
+    // n_x = n_seq * j_count; chunk table -> n_x = chunk slots.
+    auto item = [&](long long it, int& tok0, int& nrows, int& slot, int& h) -> bool {
+        const int x = (int)(it / H);
+        h = (int)(it % H);
+        if (!use_table) {
+            const int n = x / j_count, j = j_begin + x % j_count;
+            if (j >= nch_per_seq) return false;
+            slot = n * nch_per_seq + j;
+            tok0 = n * fixed_len + j * C;
+            nrows = min(C, fixed_len - j * C);
+        } else {
+            slot = x;
+            const int4 ci = chunk_info[slot];
+            if (ci.z < 0) return false;
+            const int j = slot - seq_info[ci.z].z;
+            if (j < j_begin || j >= j_begin + j_count) return false;
+            tok0 = ci.x;
+            nrows = ci.y;
+        }
+        return nrows > 0;
+    };
+    const long long n_items = (long long)n_x * H;
 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + K1_BAR);
@@ -312,256 +316,263 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
     kda::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // ---------------- a1: loads and per-block cumulative log-decay
-    const int p = w >> 2, b = w & 3;          // channel panel, row block
-    const int ch = 64 * p + 2 * lane;          // this thread's two channels
-    float G0[16], G1[16], bt[16];
-    uint32_t qv[16], kv[16];
-#pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-        const int r = 16 * b + rr;
-        const bool ok = r < nrows;
-        const size_t tok = (size_t)tok0 + r;
-        const size_t off = (tok * H + h) * DK + ch;
-        float2 gg = ok ? *reinterpret_cast<const float2*>(g + off) : make_float2(0.f, 0.f);
-        G0[rr] = gg.x;
-        G1[rr] = gg.y;
-        qv[rr] = ok ? *reinterpret_cast<const uint32_t*>(q + off) : 0u;
-        kv[rr] = ok ? *reinterpret_cast<const uint32_t*>(k + off) : 0u;
-        bt[rr] = ok ? beta[tok * H + h] : 0.f;
-    }
-    // V slice -> right half of the [K_decay | V] operand (MN-major)
-    for (int e = tid; e < C * (DV / 8); e += 256) {
-        const int t = e >> 4, cc = e & 15;
-        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (t < nrows) x = *reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + t) * H + h) * DV + 8 * cc);
-        *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) = x;
-    }
-#pragma unroll
-    for (int rr = 1; rr < 16; ++rr) { G0[rr] += G0[rr - 1]; G1[rr] += G1[rr - 1]; }
-    float* tot = reinterpret_cast<float*>(sm + K1_TOT);
-    float* first = reinterpret_cast<float*>(sm + K1_FIRST);
-    float* beta_s = reinterpret_cast<float*>(sm + K1_BETA);
-    tot[b * 128 + ch] = G0[15];
-    tot[b * 128 + ch + 1] = G1[15];
-    first[b * 128 + ch] = G0[0];
-    first[b * 128 + ch + 1] = G1[0];
-    if (p == 0 && lane == 0) {
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) beta_s[16 * b + rr] = bt[rr];
-    }
-    __syncthreads();
+    for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
+        int tok0, nrows, slot, h;
+        if (!item(it, tok0, nrows, slot, h)) continue;
+        uint8_t* blk = ws_blocks + ((size_t)slot * H + h) * WS_BLOCK;
 
-    // global cumulative log-decay at each block start (Gs) and at the chunk end
-    float Gs0[4], Gs1[4], acc0 = 0.f, acc1 = 0.f;
+        // ---------------- a1: loads and per-block cumulative log-decay
+        const int p = w >> 2, b = w & 3;          // channel panel, row block
+        const int ch = 64 * p + 2 * lane;          // this thread's two channels
+        float G0[16], G1[16], bt[16];
+        uint32_t qv[16], kv[16];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        Gs0[m] = acc0 + first[m * 128 + ch];
-        Gs1[m] = acc1 + first[m * 128 + ch + 1];
-        acc0 += tot[m * 128 + ch];
-        acc1 += tot[m * 128 + ch + 1];
-    }
-    float myG0 = Gs0[0], myG1 = Gs1[0];
+        for (int rr = 0; rr < 16; ++rr) {
+            const int r = 16 * b + rr;
+            const bool ok = r < nrows;
+            const size_t tok = (size_t)tok0 + r;
+            const size_t off = (tok * H + h) * DK + ch;
+            float2 gg = ok ? *reinterpret_cast<const float2*>(g + off) : make_float2(0.f, 0.f);
+            G0[rr] = gg.x;
+            G1[rr] = gg.y;
+            qv[rr] = ok ? *reinterpret_cast<const uint32_t*>(q + off) : 0u;
+            kv[rr] = ok ? *reinterpret_cast<const uint32_t*>(k + off) : 0u;
+            bt[rr] = ok ? beta[tok * H + h] : 0.f;
+        }
+        // V slice -> right half of the [K_decay | V] operand (MN-major)
+        for (int e = tid; e < C * (DV / 8); e += 256) {
+            const int t = e >> 4, cc = e & 15;
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (t < nrows) x = *reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + t) * H + h) * DV + 8 * cc);
+            *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) = x;
+        }
 #pragma unroll
-    for (int m = 1; m < 4; ++m)
-        if (m == b) { myG0 = Gs0[m]; myG1 = Gs1[m]; }
-    const float ap0 = __expf(myG0), ap1 = __expf(myG1);              // a at the block start
-    const float R0 = __expf(acc0 - myG0), R1 = __expf(acc1 - myG1);  // a_last / a(block start)
-    float f0[4], f1[4];                                              // a(p_m) / a(p_b), m > b
+        for (int rr = 1; rr < 16; ++rr) { G0[rr] += G0[rr - 1]; G1[rr] += G1[rr - 1]; }
+        float* tot = reinterpret_cast<float*>(sm + K1_TOT);
+        float* first = reinterpret_cast<float*>(sm + K1_FIRST);
+        float* beta_s = reinterpret_cast<float*>(sm + K1_BETA);
+        tot[b * 128 + ch] = G0[15];
+        tot[b * 128 + ch + 1] = G1[15];
+        first[b * 128 + ch] = G0[0];
+        first[b * 128 + ch + 1] = G1[0];
+        if (p == 0 && lane == 0) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m) { f0[m] = __expf(Gs0[m] - myG0); f1[m] = __expf(Gs1[m] - myG1); }
-    if (b == 0) {
-        *reinterpret_cast<float2*>(blk + WS_AL + 4 * ch) = make_float2(__expf(acc0), __expf(acc1));
-    }
+            for (int rr = 0; rr < 16; ++rr) beta_s[16 * b + rr] = bt[rr];
+        }
+        __syncthreads();
 
-    // ---------------- a1: operands
-#pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-        const int r = 16 * b + rr;
-        const float e0 = __expf(G0[rr] - G0[0]), e1 = __expf(G1[rr] - G1[0]);   // <= 1
-        const float c0 = __fdividef(1.f, e0), c1 = __fdividef(1.f, e1);         // >= 1, <= e^75
-        const float2 qf = kda::unpack_bf16x2(qv[rr]);
-        const float2 kf = kda::unpack_bf16x2(kv[rr]);
-        const float be = bt[rr];
-        const float qt0 = qf.x * e0, qt1 = qf.y * e1;            // q~ (row factor)
-        const float kh0 = be * kf.x * e0, kh1 = be * kf.y * e1;  // k^ = beta k (row factor)
-        const float kt0 = kf.x * c0, kt1 = kf.y * c1;            // k (column factor, own block)
-        st_shared_u32(sm + K1_AG + kda::sw128(32 * b + rr, ch, 128), kda::pack_bf16x2(qt0, qt1));
-        st_shared_u32(sm + K1_AG + kda::sw128(32 * b + 16 + rr, ch, 128), kda::pack_bf16x2(kh0, kh1));
+        // global cumulative log-decay at each block start (Gs) and at the chunk end
+        float Gs0[4], Gs1[4], acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            if (m >= b) {
-                const float s0 = (m == b) ? 1.f : f0[m], s1 = (m == b) ? 1.f : f1[m];
-                st_shared_u32(sm + K1_BG + kda::sw128(8 * m * (m + 1) + r, ch, 160),
-                              kda::pack_bf16x2(kt0 * s0, kt1 * s1));
-            }
+            Gs0[m] = acc0 + first[m * 128 + ch];
+            Gs1[m] = acc1 + first[m * 128 + ch + 1];
+            acc0 += tot[m * 128 + ch];
+            acc1 += tot[m * 128 + ch + 1];
         }
-        // Q_decay -> rows 0..63 of the [Q_decay; W] image
-        *reinterpret_cast<uint32_t*>(blk + WS_A1 + kda::sw128(r, ch, 128)) = kda::pack_bf16x2(qt0 * ap0, qt1 * ap1);
-        // K_decay -> left half of the [K_decay | V] operand
-        st_shared_u32(sm + K1_BWU + kda::sw128(r, ch, 64),
-                      kda::pack_bf16x2(kf.x * e0 * ap0, kf.y * e1 * ap1));
-        // K_restore -> K_restore^T image (MN-major: row = token, contiguous = channel)
-        *reinterpret_cast<uint32_t*>(blk + WS_KR + kda::sw128(r, ch, 64)) = kda::pack_bf16x2(kt0 * R0, kt1 * R1);
-    }
-    kda::fence_proxy_async_smem();
-    kda::tc_fence_before();
-    __syncthreads();
+        float myG0 = Gs0[0], myG1 = Gs1[0];
+#pragma unroll
+        for (int m = 1; m < 4; ++m)
+            if (m == b) { myG0 = Gs0[m]; myG1 = Gs1[m]; }
+        const float ap0 = __expf(myG0), ap1 = __expf(myG1);              // a at the block start
+        const float R0 = __expf(acc0 - myG0), R1 = __expf(acc1 - myG1);  // a_last / a(block start)
+        float f0[4], f1[4];                                              // a(p_m) / a(p_b), m > b
+#pragma unroll
+        for (int m = 0; m < 4; ++m) { f0[m] = __expf(Gs0[m] - myG0); f1[m] = __expf(Gs1[m] - myG1); }
+        if (b == 0) {
+            *reinterpret_cast<float2*>(blk + WS_AL + 4 * ch) = make_float2(__expf(acc0), __expf(acc1));
+        }
 
-    // ---------------- a2: Gram MMAs: all 128 rows against the 160 stacked B rows
-    // (row block b's products sit in columns [8b(b+1), 8b(b+1) + 16(b+1)))
-    if (tid == 0) {
+        // ---------------- a1: operands
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+            const int r = 16 * b + rr;
+            const float e0 = __expf(G0[rr] - G0[0]), e1 = __expf(G1[rr] - G1[0]);   // <= 1
+            const float c0 = __fdividef(1.f, e0), c1 = __fdividef(1.f, e1);         // >= 1, <= e^75
+            const float2 qf = kda::unpack_bf16x2(qv[rr]);
+            const float2 kf = kda::unpack_bf16x2(kv[rr]);
+            const float be = bt[rr];
+            const float qt0 = qf.x * e0, qt1 = qf.y * e1;            // q~ (row factor)
+            const float kh0 = be * kf.x * e0, kh1 = be * kf.y * e1;  // k^ = beta k (row factor)
+            const float kt0 = kf.x * c0, kt1 = kf.y * c1;            // k (column factor, own block)
+            st_shared_u32(sm + K1_AG + kda::sw128(32 * b + rr, ch, 128), kda::pack_bf16x2(qt0, qt1));
+            st_shared_u32(sm + K1_AG + kda::sw128(32 * b + 16 + rr, ch, 128), kda::pack_bf16x2(kh0, kh1));
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                if (m >= b) {
+                    const float s0 = (m == b) ? 1.f : f0[m], s1 = (m == b) ? 1.f : f1[m];
+                    st_shared_u32(sm + K1_BG + kda::sw128(8 * m * (m + 1) + r, ch, 160),
+                                  kda::pack_bf16x2(kt0 * s0, kt1 * s1));
+                }
+            }
+            // Q_decay -> rows 0..63 of the [Q_decay; W] image
+            *reinterpret_cast<uint32_t*>(blk + WS_A1 + kda::sw128(r, ch, 128)) = kda::pack_bf16x2(qt0 * ap0, qt1 * ap1);
+            // K_decay -> left half of the [K_decay | V] operand
+            st_shared_u32(sm + K1_BWU + kda::sw128(r, ch, 64),
+                          kda::pack_bf16x2(kf.x * e0 * ap0, kf.y * e1 * ap1));
+            // K_restore -> K_restore^T image (MN-major: row = token, contiguous = channel)
+            *reinterpret_cast<uint32_t*>(blk + WS_KR + kda::sw128(r, ch, 64)) = kda::pack_bf16x2(kt0 * R0, kt1 * R1);
+        }
+        kda::fence_proxy_async_smem();
+        kda::tc_fence_before();
+        __syncthreads();
+
+        // ---------------- a2: Gram MMAs: all 128 rows against the 160 stacked B rows
+        // (row block b's products sit in columns [8b(b+1), 8b(b+1) + 16(b+1)))
+        if (tid == 0) {
+            kda::tc_fence_after();
+            const uint32_t sAG = kda::smem_u32(sm + K1_AG), sBG = kda::smem_u32(sm + K1_BG);
+            const uint32_t idesc = kda::idesc_bf16(128, 160, 0, 0);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t ad = kda::sw128_desc(sAG + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+                const uint64_t bd = kda::sw128_desc(sBG + (s >> 2) * 20480 + (s & 3) * 32, 16, 1024);
+                kda::umma_bf16(tmem, ad, bd, idesc, s > 0 ? 1u : 0u);
+            }
+            kda::umma_commit(bar);
+        }
+        if (!kda::mbar_wait(bar, 0, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
         kda::tc_fence_after();
-        const uint32_t sAG = kda::smem_u32(sm + K1_AG), sBG = kda::smem_u32(sm + K1_BG);
-        const uint32_t idesc = kda::idesc_bf16(128, 160, 0, 0);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const uint64_t ad = kda::sw128_desc(sAG + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
-            const uint64_t bd = kda::sw128_desc(sBG + (s >> 2) * 20480 + (s & 3) * 32, 16, 1024);
-            kda::umma_bf16(tmem, ad, bd, idesc, s > 0 ? 1u : 0u);
-        }
-        kda::umma_commit(bar);
-    }
-    if (!kda::mbar_wait(bar, 0, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
-    kda::tc_fence_after();
 
-    float* LS = reinterpret_cast<float*>(sm + K1_LS);
-    float* IS = reinterpret_cast<float*>(sm + K1_IS);
-    float* XS = reinterpret_cast<float*>(sm + K1_XS);
-    if (w == 0) gram_epilogue<0>(tmem, lane, blk + WS_MQ, LS);
-    else if (w == 1) gram_epilogue<1>(tmem, lane, blk + WS_MQ, LS);
-    else if (w == 2) gram_epilogue<2>(tmem, lane, blk + WS_MQ, LS);
-    else if (w == 3) gram_epilogue<3>(tmem, lane, blk + WS_MQ, LS);
-    kda::tc_fence_before();
-    __syncthreads();
+        float* LS = reinterpret_cast<float*>(sm + K1_LS);
+        float* IS = reinterpret_cast<float*>(sm + K1_IS);
+        float* XS = reinterpret_cast<float*>(sm + K1_XS);
+        if (w == 0) gram_epilogue<0>(tmem, lane, blk + WS_MQ, LS);
+        else if (w == 1) gram_epilogue<1>(tmem, lane, blk + WS_MQ, LS);
+        else if (w == 2) gram_epilogue<2>(tmem, lane, blk + WS_MQ, LS);
+        else if (w == 3) gram_epilogue<3>(tmem, lane, blk + WS_MQ, LS);
+        kda::tc_fence_before();
+        __syncthreads();
 
-    // ---------------- a3: INV = (I + L)^-1, by 16x16 blocks
-    // (1) diagonal blocks D_b by forward substitution (warps 0-3); zero the blocks above
-    if (w < 4) {
-        if (lane < 16) {                       // diagonal block w, column `lane`
-            const int o = 16 * w, j = lane;
-            float x[16];
+        // ---------------- a3: INV = (I + L)^-1, by 16x16 blocks
+        // (1) diagonal blocks D_b by forward substitution (warps 0-3); zero the blocks above
+        if (w < 4) {
+            if (lane < 16) {                       // diagonal block w, column `lane`
+                const int o = 16 * w, j = lane;
+                float x[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {              // four partial sums shorten the FMA chain
-                float a[4] = {(r == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
+                for (int r = 0; r < 16; ++r) {              // four partial sums shorten the FMA chain
+                    float a[4] = {(r == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int t = 0; t < r; ++t) a[t & 3] = fmaf(-LS[(o + r) * LDS_ + o + t], x[t], a[t & 3]);
-                x[r] = (a[0] + a[1]) + (a[2] + a[3]);
+                    for (int t = 0; t < r; ++t) a[t & 3] = fmaf(-LS[(o + r) * LDS_ + o + t], x[t], a[t & 3]);
+                    x[r] = (a[0] + a[1]) + (a[2] + a[3]);
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) IS[(o + r) * LDS_ + o + j] = x[r];
             }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) IS[(o + r) * LDS_ + o + j] = x[r];
-        }
-    } else {
-        for (int e = tid - 128; e < 6 * 256; e += 128) {
-            const int pb = e >> 8, idx = e & 255;
-            const int bi = pb < 3 ? 0 : (pb < 5 ? 1 : 2);
-            const int bj = pb < 3 ? pb + 1 : (pb < 5 ? pb - 1 : 3);
-            IS[(16 * bi + (idx >> 4)) * LDS_ + 16 * bj + (idx & 15)] = 0.f;
-        }
-    }
-    __syncthreads();
-    auto blkL = [&](int bi, int bj) { return LS + (16 * bi) * LDS_ + 16 * bj; };
-    auto blkI = [&](int bi, int bj) { return IS + (16 * bi) * LDS_ + 16 * bj; };
-    // (2) INV_10 = -D1 (L10 D0), INV_32 = -D3 (L32 D2)   (warps 0, 1)
-    if (w < 2) {
-        const int b0 = 2 * w;
-        float acc[8];
-        mm16(acc, blkL(b0 + 1, b0), LDS_, blkI(b0, b0), LDS_, lane, false);
-        st16(XS + 256 * w, 16, acc, lane, 1.f);
-        __syncwarp();
-        mm16(acc, blkI(b0 + 1, b0 + 1), LDS_, XS + 256 * w, 16, lane, false);
-        st16(blkI(b0 + 1, b0), LDS_, acc, lane, -1.f);
-    }
-    __syncthreads();
-    // (3) X = L_[23][01] D_[01]:  X_i0 = L_{2+i,0} D0 + L_{2+i,1} INV_10,  X_i1 = L_{2+i,1} D1   (warps 0-3)
-    if (w < 4) {
-        const int xi = w >> 1, xj = w & 1;
-        float acc[8];
-        if (xj == 0) {
-            mm16(acc, blkL(2 + xi, 0), LDS_, blkI(0, 0), LDS_, lane, false);
-            mm16(acc, blkL(2 + xi, 1), LDS_, blkI(1, 0), LDS_, lane, true);
         } else {
-            mm16(acc, blkL(2 + xi, 1), LDS_, blkI(1, 1), LDS_, lane, false);
+            for (int e = tid - 128; e < 6 * 256; e += 128) {
+                const int pb = e >> 8, idx = e & 255;
+                const int bi = pb < 3 ? 0 : (pb < 5 ? 1 : 2);
+                const int bj = pb < 3 ? pb + 1 : (pb < 5 ? pb - 1 : 3);
+                IS[(16 * bi + (idx >> 4)) * LDS_ + 16 * bj + (idx & 15)] = 0.f;
+            }
         }
-        st16(XS + 256 * w, 16, acc, lane, 1.f);
-    }
-    __syncthreads();
-    // (4) INV_[23][01] = -D_[23] X:  Y_0j = D2 X_0j,  Y_1j = INV_32 X_0j + D3 X_1j   (warps 0-3)
-    if (w < 4) {
-        const int yi = w >> 1, yj = w & 1;
-        float acc[8];
-        if (yi == 0) {
-            mm16(acc, blkI(2, 2), LDS_, XS + 256 * yj, 16, lane, false);
-        } else {
-            mm16(acc, blkI(3, 2), LDS_, XS + 256 * yj, 16, lane, false);
-            mm16(acc, blkI(3, 3), LDS_, XS + 256 * (2 + yj), 16, lane, true);
+        __syncthreads();
+        auto blkL = [&](int bi, int bj) { return LS + (16 * bi) * LDS_ + 16 * bj; };
+        auto blkI = [&](int bi, int bj) { return IS + (16 * bi) * LDS_ + 16 * bj; };
+        // (2) INV_10 = -D1 (L10 D0), INV_32 = -D3 (L32 D2)   (warps 0, 1)
+        if (w < 2) {
+            const int b0 = 2 * w;
+            float acc[8];
+            mm16(acc, blkL(b0 + 1, b0), LDS_, blkI(b0, b0), LDS_, lane, false);
+            st16(XS + 256 * w, 16, acc, lane, 1.f);
+            __syncwarp();
+            mm16(acc, blkI(b0 + 1, b0 + 1), LDS_, XS + 256 * w, 16, lane, false);
+            st16(blkI(b0 + 1, b0), LDS_, acc, lane, -1.f);
         }
-        st16(blkI(2 + yi, yj), LDS_, acc, lane, -1.f);
-    }
-    __syncthreads();
-    // INV Diag(beta) -> K-major A operand as high + low bf16 parts
+        __syncthreads();
+        // (3) X = L_[23][01] D_[01]:  X_i0 = L_{2+i,0} D0 + L_{2+i,1} INV_10,  X_i1 = L_{2+i,1} D1   (warps 0-3)
+        if (w < 4) {
+            const int xi = w >> 1, xj = w & 1;
+            float acc[8];
+            if (xj == 0) {
+                mm16(acc, blkL(2 + xi, 0), LDS_, blkI(0, 0), LDS_, lane, false);
+                mm16(acc, blkL(2 + xi, 1), LDS_, blkI(1, 0), LDS_, lane, true);
+            } else {
+                mm16(acc, blkL(2 + xi, 1), LDS_, blkI(1, 1), LDS_, lane, false);
+            }
+            st16(XS + 256 * w, 16, acc, lane, 1.f);
+        }
+        __syncthreads();
+        // (4) INV_[23][01] = -D_[23] X:  Y_0j = D2 X_0j,  Y_1j = INV_32 X_0j + D3 X_1j   (warps 0-3)
+        if (w < 4) {
+            const int yi = w >> 1, yj = w & 1;
+            float acc[8];
+            if (yi == 0) {
+                mm16(acc, blkI(2, 2), LDS_, XS + 256 * yj, 16, lane, false);
+            } else {
+                mm16(acc, blkI(3, 2), LDS_, XS + 256 * yj, 16, lane, false);
+                mm16(acc, blkI(3, 3), LDS_, XS + 256 * (2 + yj), 16, lane, true);
+            }
+            st16(blkI(2 + yi, yj), LDS_, acc, lane, -1.f);
+        }
+        __syncthreads();
+        // INV Diag(beta) -> K-major A operand as high + low bf16 parts
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int e = tid + 256 * it;
-        const int r = e >> 3, cc = e & 7;
-        float f[8], lo[8];
+        for (int it = 0; it < 2; ++it) {
+            const int e = tid + 256 * it;
+            const int r = e >> 3, cc = e & 7;
+            float f[8], lo[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) f[u] = IS[r * LDS_ + 8 * cc + u] * beta_s[8 * cc + u];
-        split8(f, lo);
-        *reinterpret_cast<uint4*>(sm + K1_AI + kda::sw128(r, 8 * cc, 64)) = pack8(f);
-        *reinterpret_cast<uint4*>(sm + K1_AIL + kda::sw128(r, 8 * cc, 64)) = pack8(lo);
-    }
-    kda::fence_proxy_async_smem();
-    kda::tc_fence_before();
-    __syncthreads();
+            for (int u = 0; u < 8; ++u) f[u] = IS[r * LDS_ + 8 * cc + u] * beta_s[8 * cc + u];
+            split8(f, lo);
+            *reinterpret_cast<uint4*>(sm + K1_AI + kda::sw128(r, 8 * cc, 64)) = pack8(f);
+            *reinterpret_cast<uint4*>(sm + K1_AIL + kda::sw128(r, 8 * cc, 64)) = pack8(lo);
+        }
+        kda::fence_proxy_async_smem();
+        kda::tc_fence_before();
+        __syncthreads();
 
-    // ---------------- a3: [W | U0] = INV Diag(beta) [K_decay | V]  (INV in two bf16 parts)
-    if (tid == 0) {
+        // ---------------- a3: [W | U0] = INV Diag(beta) [K_decay | V]  (INV in two bf16 parts)
+        if (tid == 0) {
+            kda::tc_fence_after();
+            const uint32_t sB = kda::smem_u32(sm + K1_BWU);
+            const uint32_t idesc = kda::idesc_bf16(128, 256, 0, 1);
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                const uint32_t sAI = kda::smem_u32(sm + (part ? K1_AIL : K1_AI));
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ad = kda::sw128_desc(sAI + s * 32, 16, 1024);
+                    const uint64_t bd = kda::sw128_desc(sB + s * 2048, 8192, 1024);
+                    kda::umma_bf16(tmem, ad, bd, idesc, (part | s) ? 1u : 0u);
+                }
+            }
+            kda::umma_commit(bar);
+        }
+        if (!kda::mbar_wait(bar, 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
         kda::tc_fence_after();
-        const uint32_t sB = kda::smem_u32(sm + K1_BWU);
-        const uint32_t idesc = kda::idesc_bf16(128, 256, 0, 1);
+
+        if (w == 0 || w == 1) {                    // W rows -> rows 64..127 of [Q_decay; W]
+            const int r = 32 * w + lane;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const uint32_t sAI = kda::smem_u32(sm + (part ? K1_AIL : K1_AI));
+            for (int cb = 0; cb < 4; ++cb) {
+                float x[32];
+                kda::tmem_ld32(tmem + ((uint32_t)(32 * w) << 16) + 32 * cb, x);
+                kda::tmem_wait_ld();
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t ad = kda::sw128_desc(sAI + s * 32, 16, 1024);
-                const uint64_t bd = kda::sw128_desc(sB + s * 2048, 8192, 1024);
-                kda::umma_bf16(tmem, ad, bd, idesc, (part | s) ? 1u : 0u);
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4*>(blk + WS_A1 + kda::sw128(64 + r, 32 * cb + 8 * u, 128)) = pack8(x + 8 * u);
+            }
+        } else if (w == 4 || w == 5) {             // U0 rows (fp32) -> [tile][row][NT]
+            const int r = 32 * (w - 4) + lane;
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                float x[32];
+                kda::tmem_ld32(tmem + ((uint32_t)(32 * (w - 4)) << 16) + 128 + 32 * cb, x);
+                kda::tmem_wait_ld();
+                const int j = 32 * cb, tile = j / NT;
+                float4* dst = reinterpret_cast<float4*>(blk + WS_U0 + (size_t)(tile * C + r) * NT * 4);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    dst[((j % NT) / 4 + u) ^ (r & 7)] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
             }
         }
-        kda::umma_commit(bar);
+        kda::tc_fence_before();
+        __syncthreads();                           // shared memory and TMEM are reused by the next item
+        kda::tc_fence_after();
     }
-    if (!kda::mbar_wait(bar, 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
-    kda::tc_fence_after();
-
-    if (w == 0 || w == 1) {                    // W rows -> rows 64..127 of [Q_decay; W]
-        const int r = 32 * w + lane;
-#pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-            float x[32];
-            kda::tmem_ld32(tmem + ((uint32_t)(32 * w) << 16) + 32 * cb, x);
-            kda::tmem_wait_ld();
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                *reinterpret_cast<uint4*>(blk + WS_A1 + kda::sw128(64 + r, 32 * cb + 8 * u, 128)) = pack8(x + 8 * u);
-        }
-    } else if (w == 4 || w == 5) {             // U0 rows (fp32) -> [tile][row][NT]
-        const int r = 32 * (w - 4) + lane;
-#pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-            float x[32];
-            kda::tmem_ld32(tmem + ((uint32_t)(32 * (w - 4)) << 16) + 128 + 32 * cb, x);
-            kda::tmem_wait_ld();
-            const int j = 32 * cb, tile = j / NT;
-            float4* dst = reinterpret_cast<float4*>(blk + WS_U0 + (size_t)(tile * C + r) * NT * 4);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                dst[((j % NT) / 4 + u) ^ (r & 7)] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
-        }
-    }
-    kda::tc_fence_before();
-    __syncthreads();
     if (w == 0) kda::tmem_dealloc(tmem, K1_TMEM_COLS);
 }
 
@@ -1001,10 +1012,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
 
     auto prep = [&](int j0, int jn, cudaStream_t st) {
         if (jn <= 0 || a.total_chunks <= 0) return cudaSuccess;
-        const unsigned gx = use_table ? (unsigned)a.total_chunks : (unsigned)(a.n_seq * jn);
-        kda_tc_prep<<<dim3(gx, a.H), 256, prep_smem, st>>>(
+        const int gx = use_table ? a.total_chunks : a.n_seq * jn;
+        const long long items = (long long)gx * a.H;
+        const unsigned grid = (unsigned)std::min<long long>(items, 2LL * n_sm);   // two resident CTAs per SM
+        kda_tc_prep<<<grid, 256, prep_smem, st>>>(
             static_cast<const bf16*>(a.q), static_cast<const bf16*>(a.k), static_cast<const bf16*>(a.v),
-            a.log_alpha, a.beta, a.H, use_table, fixed_len, nch_per, chunk_info, seq_info, j0, jn, blocks,
+            a.log_alpha, a.beta, a.H, use_table, fixed_len, nch_per, chunk_info, seq_info, j0, jn, gx, blocks,
             a.status);
         return cudaGetLastError();
     };
