@@ -183,6 +183,40 @@ KDA_API kda_status kda_prefill_noalloc(const void* q, const void* k, const void*
                                kda_dtype dtype, void* O, float* S_final, cudaStream_t stream);
 
 /*
+ * Fused parameter-free prologue.  The Kimi Linear layer L2-normalises q and k
+ * before the operator ("Kimi K3: the manos, the mythos, the legendos",
+ * section "Kimi Linear") and keeps the log-decay inside (-5, 0) ("LLM
+ * architecture at trillion scale", section "The KDA update, in plain words").
+ * The *_fused entries take those inputs before the activations and apply, in
+ * fp32 inside the kernels, per (token, head):
+ *   q <- q / sqrt(sum_i q_i^2 + 1e-6),  k <- k / sqrt(sum_i k_i^2 + 1e-6)
+ *   log_alpha = clamp(-softplus(gate), -5, -1e-4)      (per key channel)
+ *   beta = sigmoid(beta_logit)
+ * and then compute exactly what kda_prefill / kda_decode compute.
+ *
+ * kda_prefill_fused: arguments as kda_prefill, with
+ *   q, k        [T_total, H, dk] dtype, not normalised
+ *   gate        [T_total, H, dk] float, pre-activation of the log-decay
+ *   beta_logit  [T_total, H] float, pre-activation of beta
+ * (workspace from kda_prefill_workspace_size, as for kda_prefill).
+ */
+KDA_API kda_status kda_prefill_fused(const void* q, const void* k, const void* v,
+                             const float* gate, const float* beta_logit, const float* S0,
+                             const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                             int n_seq, int T_total, int H, int dk, int dv, int chunk,
+                             kda_dtype dtype, void* O, float* S_final, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * kda_decode_fused: one decode step as kda_decode, with q, k [N, H, dk] not
+ * normalised, gate [N, H, dk] and beta_logit [N, H] pre-activations (see
+ * kda_prefill_fused for the prologue).
+ */
+KDA_API kda_status kda_decode_fused(const void* q, const void* k, const void* v,
+                            const float* gate, const float* beta_logit, float* S, int N, int H,
+                            int dk, int dv, kda_dtype dtype, void* o, cudaStream_t stream);
+
+/*
  * One decode step for N independent sequences (one token each), the per-token
  * form u = beta (v - (D S)^T k), S <- D S + k u^T, o = S^T q of "Kimi K3: the
  * manos, the mythos, the legendos", section "FlashKDA Algorithm".

@@ -18,8 +18,9 @@ LIB_PATH = os.path.join(_PKG, "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(6)
 KDA_FP32, KDA_BF16 = 0, 1
-SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_ckpt", "kda_prefill_noalloc", "kda_decode",
-           "kda_decode_multi", "kda_get_last_device_status", "kda_set_trace_events", "kda_status_string")
+SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_ckpt", "kda_prefill_fused",
+           "kda_prefill_noalloc", "kda_decode", "kda_decode_fused", "kda_decode_multi",
+           "kda_get_last_device_status", "kda_set_trace_events", "kda_status_string")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lock = threading.Lock()
@@ -49,6 +50,10 @@ def load():
         lib.kda_prefill.restype = I
         lib.kda_prefill_ckpt.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, I, P, I, P, Z, P]
         lib.kda_prefill_ckpt.restype = I
+        lib.kda_prefill_fused.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, Z, P]
+        lib.kda_prefill_fused.restype = I
+        lib.kda_decode_fused.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P]
+        lib.kda_decode_fused.restype = I
         lib.kda_prefill_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
         lib.kda_prefill_noalloc.restype = I
         lib.kda_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P]
@@ -108,6 +113,21 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, cu_seqlens_h
     """Chunked prefill; returns (O, S_final).  Shapes as in ``include/kda.h``:
     q, k, log_alpha [T, H, dk]; v [T, H, dv]; beta [T, H]; S0 [n_seq, H, dk, dv] fp32 or
     None; cu_seqlens int32 [n_seq+1] on the device or None (one sequence)."""
+    return _prefill("kda_prefill", q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, chunk, O,
+                    S_final, workspace, stream, want_state)
+
+
+def kda_prefill_fused(q, k, v, gate, beta_logit, S0=None, cu_seqlens=None, cu_seqlens_host=None, chunk=64,
+                      O=None, S_final=None, workspace=None, stream=None, want_state=True):
+    """kda_prefill with the parameter-free prologue fused in (include/kda.h):
+    q, k not normalised, gate and beta_logit are the pre-activations of
+    log_alpha and beta.  Returns (O, S_final)."""
+    return _prefill("kda_prefill_fused", q, k, v, gate, beta_logit, S0, cu_seqlens, cu_seqlens_host, chunk, O,
+                    S_final, workspace, stream, want_state)
+
+
+def _prefill(entry, q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, chunk, O, S_final, workspace,
+             stream, want_state):
     lib = load()
     dev = q.device
     T, H, dk = q.shape
@@ -132,11 +152,11 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, cu_seqlens_h
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(cu_seqlens),
-                         host, n_seq, T, H, dk, dv, chunk, dt, _ptr(O), _ptr(S_final), _ptr(workspace),
-                         ws_bytes, _stream(stream, dev))
+    st = getattr(lib, entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                             _ptr(cu_seqlens), host, n_seq, T, H, dk, dv, chunk, dt, _ptr(O), _ptr(S_final),
+                             _ptr(workspace), ws_bytes, _stream(stream, dev))
     if st != KDA_OK:
-        raise KDAError(st, "kda_prefill")
+        raise KDAError(st, entry)
     return O, S_final
 
 
@@ -229,6 +249,15 @@ def kda_prefill_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, cu_s
 
 def kda_decode(q, k, v, log_alpha, beta, S, o=None, stream=None):
     """One decode step; S [N, H, dk, dv] fp32 is updated in place; returns o [N, H, dv]."""
+    return _decode("kda_decode", q, k, v, log_alpha, beta, S, o, stream)
+
+
+def kda_decode_fused(q, k, v, gate, beta_logit, S, o=None, stream=None):
+    """kda_decode with the parameter-free prologue fused in (see kda_prefill_fused)."""
+    return _decode("kda_decode_fused", q, k, v, gate, beta_logit, S, o, stream)
+
+
+def _decode(entry, q, k, v, log_alpha, beta, S, o, stream):
     lib = load()
     dev = q.device
     N, H, dk = q.shape
@@ -240,10 +269,10 @@ def kda_decode(q, k, v, log_alpha, beta, S, o=None, stream=None):
     _check_dev("S", S, dev, torch.float32)
     if o is None:
         o = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
-    st = lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S), N, H, dk, dv,
-                        _dtype_code(q.dtype), _ptr(o), _stream(stream, dev))
+    st = getattr(lib, entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S), N, H, dk, dv,
+                             _dtype_code(q.dtype), _ptr(o), _stream(stream, dev))
     if st != KDA_OK:
-        raise KDAError(st, "kda_decode")
+        raise KDAError(st, entry)
     return o
 
 

@@ -61,6 +61,19 @@ __device__ __forceinline__ int ckpt_base(int n, int every, LenFn lens_of) {
     return tot;
 }
 
+// ---- fused parameter-free prologue of the Kimi Linear layer ("Kimi K3: the
+// manos, the mythos, the legendos", section "Kimi Linear": q and k are L2
+// normalised; the log-decay is kept inside (-5, 0) per the "LLM architecture at
+// trillion scale" page, section "The KDA update, in plain words").
+//   log_alpha = clamp(-softplus(a), -5, -1e-4),  beta = sigmoid(b),
+//   x_hat = x / sqrt(sum x^2 + kNormEps)  over d_k, per (token, head).
+constexpr float kNormEps = 1e-6f;
+__device__ __forceinline__ float prologue_log_alpha(float a) {
+    const float sp = a > 20.f ? a : log1pf(__expf(a));
+    return fminf(fmaxf(-sp, -5.f), -1e-4f);
+}
+__device__ __forceinline__ float prologue_beta(float b) { return 1.f / (1.f + __expf(-b)); }
+
 }  // namespace kda
 
 // Host-side launchers implemented by the kernel translation units.
@@ -87,6 +100,7 @@ struct PrefillArgs {
     int ckpt_every;              // 0: no checkpoints; else a multiple of chunk (tokens)
     float* ckpt;                 // [ckpt_cap, H, dk, dv]
     int ckpt_cap;
+    int prologue;                // 1: q, k unnormalised, log_alpha / beta are pre-activations
 };
 
 struct DecodeArgs {
@@ -100,6 +114,7 @@ struct DecodeArgs {
     kda_dtype dtype;
     void* o;
     cudaStream_t stream;
+    int prologue;                // as in PrefillArgs
 };
 
 // Records the next trace event (see kda_set_trace_events) on `stream`.

@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                   const TIn* __restrict__ v, const float* __restrict__ log_alpha,
                   const float* __restrict__ beta, float* __restrict__ S,
-                  TIn* __restrict__ o) {
+                  TIn* __restrict__ o, int prologue) {
     constexpr int LPR = DV / 4;                       // threads per state row
     constexpr int RPP = kThreads / LPR;               // rows per pass
     constexpr int NPASS = (DK + RPP - 1) / RPP;
@@ -56,15 +56,34 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     for (int i = tid; i < DK; i += kThreads) {
         s_k[i] = kda::io<TIn>::ld(k + unit * DK + i);
         s_q[i] = kda::io<TIn>::ld(q + unit * DK + i);
-        s_a[i] = __expf(log_alpha[unit * DK + i]);
+        const float la = log_alpha[unit * DK + i];
+        s_a[i] = __expf(prologue ? kda::prologue_log_alpha(la) : la);
     }
     float4 vv;
     vv.x = kda::io<TIn>::ld(v + unit * DV + 4 * c4 + 0);
     vv.y = kda::io<TIn>::ld(v + unit * DV + 4 * c4 + 1);
     vv.z = kda::io<TIn>::ld(v + unit * DV + 4 * c4 + 2);
     vv.w = kda::io<TIn>::ld(v + unit * DV + 4 * c4 + 3);
-    const float bt = beta[unit];
+    const float bt = prologue ? kda::prologue_beta(beta[unit]) : beta[unit];
     __syncthreads();
+    // fused prologue: k and q scaled to unit length (1 / norms from warp 0)
+    float nk = 1.f, nq = 1.f;
+    if (prologue) {
+        __shared__ float s_n[2];
+        if (tid < 32) {
+            float sk = 0.f, sq = 0.f;
+            for (int i = tid; i < DK; i += 32) { sk = fmaf(s_k[i], s_k[i], sk); sq = fmaf(s_q[i], s_q[i], sq); }
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) {
+                sk += __shfl_xor_sync(0xffffffffu, sk, o2);
+                sq += __shfl_xor_sync(0xffffffffu, sq, o2);
+            }
+            if (tid == 0) { s_n[0] = rsqrtf(sk + kda::kNormEps); s_n[1] = rsqrtf(sq + kda::kNormEps); }
+        }
+        __syncthreads();
+        nk = s_n[0];
+        nq = s_n[1];
+    }
 
     // 3. decay the rows and form the partial reductions x = Sbar^T k, y = Sbar^T q
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
@@ -72,7 +91,7 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     for (int p = 0; p < NPASS; ++p) {
         const int i = r0 + p * RPP;
         if (i < DK) {
-            const float a = s_a[i], ki = s_k[i], qi = s_q[i];
+            const float a = s_a[i], ki = s_k[i] * nk, qi = s_q[i] * nq;
             s[p].x *= a; s[p].y *= a; s[p].z *= a; s[p].w *= a;
             x.x = fmaf(s[p].x, ki, x.x); x.y = fmaf(s[p].y, ki, x.y);
             x.z = fmaf(s[p].z, ki, x.z); x.w = fmaf(s[p].w, ki, x.w);
@@ -100,7 +119,7 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     for (int p = 0; p < NPASS; ++p) {
         const int i = r0 + p * RPP;
         if (i < DK) {
-            const float ki = s_k[i];
+            const float ki = s_k[i] * nk;
             float4 w;
             w.x = fmaf(ki, u.x, s[p].x); w.y = fmaf(ki, u.y, s[p].y);
             w.z = fmaf(ki, u.z, s[p].z); w.w = fmaf(ki, u.w, s[p].w);
@@ -117,6 +136,7 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         }
         float kq = 0.f;
         for (int i = 0; i < DK; ++i) kq = fmaf(s_k[i], s_q[i], kq);
+        kq *= nk * nq;
         TIn* ou = o + unit * DV + 4 * c4;
         kda::io<TIn>::st(ou + 0, fmaf(kq, u.x, Y.x));
         kda::io<TIn>::st(ou + 1, fmaf(kq, u.y, Y.y));
@@ -247,7 +267,7 @@ cudaError_t launch(const kda_host::DecodeArgs& a) {
     if (units == 0) return cudaSuccess;
     kda_decode_kernel<DK, DV, TIn><<<units, kThreads, 0, a.stream>>>(
         static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v),
-        a.log_alpha, a.beta, a.S, static_cast<TIn*>(a.o));
+        a.log_alpha, a.beta, a.S, static_cast<TIn*>(a.o), a.prologue);
     return cudaGetLastError();
 }
 

@@ -81,7 +81,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
                         const int32_t* cu_seqlens_host, int n_seq, int T_total, int H, int dk, int dv,
                         int chunk, kda_dtype dtype, void* O, float* S_final, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream, int ckpt_every, float* ckpt,
-                        int ckpt_cap) {
+                        int ckpt_cap, int prologue) {
     if (n_seq < 0 || T_total < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return KDA_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv) || !chunk_ok(chunk)) return KDA_ERR_UNSUPPORTED;
@@ -122,6 +122,7 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
     a.O = O;
     a.S_final = S_final; a.workspace = workspace; a.workspace_bytes = workspace_bytes;
     a.stream = stream; a.ckpt_every = ckpt_every; a.ckpt = ckpt; a.ckpt_cap = ckpt_cap;
+    a.prologue = prologue;
 
     if (kda_host::tc_supported(dk, dv, chunk, dtype)) {
         const size_t need = kda_host::tc_workspace_bytes(n_seq, T_total, H, chunk);
@@ -145,6 +146,25 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
     return from_cuda(simt[dtype == KDA_BF16 ? 1 : 0][ci](a));
 }
 
+
+kda_status decode_impl(const void* q, const void* k, const void* v, const float* log_alpha,
+                       const float* beta, float* S, int N, int H, int dk, int dv, kda_dtype dtype,
+                       void* o, cudaStream_t stream, int prologue) {
+    if (N < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return KDA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if ((long long)N * H >= (1LL << 31)) return KDA_ERR_UNSUPPORTED;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !S || !o) return KDA_ERR_INVALID_ARG;
+    if (o == q || o == k || o == v || o == (void*)S) return KDA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(S) % 16 != 0) return KDA_ERR_INVALID_ARG;
+    kda_host::DecodeArgs a{q, k, v, log_alpha, beta, S, N, H, dk, dv, dtype, o, stream, prologue};
+    kda_host::trace_reset();
+    kda_host::trace_mark(stream);
+    const cudaError_t e = kda_host::launch_decode(a);
+    kda_host::trace_mark(stream);
+    return from_cuda(e);
+}
 }  // namespace
 
 extern "C" {
@@ -155,7 +175,16 @@ kda_status kda_prefill(const void* q, const void* k, const void* v, const float*
                        int dv, int chunk, kda_dtype dtype, void* O, float* S_final,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     return prefill_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, n_seq, T_total, H, dk, dv,
-                        chunk, dtype, O, S_final, workspace, workspace_bytes, stream, 0, nullptr, 0);
+                        chunk, dtype, O, S_final, workspace, workspace_bytes, stream, 0, nullptr, 0, 0);
+}
+
+kda_status kda_prefill_fused(const void* q, const void* k, const void* v, const float* gate,
+                             const float* beta_logit, const float* S0, const int32_t* cu_seqlens,
+                             const int32_t* cu_seqlens_host, int n_seq, int T_total, int H, int dk, int dv,
+                             int chunk, kda_dtype dtype, void* O, float* S_final, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+    return prefill_impl(q, k, v, gate, beta_logit, S0, cu_seqlens, cu_seqlens_host, n_seq, T_total, H, dk, dv,
+                        chunk, dtype, O, S_final, workspace, workspace_bytes, stream, 0, nullptr, 0, 1);
 }
 
 kda_status kda_prefill_ckpt(const void* q, const void* k, const void* v, const float* log_alpha,
@@ -178,26 +207,20 @@ kda_status kda_prefill_ckpt(const void* q, const void* k, const void* v, const f
     }
     return prefill_impl(q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, n_seq, T_total, H, dk, dv,
                         chunk, dtype, O, S_final, workspace, workspace_bytes, stream, ckpt_every, ckpt,
-                        ckpt_capacity);
+                        ckpt_capacity, 0);
 }
+
 
 kda_status kda_decode(const void* q, const void* k, const void* v, const float* log_alpha,
                       const float* beta, float* S, int N, int H, int dk, int dv, kda_dtype dtype,
                       void* o, cudaStream_t stream) {
-    if (N < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
-    if (!dtype_ok(dtype)) return KDA_ERR_INVALID_ARG;
-    if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
-    if ((long long)N * H >= (1LL << 31)) return KDA_ERR_UNSUPPORTED;
-    if (N == 0) return KDA_OK;
-    if (!q || !k || !v || !log_alpha || !beta || !S || !o) return KDA_ERR_INVALID_ARG;
-    if (o == q || o == k || o == v || o == (void*)S) return KDA_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(S) % 16 != 0) return KDA_ERR_INVALID_ARG;
-    kda_host::DecodeArgs a{q, k, v, log_alpha, beta, S, N, H, dk, dv, dtype, o, stream};
-    kda_host::trace_reset();
-    kda_host::trace_mark(stream);
-    const cudaError_t e = kda_host::launch_decode(a);
-    kda_host::trace_mark(stream);
-    return from_cuda(e);
+    return decode_impl(q, k, v, log_alpha, beta, S, N, H, dk, dv, dtype, o, stream, 0);
+}
+
+kda_status kda_decode_fused(const void* q, const void* k, const void* v, const float* gate,
+                            const float* beta_logit, float* S, int N, int H, int dk, int dv, kda_dtype dtype,
+                            void* o, cudaStream_t stream) {
+    return decode_impl(q, k, v, gate, beta_logit, S, N, H, dk, dv, dtype, o, stream, 1);
 }
 
 kda_status kda_decode_multi(const void* q, const void* k, const void* v, const float* log_alpha,
@@ -212,7 +235,7 @@ kda_status kda_decode_multi(const void* q, const void* k, const void* v, const f
     if (!q || !k || !v || !log_alpha || !beta || !S) return KDA_ERR_INVALID_ARG;
     if (o && (o == q || o == k || o == v || o == (void*)S)) return KDA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(S) % 16 != 0) return KDA_ERR_INVALID_ARG;
-    kda_host::DecodeArgs a{q, k, v, log_alpha, beta, S, N, H, dk, dv, dtype, o, stream};
+    kda_host::DecodeArgs a{q, k, v, log_alpha, beta, S, N, H, dk, dv, dtype, o, stream, 0};
     kda_host::trace_reset();
     kda_host::trace_mark(stream);
     const cudaError_t e = kda_host::launch_decode_multi(a, K, commit_len);

@@ -55,7 +55,7 @@ kda_prefill_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                         const float* __restrict__ beta, const float* __restrict__ S0,
                         const int32_t* __restrict__ cu_seqlens, int T_total, int H,
                         int seq_len_fixed, TIn* __restrict__ O, float* __restrict__ S_final,
-                        int ckpt_every, float* __restrict__ ckpt, int ckpt_cap) {
+                        int ckpt_every, float* __restrict__ ckpt, int ckpt_cap, int prologue) {
     constexpr int DVT = DV < 32 ? DV : 32;
     using Sm = SimtSmem<DK, DVT, C>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -113,15 +113,29 @@ kda_prefill_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
             const size_t off = ((size_t)(c0 + r) * H + h) * DK + i;
             sm.q[r][i] = ok ? kda::io<TIn>::ld(q + off) : 0.f;
             sm.k[r][i] = ok ? kda::io<TIn>::ld(k + off) : 0.f;
-            sm.g[r][i] = ok ? log_alpha[off] : 0.f;
+            sm.g[r][i] = ok ? (prologue ? kda::prologue_log_alpha(log_alpha[off]) : log_alpha[off]) : 0.f;
         }
         for (int e = tid; e < C * DVT; e += kThreads) {
             const int r = e / DVT, j = e % DVT;
             sm.v[r][j] = r < nr ? kda::io<TIn>::ld(v + ((size_t)(c0 + r) * H + h) * DV + j0 + j) : 0.f;
         }
-        for (int r = tid; r < C; r += kThreads)
-            sm.beta[r] = r < nr ? beta[(size_t)(c0 + r) * H + h] : 0.f;
+        for (int r = tid; r < C; r += kThreads) {
+            const float bl = r < nr ? beta[(size_t)(c0 + r) * H + h] : 0.f;
+            sm.beta[r] = r < nr ? (prologue ? kda::prologue_beta(bl) : bl) : 0.f;
+        }
         __syncthreads();
+        if (prologue) {                          // fused prologue: unit-length q and k rows
+            for (int e = tid >> 5; e < 2 * C; e += kThreads / 32) {   // one warp per row
+                float* x = e < C ? sm.q[e] : sm.k[e - C];
+                float ss = 0.f;
+                for (int i = tid & 31; i < DK; i += 32) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float sc = rsqrtf(ss + kda::kNormEps);
+                for (int i = tid & 31; i < DK; i += 32) x[i] *= sc;
+            }
+            __syncthreads();
+        }
 
         // ---- inclusive cumulative log-decay per key channel
         for (int i = tid; i < DK; i += kThreads) {
@@ -267,7 +281,7 @@ cudaError_t launch(const kda_host::PrefillArgs& a) {
     kern<<<grid, kThreads, smem, a.stream>>>(
         static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v),
         a.log_alpha, a.beta, a.S0, a.cu_seqlens, a.T_total, a.H, fixed,
-        static_cast<TIn*>(a.O), a.S_final, a.ckpt_every, a.ckpt, a.ckpt_cap);
+        static_cast<TIn*>(a.O), a.S_final, a.ckpt_every, a.ckpt, a.ckpt_cap, a.prologue);
     const cudaError_t err = cudaGetLastError();
     kda_host::trace_mark(a.stream);
     return err;

@@ -76,7 +76,8 @@ constexpr uint32_t K1_TOT = 106496;          // float [4][128] block totals of l
 constexpr uint32_t K1_FIRST = 108544;        // float [4][128] first-row log-decay of each block
 constexpr uint32_t K1_BETA = 110592;         // float [64]
 constexpr uint32_t K1_BAR = 110848;          // mbarrier (8 B) + TMEM address (4 B)
-constexpr uint32_t K1_BYTES = 110912;
+constexpr uint32_t K1_NRM = 110912;          // fused prologue: float [q, k][channel half][64 rows] sums of squares
+constexpr uint32_t K1_BYTES = 111936;
 // aliases, valid once the Gram MMAs have completed
 constexpr int LDS_ = 68;                     // row stride (floats) of the fp32 64x64 matrices
 constexpr uint32_t K1_LS = 0;                // L   fp32 [64][68]
@@ -266,6 +267,7 @@ __device__ __forceinline__ void gram_epilogue(uint32_t tmem, int lane, uint8_t* 
     }
 }
 
+template <bool PROLOGUE>
 __global__ void __launch_bounds__(256, 2)
 kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
             const float* __restrict__ g, const float* __restrict__ beta, int H, int use_table,
@@ -339,6 +341,30 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
             kv[rr] = ok ? *reinterpret_cast<const uint32_t*>(k + off) : 0u;
             bt[rr] = ok ? beta[tok * H + h] : 0.f;
         }
+        float* nrm = reinterpret_cast<float*>(sm + K1_NRM);
+        if (PROLOGUE) {
+            // fused prologue: gates from their pre-activations; squared norms of
+            // q and k rows over this warp's 64 channels
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                if (16 * b + rr < nrows) {
+                    G0[rr] = kda::prologue_log_alpha(G0[rr]);
+                    G1[rr] = kda::prologue_log_alpha(G1[rr]);
+                    bt[rr] = kda::prologue_beta(bt[rr]);
+                }
+                const float2 qf = kda::unpack_bf16x2(qv[rr]), kf = kda::unpack_bf16x2(kv[rr]);
+                float sq = fmaf(qf.x, qf.x, qf.y * qf.y), sk = fmaf(kf.x, kf.x, kf.y * kf.y);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                }
+                if (lane == 0) {
+                    nrm[p * 64 + 16 * b + rr] = sq;
+                    nrm[128 + p * 64 + 16 * b + rr] = sk;
+                }
+            }
+        }
         // V slice -> right half of the [K_decay | V] operand (MN-major)
         for (int e = tid; e < C * (DV / 8); e += 256) {
             const int t = e >> 4, cc = e & 15;
@@ -389,8 +415,13 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
             const int r = 16 * b + rr;
             const float e0 = __expf(G0[rr] - G0[0]), e1 = __expf(G1[rr] - G1[0]);   // <= 1
             const float c0 = __fdividef(1.f, e0), c1 = __fdividef(1.f, e1);         // >= 1, <= e^75
-            const float2 qf = kda::unpack_bf16x2(qv[rr]);
-            const float2 kf = kda::unpack_bf16x2(kv[rr]);
+            float2 qf = kda::unpack_bf16x2(qv[rr]);
+            float2 kf = kda::unpack_bf16x2(kv[rr]);
+            if (PROLOGUE) {                        // unit-length q and k rows
+                const float iq = rsqrtf(nrm[r] + nrm[64 + r] + kda::kNormEps);
+                const float ik = rsqrtf(nrm[128 + r] + nrm[192 + r] + kda::kNormEps);
+                qf.x *= iq; qf.y *= iq; kf.x *= ik; kf.y *= ik;
+            }
             const float be = bt[rr];
             const float qt0 = qf.x * e0, qt1 = qf.y * e1;            // q~ (row factor)
             const float kh0 = be * kf.x * e0, kh1 = be * kf.y * e1;  // k^ = beta k (row factor)
@@ -1005,7 +1036,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     }
     const int prep_smem = (int)(K1_BYTES + 1024);
     const int chain_smem = (int)(K2_BYTES + 1024);
-    cudaError_t e = cudaFuncSetAttribute(kda_tc_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
+    auto prep_kernel = a.prologue ? kda_tc_prep<true> : kda_tc_prep<false>;
+    cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kda_tc_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
     if (e != cudaSuccess) return e;
@@ -1015,7 +1047,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         const int gx = use_table ? a.total_chunks : a.n_seq * jn;
         const long long items = (long long)gx * a.H;
         const unsigned grid = (unsigned)std::min<long long>(items, 2LL * n_sm);   // two resident CTAs per SM
-        kda_tc_prep<<<grid, 256, prep_smem, st>>>(
+        prep_kernel<<<grid, 256, prep_smem, st>>>(
             static_cast<const bf16*>(a.q), static_cast<const bf16*>(a.k), static_cast<const bf16*>(a.v),
             a.log_alpha, a.beta, a.H, use_table, fixed_len, nch_per, chunk_info, seq_info, j0, jn, gx, blocks,
             a.status);

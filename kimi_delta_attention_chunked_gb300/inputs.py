@@ -19,6 +19,10 @@ workloads.  The per-tensor recipe is
 
 Draw order on one ``torch.Generator``: q, k, v, beta-logits, gate-logits, S0.
 Variable lengths are drawn first from ``numpy.random.default_rng(seed)``.
+
+``raw=True`` returns the same draws before the normalisation and the two
+activations (q, k ~ N(0, 1) cast to the storage dtype; gate = N(mu, 1) and
+beta_logit = N(0, 1) in fp32), the inputs of the fused-prologue entry points.
 """
 from __future__ import annotations
 
@@ -81,24 +85,33 @@ def _unit_rows(x):
     return x / torch.linalg.vector_norm(x, dim=-1, keepdim=True).clamp_min(1e-12)
 
 
-def make_qkv_gates(T, H, dk, dv, dtype, gen, device, gate_mu=0.0):
-    """q, k, v, beta, log_alpha for T packed tokens, in the draw order above."""
-    q = _unit_rows(_normal((T, H, dk), gen, device)).to(dtype)
-    k = _unit_rows(_normal((T, H, dk), gen, device)).to(dtype)
+def make_qkv_gates(T, H, dk, dv, dtype, gen, device, gate_mu=0.0, raw=False):
+    """q, k, v, beta, log_alpha for T packed tokens, in the draw order above
+    (raw: q, k, v, beta_logit, gate before the normalisation and activations)."""
+    q = _normal((T, H, dk), gen, device)
+    k = _normal((T, H, dk), gen, device)
     v = _normal((T, H, dv), gen, device).to(dtype)
-    beta = torch.sigmoid(_normal((T, H), gen, device))
-    log_alpha = (-torch.nn.functional.softplus(_normal((T, H, dk), gen, device) + gate_mu)).clamp(-5.0, -1e-4)
+    b = _normal((T, H), gen, device)
+    a = _normal((T, H, dk), gen, device) + gate_mu
+    if raw:
+        return q.to(dtype).contiguous(), k.to(dtype).contiguous(), v.contiguous(), b.contiguous(), a.contiguous()
+    q = _unit_rows(q).to(dtype)
+    k = _unit_rows(k).to(dtype)
+    beta = torch.sigmoid(b)
+    log_alpha = (-torch.nn.functional.softplus(a)).clamp(-5.0, -1e-4)
     return q.contiguous(), k.contiguous(), v.contiguous(), beta.contiguous(), log_alpha.contiguous()
 
 
-def make_prefill(w: Workload, device="cpu", seed: int = 0, lengths=None):
+def make_prefill(w: Workload, device="cpu", seed: int = 0, lengths=None, raw=False):
     """Inputs for a prefill workload: dict with q, k, v, log_alpha, beta, S0,
-    cu_seqlens (int32, on ``device``), cu_seqlens_host (list) and lengths."""
+    cu_seqlens (int32, on ``device``), cu_seqlens_host (list) and lengths.
+    raw=True: gate and beta_logit in place of log_alpha and beta, q and k not
+    normalised."""
     lens = list(lengths) if lengths is not None else seq_lengths(w, seed)
     T = int(sum(lens))
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
-    q, k, v, beta, log_alpha = make_qkv_gates(T, w.H, w.dk, w.dv, w.dtype, gen, device, w.gate_mu)
+    q, k, v, beta, log_alpha = make_qkv_gates(T, w.H, w.dk, w.dv, w.dtype, gen, device, w.gate_mu, raw)
     S0 = None
     if w.s0_std > 0:
         S0 = (_normal((len(lens), w.H, w.dk, w.dv), gen, device) * w.s0_std).contiguous()
@@ -106,19 +119,22 @@ def make_prefill(w: Workload, device="cpu", seed: int = 0, lengths=None):
     for L in lens:
         cu_host.append(cu_host[-1] + L)
     cu = torch.tensor(cu_host, dtype=torch.int32, device=device)
-    return dict(q=q, k=k, v=v, log_alpha=log_alpha, beta=beta, S0=S0, cu_seqlens=cu,
-                cu_seqlens_host=cu_host, lengths=lens, T=T)
+    gates = dict(gate=log_alpha, beta_logit=beta) if raw else dict(log_alpha=log_alpha, beta=beta)
+    return dict(q=q, k=k, v=v, S0=S0, cu_seqlens=cu, cu_seqlens_host=cu_host, lengths=lens, T=T, **gates)
 
 
-def make_decode(w: Workload, device="cpu", seed: int = 0, n_token_sets: int = 1):
+def make_decode(w: Workload, device="cpu", seed: int = 0, n_token_sets: int = 1, raw=False):
     """State plus ``n_token_sets`` fresh one-token sets for a decode workload.
 
     Returns dict with S [N, H, dk, dv] fp32 and lists q, k, v, log_alpha, beta
-    (one [N, H, .] tensor per set)."""
+    (one [N, H, .] tensor per set); raw=True: gate, beta_logit instead."""
     N = w.B
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
-    sets = [make_qkv_gates(N, w.H, w.dk, w.dv, w.dtype, gen, device, w.gate_mu) for _ in range(n_token_sets)]
+    sets = [make_qkv_gates(N, w.H, w.dk, w.dv, w.dtype, gen, device, w.gate_mu, raw)
+            for _ in range(n_token_sets)]
     S = (_normal((N, w.H, w.dk, w.dv), gen, device) * (w.s0_std if w.s0_std > 0 else 0.02)).contiguous()
     q, k, v, beta, log_alpha = (list(x) for x in zip(*sets))
+    if raw:
+        return dict(q=q, k=k, v=v, beta_logit=beta, gate=log_alpha, S=S)
     return dict(q=q, k=k, v=v, beta=beta, log_alpha=log_alpha, S=S)

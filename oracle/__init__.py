@@ -7,6 +7,10 @@ never calls it, links it or falls back to it, and it shares no code with it.
 * ``prefill``   -- the per-token recurrence in C (``kda_ref.c``), fp64,
   OpenMP over (sequence, head).  This is the oracle every GPU result is
   compared with.  Decode is the same call with one token per sequence.
+* ``prefill_fused`` / ``decode_fused`` / ``prologue`` -- the same recurrence
+  behind the parameter-free prologue of the Kimi Linear layer (q, k
+  L2-normalised, log-decay = clamp(-softplus(gate), -5, -1e-4), beta =
+  sigmoid(beta_logit)), also in ``kda_ref.c``.
 * ``chunked``   -- the pages' FlashKDA chunk form in fp64 numpy, used only to
   cross-check the token loop (pin P5).
 
@@ -52,6 +56,11 @@ def bind(path: str):
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     P, P, ctypes.c_int]
     lib.kda_ref_prefill.restype = ctypes.c_int
+    lib.kda_ref_prefill_prologue.argtypes = lib.kda_ref_prefill.argtypes
+    lib.kda_ref_prefill_prologue.restype = ctypes.c_int
+    I = ctypes.c_int
+    lib.kda_ref_prologue.argtypes = [P, I, I, P, P, I, P, P, I, P]
+    lib.kda_ref_prologue.restype = None
     lib.kda_ref_max_threads.argtypes = []
     lib.kda_ref_max_threads.restype = ctypes.c_int
     return lib
@@ -78,7 +87,7 @@ def _f32(x):
 
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, S0=None, heads=None,
-            n_threads: int = 0, want_O: bool = True, lib=None):
+            n_threads: int = 0, want_O: bool = True, lib=None, _prologue: bool = False):
     """Per-token fp64 KDA over a packed varlen batch (the definition).
 
     q, k, log_alpha: [T, H, dk]; v: [T, H, dv]; beta: [T, H] (numpy or torch,
@@ -110,11 +119,56 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, S0=None, heads=None,
     O = np.empty((T, Hs, dv), dtype=np.float64) if want_O else None
     Sf = np.empty((n_seq, Hs, dk, dv), dtype=np.float64)
     ptr = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
-    rc = lib.kda_ref_prefill(ptr(q), ptr(k), ptr(v), ptr(log_alpha), ptr(beta), ptr(s0), ptr(cu),
-                             n_seq, H, dk, dv, h0, h1, ptr(O), ptr(Sf), int(n_threads))
+    fn = lib.kda_ref_prefill_prologue if _prologue else lib.kda_ref_prefill
+    rc = fn(ptr(q), ptr(k), ptr(v), ptr(log_alpha), ptr(beta), ptr(s0), ptr(cu),
+            n_seq, H, dk, dv, h0, h1, ptr(O), ptr(Sf), int(n_threads))
     if rc != 0:
         raise ValueError(f"kda_ref_prefill failed with code {rc}")
     return O, Sf
+
+
+def prefill_fused(q, k, v, gate, beta_logit, cu_seqlens=None, S0=None, heads=None, n_threads: int = 0,
+                  want_O: bool = True):
+    """``prefill`` behind the parameter-free prologue: q, k unnormalised,
+    gate [T, H, dk] and beta_logit [T, H] the pre-activations of log_alpha and
+    beta ("Kimi K3: the manos, the mythos, the legendos", section "Kimi Linear";
+    "LLM architecture at trillion scale", section "The KDA update, in plain
+    words")."""
+    return prefill(q, k, v, gate, beta_logit, cu_seqlens=cu_seqlens, S0=S0, heads=heads, n_threads=n_threads,
+                   want_O=want_O, _prologue=True)
+
+
+def decode_fused(q, k, v, gate, beta_logit, S, n_threads: int = 0):
+    """``decode`` behind the parameter-free prologue (see ``prefill_fused``)."""
+    N = q.shape[0]
+    cu = np.arange(N + 1, dtype=np.int64)
+    return prefill_fused(q, k, v, gate, beta_logit, cu_seqlens=cu, S0=S, n_threads=n_threads)
+
+
+def prologue(x=None, gate=None, beta_logit=None):
+    """The prologue alone, fp64: x [..., d] -> x / sqrt(sum x^2 + 1e-6) over the
+    last axis; gate -> clamp(-softplus(gate), -5, -1e-4); beta_logit ->
+    sigmoid(beta_logit).  Returns (x_hat, log_alpha, beta), None where no input."""
+    lib = _load()
+    ptr = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    xh = la = bt = None
+    xf = gf = bf = None
+    n_rows = d = n_g = n_b = 0
+    if x is not None:
+        xf = _f32(x)
+        d = xf.shape[-1]
+        n_rows = xf.size // d
+        xh = np.empty(xf.shape, dtype=np.float64)
+    if gate is not None:
+        gf = _f32(gate)
+        n_g = gf.size
+        la = np.empty(gf.shape, dtype=np.float64)
+    if beta_logit is not None:
+        bf = _f32(beta_logit)
+        n_b = bf.size
+        bt = np.empty(bf.shape, dtype=np.float64)
+    lib.kda_ref_prologue(ptr(xf), n_rows, d, ptr(xh), ptr(gf), n_g, ptr(la), ptr(bf), n_b, ptr(bt))
+    return xh, la, bt
 
 
 def decode(q, k, v, log_alpha, beta, S, n_threads: int = 0):
