@@ -113,6 +113,8 @@ KDA_API size_t kda_prefill_workspace_size(int n_seq, int T_total, int H, int dk,
  *            256-byte aligned (may be NULL when that size is 0).  Its contents
  *            on entry do not matter; the call owns it until the work completes.
  * Sequences of length 0 are allowed (their S_final is S0).
+ * On the tensor-core path (bf16, dk = dv = 128, chunk 64) q, k, v, log_alpha
+ * and O must be 16-byte aligned; otherwise KDA_ERR_INVALID_ARG.
  */
 KDA_API kda_status kda_prefill(const void* q, const void* k, const void* v,
                        const float* log_alpha, const float* beta, const float* S0,
@@ -168,8 +170,8 @@ KDA_API kda_status kda_prefill_ckpt(const void* q, const void* k, const void* v,
  * KDA_NOALLOC_SCRATCH_BYTES; the call allocates nothing.
  *   - Returns KDA_ERR_WORKSPACE, before launching anything, when
  *     kda_prefill_workspace_size(...) for the problem exceeds
- *     KDA_NOALLOC_SCRATCH_BYTES (e.g. more than about 640 chunk-head slots
- *     on the tensor-core path: H = 32 heads of ~1280 tokens).
+ *     KDA_NOALLOC_SCRATCH_BYTES (e.g. more than about 580 chunk-head slots
+ *     on the tensor-core path: H = 32 heads of ~1100 tokens).
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - All calls on a device share the array and it keeps the last call's

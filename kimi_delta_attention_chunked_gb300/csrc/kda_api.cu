@@ -125,6 +125,9 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
     a.prologue = prologue;
 
     if (kda_host::tc_supported(dk, dv, chunk, dtype)) {
+        // the tensor-core kernels move whole 16-byte vectors of every token row
+        for (const void* p : {q, k, v, (const void*)log_alpha, (const void*)O})
+            if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return KDA_ERR_INVALID_ARG;
         const size_t need = kda_host::tc_workspace_bytes(n_seq, T_total, H, chunk);
         if (workspace_bytes < need || (need && !workspace)) return KDA_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return KDA_ERR_WORKSPACE;

@@ -24,23 +24,28 @@
 //          column operands stacked along N = 160): M_qk (diagonal included)
 //          and L (strict, beta folded in).
 //      a3  INV = (I + L)^-1 in fp32 (16x16 diagonal blocks by substitution,
-//          then two levels of 2x2 block merges done warp by warp), then one MMA
-//          [INV Diag(beta)] [K_decay | V] -> W, U0.
+//          then two levels of 2x2 block merges done warp by warp) and
+//          X = M_qk INV; then one MMA with M = 128 stacked rows
+//             [INV Diag(beta); X Diag(beta)] [K_decay | V]
+//          gives W = INV Diag(beta) K_decay, U0 = INV Diag(beta) V and, in the
+//          same instruction, M_qk W and O0 = M_qk U0.  Since U = U0 - W S_in,
+//             O = Q_decay S_in + M_qk U = Q' S_in + O0,  Q' = Q_decay - M_qk W,
+//          so the state pass needs no product for M_qk U.
 //      Writes, per (chunk, head), the MMA-ready operand images the chain
-//      needs: [Q_decay; W], K_restore^T, M_qk, U0, a_last.
+//      needs: [Q'; W], K_restore^T, U0, O0, a_last.
 //
 //  kda_tc_chain  one CTA per (sequence, head, 64-column slice of d_v);
 //      a4/a5  for each chunk in order (operands streamed by bulk copies,
 //          two stages deep), with S kept in TMEM in fp32:
-//             P  = [Q_decay; W] S_in                    (MMA, M = 128)
+//             P  = [Q'; W] S_in                         (MMA, M = 128)
 //             U  = U0 - P_w                             (W S_in = K_decay part)
+//             O  = P_q + O0
 //             S  = Diag(a_last) S_in + K_restore^T U    (MMA, accumulate)
-//             P_q += M_qk U  ->  O                      (MMA, accumulate)
 //
-// Precision: MMA operands are bf16 with fp32 accumulation.  The four operands
-// whose rounding dominated the error budget -- INV Diag(beta), M_qk, U0 and U
-// -- are carried as a high and a low bf16 part (U0 as fp32), which leaves the
-// bf16 output rounding as the largest single error term.
+// Precision: MMA operands are bf16 with fp32 accumulation.  The operands
+// whose rounding dominated the error budget -- [INV; X] Diag(beta) and U --
+// are carried as a high and a low bf16 part, and U0 and O0 stay fp32, which
+// leaves the bf16 output rounding as the largest single error term.
 //
 // Every wait on an asynchronous event is bounded; a wait that runs out records
 // KDA_ERR_TIMEOUT in the status word and the kernel runs to completion.
@@ -59,13 +64,13 @@ constexpr int NT = 64;                       // d_v columns per chain CTA
 constexpr int NTILES = DV / NT;
 
 // ---- per (chunk, head) workspace block: images of shared-memory operands
-constexpr uint32_t WS_A1 = 0;                // [Q_decay; W]  K-major SW128, 128 rows, K = 128 (2 panels)
+constexpr uint32_t WS_A1 = 0;                // [Q'; W]       K-major SW128, 128 rows, K = 128 (2 panels)
 constexpr uint32_t WS_KR = 32768;            // K_restore^T   MN-major SW128, K = 64 rows, M = 128 (2 panels)
-constexpr uint32_t WS_MQ = 49152;            // M_qk high and low bf16 parts, each K-major SW128, 64 rows, K = 64
-constexpr uint32_t WS_U0 = 65536;            // U0            fp32 [NTILES][C][NT], 16-byte chunk j of row r at j ^ (r % 8)
-constexpr uint32_t WS_AL = 98304;            // a_last        fp32 [DK]
-constexpr uint32_t WS_BLOCK = 99328;         // 97 KiB
-constexpr uint32_t COPY_BYTES = 32768 + 16384 + 16384 + C * NT * 4 + DK * 4;
+constexpr uint32_t TILE_F32 = C * NT * 4;    // one d_v slice of U0 or O0: fp32 [C][NT], 16-byte chunk j of row r at j ^ (r % 8)
+constexpr uint32_t WS_UO = 49152;            // per d_v slice t: U0 at WS_UO + 2 t TILE_F32, O0 = M_qk U0 right after it
+constexpr uint32_t WS_AL = WS_UO + NTILES * 2 * TILE_F32;   // a_last fp32 [DK]
+constexpr uint32_t WS_BLOCK = 115712;        // 113 KiB
+__host__ __device__ constexpr uint32_t ws_u0(int t) { return WS_UO + 2u * TILE_F32 * (uint32_t)t; }
 
 // ---- prep kernel shared memory
 constexpr uint32_t K1_AG = 0;                // Gram A: 128 rows [q~ b0 | k^ b0 | q~ b1 | ...], K = 128
@@ -75,7 +80,7 @@ constexpr uint32_t K1_BWU = 73728;           // [K_decay | V]: MN-major, K = 64 
 constexpr uint32_t K1_TOT = 106496;          // float [4][128] block totals of log-decay
 constexpr uint32_t K1_FIRST = 108544;        // float [4][128] first-row log-decay of each block
 constexpr uint32_t K1_BETA = 110592;         // float [64]
-constexpr uint32_t K1_BAR = 110848;          // mbarrier (8 B) + TMEM address (4 B)
+constexpr uint32_t K1_BAR = 110848;          // MMA mbarrier (8 B), TMEM address (4 B), Q_decay copy mbarrier at +16
 constexpr uint32_t K1_NRM = 110912;          // fused prologue: float [q, k][channel half][64 rows] sums of squares
 constexpr uint32_t K1_BYTES = 111936;
 // aliases, valid once the Gram MMAs have completed
@@ -83,26 +88,44 @@ constexpr int LDS_ = 68;                     // row stride (floats) of the fp32 
 constexpr uint32_t K1_LS = 0;                // L   fp32 [64][68]
 constexpr uint32_t K1_IS = 17408;            // INV fp32 [64][68]
 constexpr uint32_t K1_XS = 34816;            // 4 x 16x16 fp32 scratch blocks (dense)
-constexpr uint32_t K1_AI = 38912;            // INV Diag(beta), high bf16 part, K-major SW128, 64 rows, K = 64
-constexpr uint32_t K1_AIL = 55296;           // ... low bf16 part (rows 64..127 of both are never used)
+constexpr uint32_t K1_MH = 38912;            // M_qk high / low bf16 parts, K-major SW128, 64 rows, K = 64
+constexpr uint32_t K1_ML = 47104;            //   (the M = 128 product reads 64 rows past each: still in the tile)
+constexpr uint32_t K1_IH = 0;                // INV high / low bf16 parts, MN-major SW128, K = 64 rows, N = 64
+constexpr uint32_t K1_IL = 8192;             //   (over L, once the inverse no longer needs it)
+constexpr uint32_t K1_AI = 38912;            // [INV; X] Diag(beta), high bf16 part, K-major SW128, 128 rows, K = 64
+constexpr uint32_t K1_AIL = 55296;           // ... low bf16 part (both written once the X product is done)
 constexpr uint32_t K1_TMEM_COLS = 256;
+constexpr uint32_t K1_TX = 160;              // TMEM columns of X = M_qk INV (lanes 0..63)
+// output images, assembled once the last MMA has completed (everything below
+// K1_TOT is free then) and written to the workspace by two bulk copies
+constexpr uint32_t K1_OUT_A1 = 0;            // [Q'; W] image (rows 0..63 arrive as Q_decay from the workspace)
+constexpr uint32_t K1_OUT_UO = 32768;        // [U0 | O0] of both d_v slices, the workspace's WS_UO layout
 
 // ---- chain kernel shared memory
-constexpr int K2_NS = 2;                     // operand stages in flight
-constexpr uint32_t K2_STAGE = 82944;
-constexpr uint32_t ST_A1 = 0, ST_KR = 32768, ST_MQ = 49152, ST_MQL = 57344, ST_U0 = 65536, ST_AL = 81920;
-constexpr uint32_t K2_SB = K2_NS * K2_STAGE; // S_in bf16, MN-major SW128, K = 128 rows, N = 64 (16 KiB used)
-constexpr uint32_t K2_UB = K2_SB + 32768;    // [U_hi | U_lo] bf16, MN-major SW128, K = 64 rows, N = 2 x 64
-constexpr uint32_t K2_XO = K2_UB + 16384;    // M_lo U share of O, bf16 SW128 [64 rows][64]
-constexpr uint32_t K2_BAR = K2_XO + 8192;    // full[K2_NS], p, s, o, TMEM address
-constexpr uint32_t K2_BYTES = K2_BAR + 64;
-constexpr uint32_t K2_TMEM_COLS = 512;       // S [0, 64), X [64, 128), P buffers [128, 256), [256, 384)
+constexpr int K2_NA = 2;                     // [Q'; W] stages (released as soon as the P product is done)
+constexpr int K2_NB = 2;                     // [K_restore^T | U0] stages (released after the state update)
+constexpr int K2_NO = 3;                     // O0 stages (read one chunk later, when O is formed)
+constexpr uint32_t K2_ASTAGE = 32768;
+constexpr uint32_t K2_BSTAGE = 16384 + TILE_F32;
+constexpr uint32_t K2_OSTAGE = TILE_F32;     // O0 fp32; the bf16 output rows are staged over it
+constexpr uint32_t K2_B0 = K2_NA * K2_ASTAGE;            // B ring: K_restore^T at +0, U0 at +16384
+constexpr uint32_t K2_O0 = K2_B0 + K2_NB * K2_BSTAGE;    // O ring
+constexpr uint32_t K2_SB = K2_O0 + K2_NO * K2_OSTAGE;    // S_in bf16, MN-major SW128, K = 128 rows, N = 64
+constexpr uint32_t K2_UB = K2_SB + 16384;                // [U_hi | U_lo] bf16, MN-major SW128, K = 64 rows, N = 2 x 64
+constexpr uint32_t K2_BAR = K2_UB + 16384;               // full / empty A, B, O; p; s; TMEM address
+constexpr uint32_t K2_BYTES = K2_BAR + 192;
+constexpr uint32_t K2_TMEM_COLS = 256;       // S [0, 64), X [64, 128), P (chunk parity) [128, 192), [192, 256)
 
-static_assert(COPY_BYTES <= K2_STAGE, "stage too small");
-static_assert(ST_MQL == ST_MQ + 8192, "[M_hi; M_lo] is one 128-row operand");
-static_assert(K2_SB % 1024 == 0, "SW128 operands are 1024-byte aligned");
-static_assert(K1_AIL + 16384 <= K1_BWU, "INV rows 64..127 must stay inside the alias region");
-static_assert(K2_BYTES + 1024 <= 232448, "chain smem");
+static_assert(K2_BSTAGE % 1024 == 0 && K2_O0 % 1024 == 0 && K2_SB % 1024 == 0 && K2_UB % 1024 == 0,
+              "SW128 operands are 1024-byte aligned");
+static_assert(ws_u0(0) == WS_KR + 16384, "slice 0's [K_restore^T | U0] is one contiguous copy");
+static_assert(K1_AIL + 16384 <= K1_BWU, "[INV; X] must stay inside the alias region");
+static_assert(K1_ML + 16384 <= K1_BWU && K1_IL + 8192 <= K1_IS, "X operands stay inside the alias region");
+static_assert(K1_OUT_UO + NTILES * 2 * TILE_F32 <= K1_TOT && K1_OUT_A1 + 32768 <= K1_OUT_UO, "output images");
+static_assert(K1_IS + 64 * LDS_ * 4 <= K1_XS && K1_XS + 4096 <= K1_MH && 16384 + 8192 <= K1_XS,
+              "Q_decay rows land in the free L / INV region while the last MMA runs");
+static_assert(WS_BLOCK % 1024 == 0 && WS_AL + DK * 4 <= WS_BLOCK, "workspace block");
+static_assert(K2_BYTES + 1024 + 256 <= 232448, "chain smem");
 static_assert(2 * (K1_BYTES + 1024 + 1024) <= 233472, "prep must fit two CTAs per SM");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -111,16 +134,22 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 __device__ __forceinline__ void st_shared_u32(uint8_t* p, uint32_t x) { *reinterpret_cast<uint32_t*>(p) = x; }
 
-// x = hi + lo with hi = bf16(x) (returned in place) and lo = bf16(x - hi): the
-// pair carries ~16 significant bits, enough to keep an MMA operand's rounding
-// out of the error budget.
-__device__ __forceinline__ void split8(float* x, float* lo) {
+// x = hi + lo with hi = x truncated to bf16 and lo = bf16(x - hi): the pair
+// carries ~16 significant bits (|x - hi| < 2^-7 |x|, and lo is rounded to
+// nearest), enough to keep an MMA operand's rounding out of the error budget.
+// Eight values -> two packed bf16 x 8; hi needs no conversion instruction.
+__device__ __forceinline__ void split_pack8(const float* x, uint4& hi, uint4& lo) {
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const float hi = __bfloat162float(__float2bfloat16_rn(x[u]));
-        lo[u] = x[u] - hi;
-        x[u] = hi;
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t a = __float_as_uint(x[2 * j]), b = __float_as_uint(x[2 * j + 1]);
+        h[j] = __byte_perm(a, b, 0x7632);              // upper halves of a (low 16 bits) and b
+        const __nv_bfloat162 lb = __floats2bfloat162_rn(x[2 * j] - __uint_as_float(a & 0xFFFF0000u),
+                                                        x[2 * j + 1] - __uint_as_float(b & 0xFFFF0000u));
+        l[j] = *reinterpret_cast<const uint32_t*>(&lb);
     }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // One warp: acc (+)= A * B for 16x16 fp32 blocks in shared memory (row-major,
@@ -231,26 +260,27 @@ kda_tc_schedule(const int32_t* __restrict__ cu, int n_seq, int T_total, int slot
 
 // ============================================================== prep (a1-a3)
 template <int B>
-__device__ __forceinline__ void gram_epilogue(uint32_t tmem, int lane, uint8_t* mq_out, float* LS) {
+__device__ __forceinline__ void gram_epilogue(uint32_t tmem, int lane, uint8_t* mh, uint8_t* ml, float* LS) {
     constexpr int N = 16 * (B + 1);
     constexpr int OFF = 8 * B * (B + 1);
     float v[N];
 #pragma unroll
     for (int c = 0; c < N; c += 16) kda::tmem_ld16(tmem + ((uint32_t)(32 * B) << 16) + OFF + c, v + c);
     kda::tmem_wait_ld();
-    if (lane < 16) {                          // M_qk row, diagonal included
+    if (lane < 16) {                          // M_qk row (diagonal included) -> high / low bf16 operand parts
         const int r = 16 * B + lane;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
-            float f[8], lo[8];
+            float f[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int t = 8 * cc + u;
                 f[u] = (t < N && t <= r) ? v[t < N ? t : 0] : 0.f;
             }
-            split8(f, lo);
-            *reinterpret_cast<uint4*>(mq_out + kda::sw128(r, 8 * cc, 64)) = pack8(f);
-            *reinterpret_cast<uint4*>(mq_out + 8192 + kda::sw128(r, 8 * cc, 64)) = pack8(lo);
+            uint4 hi, lo;
+            split_pack8(f, hi, lo);
+            *reinterpret_cast<uint4*>(mh + kda::sw128(r, 8 * cc, 64)) = hi;
+            *reinterpret_cast<uint4*>(ml + kda::sw128(r, 8 * cc, 64)) = lo;
         }
     } else {                                  // L row (beta folded in), strict
         const int r = 16 * B + lane - 16;
@@ -305,23 +335,46 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + K1_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + K1_BAR + 8);
+    uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + K1_BAR + 16);
     if (w == 0) {
         kda::tmem_alloc(tmem_slot, K1_TMEM_COLS);
         kda::tmem_relinquish();
     }
     if (tid == 0) {
         kda::mbar_init(bar, 1);
+        kda::mbar_init(bar_q, 1);
         kda::fence_barrier_init();
     }
+    uint32_t n_done = 0;                          // items finished by this CTA (bar_q parity)
+    uint32_t bar_phase = 0;                       // completed phases of bar (three per item)
     kda::tc_fence_before();
     __syncthreads();
     kda::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // The next item's inputs are prefetched into L2 while this one computes.
+    // Items run head-fastest, so the H heads of a chunk are processed by H
+    // neighbouring CTAs at about the same time: each prefetches its share of
+    // the chunk's token rows across all heads, which is contiguous in memory
+    // (four bulk prefetches instead of one per row and tensor).
+    auto prefetch = [&](long long it2) {
+        int t0, nr, sl, h2;
+        if (it2 >= n_items || !item(it2, t0, nr, sl, h2)) return;
+        const int per = (C + H - 1) / H;              // tokens per head slot
+        const int a0 = min(nr, h2 * per), a1 = min(nr, a0 + per);
+        if (a0 >= a1) return;
+        const size_t off = (size_t)(t0 + a0) * H * DK;
+        const uint32_t rows = (uint32_t)(a1 - a0) * (uint32_t)H;
+        kda::prefetch_l2(q + off, rows * DK * 2);
+        kda::prefetch_l2(k + off, rows * DK * 2);
+        kda::prefetch_l2(v + off, rows * DV * 2);
+        kda::prefetch_l2(g + off, rows * DK * 4);
+    };
     for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
         int tok0, nrows, slot, h;
         if (!item(it, tok0, nrows, slot, h)) continue;
         uint8_t* blk = ws_blocks + ((size_t)slot * H + h) * WS_BLOCK;
+        if (tid == 32 * 7) prefetch(it + gridDim.x);
 
         // ---------------- a1: loads and per-block cumulative log-decay
         const int p = w >> 2, b = w & 3;          // channel panel, row block
@@ -341,6 +394,16 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
             kv[rr] = ok ? *reinterpret_cast<const uint32_t*>(k + off) : 0u;
             bt[rr] = ok ? beta[tok * H + h] : 0.f;
         }
+        uint4 vx[C * (DV / 8) / 256];              // this thread's share of the V tile
+#pragma unroll
+        for (int i = 0; i < C * (DV / 8) / 256; ++i) {
+            const int e = tid + 256 * i, t = e >> 4, cc = e & 15;
+            vx[i] = t < nrows ? *reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + t) * H + h) * DV + 8 * cc)
+                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+        // the previous item's output images must have left shared memory
+        if (tid == 0) kda::bulk_wait_read_all();
+        __syncthreads();
         float* nrm = reinterpret_cast<float*>(sm + K1_NRM);
         if (PROLOGUE) {
             // fused prologue: gates from their pre-activations; squared norms of
@@ -366,11 +429,10 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
             }
         }
         // V slice -> right half of the [K_decay | V] operand (MN-major)
-        for (int e = tid; e < C * (DV / 8); e += 256) {
-            const int t = e >> 4, cc = e & 15;
-            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (t < nrows) x = *reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + t) * H + h) * DV + 8 * cc);
-            *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) = x;
+#pragma unroll
+        for (int i = 0; i < C * (DV / 8) / 256; ++i) {
+            const int e = tid + 256 * i, t = e >> 4, cc = e & 15;
+            *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) = vx[i];
         }
 #pragma unroll
         for (int rr = 1; rr < 16; ++rr) { G0[rr] += G0[rr - 1]; G1[rr] += G1[rr - 1]; }
@@ -444,7 +506,7 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
             // K_restore -> K_restore^T image (MN-major: row = token, contiguous = channel)
             *reinterpret_cast<uint32_t*>(blk + WS_KR + kda::sw128(r, ch, 64)) = kda::pack_bf16x2(kt0 * R0, kt1 * R1);
         }
-        kda::fence_proxy_async_smem();
+        kda::fence_proxy_async_all();              // shared operands and the Q_decay rows read back later
         kda::tc_fence_before();
         __syncthreads();
 
@@ -462,16 +524,17 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
             }
             kda::umma_commit(bar);
         }
-        if (!kda::mbar_wait(bar, 0, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        if (!kda::mbar_wait(bar, bar_phase & 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        ++bar_phase;
         kda::tc_fence_after();
 
         float* LS = reinterpret_cast<float*>(sm + K1_LS);
         float* IS = reinterpret_cast<float*>(sm + K1_IS);
         float* XS = reinterpret_cast<float*>(sm + K1_XS);
-        if (w == 0) gram_epilogue<0>(tmem, lane, blk + WS_MQ, LS);
-        else if (w == 1) gram_epilogue<1>(tmem, lane, blk + WS_MQ, LS);
-        else if (w == 2) gram_epilogue<2>(tmem, lane, blk + WS_MQ, LS);
-        else if (w == 3) gram_epilogue<3>(tmem, lane, blk + WS_MQ, LS);
+        if (w == 0) gram_epilogue<0>(tmem, lane, sm + K1_MH, sm + K1_ML, LS);
+        else if (w == 1) gram_epilogue<1>(tmem, lane, sm + K1_MH, sm + K1_ML, LS);
+        else if (w == 2) gram_epilogue<2>(tmem, lane, sm + K1_MH, sm + K1_ML, LS);
+        else if (w == 3) gram_epilogue<3>(tmem, lane, sm + K1_MH, sm + K1_ML, LS);
         kda::tc_fence_before();
         __syncthreads();
 
@@ -539,17 +602,69 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
             st16(blkI(2 + yi, yj), LDS_, acc, lane, -1.f);
         }
         __syncthreads();
-        // INV Diag(beta) -> K-major A operand as high + low bf16 parts
+        // (5) X = M_qk INV on the tensor cores: INV -> high / low bf16 operand parts
+        // (over L), then X = M_hi I_hi + M_hi I_lo + M_lo I_hi into TMEM
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
             const int e = tid + 256 * it;
-            const int r = e >> 3, cc = e & 7;
-            float f[8], lo[8];
+            const int t = e >> 3, cc = e & 7;
+            uint4 hi, lo;
+            split_pack8(IS + t * LDS_ + 8 * cc, hi, lo);
+            *reinterpret_cast<uint4*>(sm + K1_IH + kda::sw128(t, 8 * cc, 64)) = hi;
+            *reinterpret_cast<uint4*>(sm + K1_IL + kda::sw128(t, 8 * cc, 64)) = lo;
+        }
+        kda::fence_proxy_async_smem();
+        kda::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            kda::tc_fence_after();
+            const uint32_t idesc = kda::idesc_bf16(128, 64, 0, 1);
+            const uint32_t sA[3] = {kda::smem_u32(sm + K1_MH), kda::smem_u32(sm + K1_MH), kda::smem_u32(sm + K1_ML)};
+            const uint32_t sB[3] = {kda::smem_u32(sm + K1_IH), kda::smem_u32(sm + K1_IL), kda::smem_u32(sm + K1_IH)};
 #pragma unroll
-            for (int u = 0; u < 8; ++u) f[u] = IS[r * LDS_ + 8 * cc + u] * beta_s[8 * cc + u];
-            split8(f, lo);
-            *reinterpret_cast<uint4*>(sm + K1_AI + kda::sw128(r, 8 * cc, 64)) = pack8(f);
-            *reinterpret_cast<uint4*>(sm + K1_AIL + kda::sw128(r, 8 * cc, 64)) = pack8(lo);
+            for (int pr = 0; pr < 3; ++pr) {
+#pragma unroll
+                for (int st = 0; st < 4; ++st) {
+                    const uint64_t ad = kda::sw128_desc(sA[pr] + st * 32, 16, 1024);
+                    const uint64_t bd = kda::sw128_desc(sB[pr] + st * 2048, 8192, 1024);
+                    kda::umma_bf16(tmem + K1_TX, ad, bd, idesc, (pr | st) ? 1u : 0u);
+                }
+            }
+            kda::umma_commit(bar);
+        }
+        if (!kda::mbar_wait(bar, bar_phase & 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        ++bar_phase;
+        kda::tc_fence_after();
+        // [INV; X] Diag(beta) -> 128-row K-major A operand as high + low bf16 parts
+        // (the operand overlays the M_qk parts, which the X product has finished reading)
+        if ((w & 2) == 0) {                        // warps 0, 1, 4, 5: X rows from TMEM lanes 0..63
+            const int r = 32 * (w & 1) + lane, c0 = 32 * (w >> 2);
+            float x[32];
+            kda::tmem_ld32(tmem + ((uint32_t)(32 * (w & 1)) << 16) + K1_TX + c0, x);
+            kda::tmem_wait_ld();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float f[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) f[u] = x[8 * cc + u] * beta_s[c0 + 8 * cc + u];
+                uint4 hi, lo;
+                split_pack8(f, hi, lo);
+                *reinterpret_cast<uint4*>(sm + K1_AI + kda::sw128(64 + r, c0 + 8 * cc, 64)) = hi;
+                *reinterpret_cast<uint4*>(sm + K1_AIL + kda::sw128(64 + r, c0 + 8 * cc, 64)) = lo;
+            }
+        } else {                                   // warps 2, 3, 6, 7: INV rows from shared memory
+            const int li = 32 * (((w >> 2) << 1) | (w & 1)) + lane;
+            const int r = li >> 1, c0 = 32 * (li & 1);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                float f[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) f[u] = IS[r * LDS_ + c0 + 8 * cc + u] * beta_s[c0 + 8 * cc + u];
+                uint4 hi, lo;
+                split_pack8(f, hi, lo);
+                *reinterpret_cast<uint4*>(sm + K1_AI + kda::sw128(r, c0 + 8 * cc, 64)) = hi;
+                *reinterpret_cast<uint4*>(sm + K1_AIL + kda::sw128(r, c0 + 8 * cc, 64)) = lo;
+            }
         }
         kda::fence_proxy_async_smem();
         kda::tc_fence_before();
@@ -571,78 +686,123 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
                 }
             }
             kda::umma_commit(bar);
+            // meanwhile, the Q_decay rows (both 64-channel panels) back into the [Q'; W] image
+            kda::mbar_arrive_expect_tx(bar_q, 16384);
+            kda::bulk_g2s(sm + K1_OUT_A1, blk + WS_A1, 8192, bar_q);
+            kda::bulk_g2s(sm + K1_OUT_A1 + 16384, blk + WS_A1 + 16384, 8192, bar_q);
         }
-        if (!kda::mbar_wait(bar, 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        if (!kda::mbar_wait(bar, bar_phase & 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        ++bar_phase;
         kda::tc_fence_after();
 
-        if (w == 0 || w == 1) {                    // W rows -> rows 64..127 of [Q_decay; W]
-            const int r = 32 * w + lane;
+        // TMEM lanes 0..63 hold [W | U0], lanes 64..127 hold [M_qk W | O0] (columns 0..127 | 128..255)
+        const int quad = w & 3, r = 32 * (quad & 1) + lane;
+        const uint32_t t_row = tmem + ((uint32_t)(32 * quad) << 16) + (w >= 4 ? 128u : 0u);
+        if (w == 0 || w == 1) {                    // W rows -> rows 64..127 of [Q'; W]
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 float x[32];
-                kda::tmem_ld32(tmem + ((uint32_t)(32 * w) << 16) + 32 * cb, x);
+                kda::tmem_ld32(t_row + 32 * cb, x);
                 kda::tmem_wait_ld();
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    *reinterpret_cast<uint4*>(blk + WS_A1 + kda::sw128(64 + r, 32 * cb + 8 * u, 128)) = pack8(x + 8 * u);
+                    *reinterpret_cast<uint4*>(sm + K1_OUT_A1 + kda::sw128(64 + r, 32 * cb + 8 * u, 128)) = pack8(x + 8 * u);
             }
-        } else if (w == 4 || w == 5) {             // U0 rows (fp32) -> [tile][row][NT]
-            const int r = 32 * (w - 4) + lane;
+        } else if (w == 2 || w == 3) {             // Q' = Q_decay - M_qk W -> rows 0..63 of [Q'; W]
+            if (!kda::mbar_wait(bar_q, n_done & 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 float x[32];
-                kda::tmem_ld32(tmem + ((uint32_t)(32 * (w - 4)) << 16) + 128 + 32 * cb, x);
+                kda::tmem_ld32(t_row + 32 * cb, x);
+                kda::tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4* qp = reinterpret_cast<uint4*>(sm + K1_OUT_A1 + kda::sw128(r, 32 * cb + 8 * u, 128));
+                    const uint4 qd = *qp;
+                    const uint32_t qs[4] = {qd.x, qd.y, qd.z, qd.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 f = kda::unpack_bf16x2(qs[j]);
+                        x[8 * u + 2 * j] = f.x - x[8 * u + 2 * j];
+                        x[8 * u + 2 * j + 1] = f.y - x[8 * u + 2 * j + 1];
+                    }
+                    *qp = pack8(x + 8 * u);
+                }
+            }
+        } else {                                   // U0 (warps 4, 5) or O0 (warps 6, 7) rows, fp32, per d_v slice
+            const uint32_t part = w < 6 ? 0u : TILE_F32;
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                float x[32];
+                kda::tmem_ld32(t_row + 32 * cb, x);
                 kda::tmem_wait_ld();
                 const int j = 32 * cb, tile = j / NT;
-                float4* dst = reinterpret_cast<float4*>(blk + WS_U0 + (size_t)(tile * C + r) * NT * 4);
+                float4* dst = reinterpret_cast<float4*>(sm + K1_OUT_UO + (ws_u0(tile) - WS_UO) + part + r * NT * 4);
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     dst[((j % NT) / 4 + u) ^ (r & 7)] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
             }
         }
+        kda::fence_proxy_async_smem();
         kda::tc_fence_before();
         __syncthreads();                           // shared memory and TMEM are reused by the next item
         kda::tc_fence_after();
+        if (tid == 0) {
+            kda::bulk_s2g(blk + WS_A1, sm + K1_OUT_A1, 32768);
+            kda::bulk_s2g(blk + WS_UO, sm + K1_OUT_UO, NTILES * 2 * TILE_F32);
+            kda::bulk_commit();
+        }
+        ++n_done;
     }
+    if (tid == 0) kda::bulk_wait_all();           // the workspace is complete when the kernel ends
     if (w == 0) kda::tmem_dealloc(tmem, K1_TMEM_COLS);
 }
 
 // ============================================================== chain (a4, a5)
-// Per CTA: one (sequence, head) pair and NT = 64 columns of d_v.  The high
-// and low bf16 parts of U sit side by side along N where the product allows
-// it.  TMEM columns:
+// Per CTA: one (sequence, head) pair and NT = 64 columns of d_v.  TMEM columns:
 //   [0, 64)      S, the fp32 state slice (TMEM lane = key channel)
 //   [64, 128)    X, the low-part share K_restore^T U_lo of the state update,
 //                folded into S when the state is next read
-//   [128, 256), [256, 384)  P buffers (chunk parity)
-// MMAs per chunk (20 instructions):
-//   P[:, 0:64]   = [Q_decay; W] S_in              K = 128, N = 64   -> commit(p)
-//   [S | X]     += K_restore^T [U_hi | U_lo]     K = 64,  N = 128  -> commit(s)
-//   P[:, 0:64]  += [M_hi; M_lo] U_hi             K = 64,  N = 64
-//   P[:, 64:128] = [M_hi; M_lo] U_lo             K = 64,  N = 64   -> commit(o)
-// The W rows of P are zeroed once U has been formed, so after the last
-// product lanes 0..63 of P hold Q_decay S + M_hi U and lanes 64..127 hold
-// M_lo U: output row r is the sum of the two 64-column blocks of lanes r and
-// 64 + r.
+//   [128, 192)   P = [Q'; W] S_in: lanes 0..63 Q' S_in, lanes 64..127 W S_in
+// MMAs per chunk (12 instructions):
+//   P        = [Q'; W] S_in                 K = 128, N = 64   -> commit(p)
+//   [S | X] += K_restore^T [U_hi | U_lo]    K = 64,  N = 128  -> commit(s)
+// with U = U0 - W S_in and O = Q' S_in + O0.  Q' = Q_decay - M_qk W and
+// O0 = M_qk U0 come from the prep kernel, so O = Q_decay S_in + M_qk U needs no
+// product of its own here.
+// Operands stream through three rings filled by bulk copies: [Q'; W] (needed
+// first, released when P is done), [K_restore^T | U0] (released after the
+// state update) and O0 (used one chunk later); a_last is read into registers
+// one chunk ahead.  P alternates between two TMEM buffers, so the output rows
+// of chunk c are formed while chunk c + 1 runs, off the sequential path.
 // Warp roles:
-//   warps 0-7  conversion warps; warp w reads TMEM lanes 32 (w % 4) .. +31 and
-//              columns 32 (w / 4) .. +31 of each 64-wide block.
-//              - all 8: S_in = S + X -> bf16 operand, S <- Diag(a_last) S_in, X <- 0  (chunk c)
-//              - lanes 64..127 (warps 2, 3, 6, 7): M_lo U share of O (chunk c - 1) -> shared
-//                memory; U = U0 - W S_in -> high/low bf16 operand; W rows of P <- 0           (chunk c)
-//              - lanes 0..63 (warps 0, 1, 4, 5): O rows                                       (chunk c - 1)
-//   warp 8     lane 0 issues every MMA and bulk copy.
-// Named barriers: 1 = everyone; 2 = conversion warps arrive, issuer waits
-// (U ready); 3 = lanes 64..127 warps arrive, lanes 0..63 warps wait (O share);
-// 4 = conversion warps, once, before the last chunk's O.
-constexpr int K2_THREADS = 288;
-constexpr int K2_ISSUER_WARP = 8;
+//   warps 0-15 conversion warps; warp w reads TMEM lanes 32 (w % 4) .. +31 and
+//              columns 16 (w / 4) .. +15 of each 64-wide block (four warps per
+//              sub-partition, so that their latencies overlap).
+//              - all 16: S_in = S + X -> bf16 operand; then S <- Diag(a_last) S_in, X <- 0
+//              - lanes 64..127 (w % 4 = 2, 3): U = U0 - W S_in -> high/low bf16 operand
+//              - lanes 0..63 (w % 4 = 0, 1): O rows of the previous chunk =
+//                Q' S_in + O0, staged in shared memory and stored row by row
+//   warp 16    lane 0 issues the MMAs
+//   warp 17    lane 0 issues the bulk copies
+// Named barriers (warps 0-16): 1 = S_in ready; 2 = conversion warps arrive, the
+// issuer waits (U ready, state rescaled); 3 = the eight O warps (output staging).
+constexpr int K2_CONV_WARPS = 16;
+constexpr int K2_CW = NT / (K2_CONV_WARPS / 4);   // state columns per conversion warp
+constexpr int K2_THREADS = 32 * (K2_CONV_WARPS + 2);
+constexpr int K2_SYNC = 32 * (K2_CONV_WARPS + 1);  // conversion warps + the MMA issuer
+constexpr int K2_ISSUER_WARP = K2_CONV_WARPS;
+constexpr int K2_PRODUCER_WARP = K2_CONV_WARPS + 1;
+static_assert(K2_CW == 16, "conversion code below moves 16 columns per thread");
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 __device__ __forceinline__ void named_bar_arrive(int id, int count) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(kda::smem_u32(bar)) : "memory");
 }
 
 __global__ void __launch_bounds__(K2_THREADS, 1)
@@ -669,269 +829,277 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     if (ckpt_every > 0)
         ck_base = use_table ? kda::ckpt_base(n, ckpt_every, [&](int m) { return seq_info[m].y; })
                             : n * (fixed_len / ckpt_every);
-    // store this thread's 32 state values as checkpoint `idx` (if it fits)
-    auto put_ckpt = [&](int idx, const float* v32, int row_, int col0) {
+    // store this thread's K2_CW state values as checkpoint `idx` (if it fits)
+    auto put_ckpt = [&](int idx, const float* vals, int row_, int col0) {
         if (idx < 0 || idx >= ckpt_cap) return;
         float4* dst = reinterpret_cast<float4*>(ckpt + (((size_t)idx * H + h) * DK + row_) * DV + tile * NT + col0);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) dst[u] = make_float4(v32[4 * u], v32[4 * u + 1], v32[4 * u + 2], v32[4 * u + 3]);
+        for (int u = 0; u < K2_CW / 4; ++u)
+            dst[u] = make_float4(vals[4 * u], vals[4 * u + 1], vals[4 * u + 2], vals[4 * u + 3]);
     };
+    auto block_of = [&](int c) { return ws_blocks + ((size_t)(first + cb + c) * H + h) * WS_BLOCK; };
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + K2_BAR);
-    uint64_t* bar_p = full + K2_NS;
+    uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + K2_BAR);
+    uint64_t* emptyA = fullA + K2_NA;
+    uint64_t* fullB = emptyA + K2_NA;
+    uint64_t* emptyB = fullB + K2_NB;
+    uint64_t* fullO = emptyB + K2_NB;
+    uint64_t* emptyO = fullO + K2_NO;
+    uint64_t* bar_p = emptyO + K2_NO;
     uint64_t* bar_s = bar_p + 1;
-    uint64_t* bar_o = bar_p + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_p + 3);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 1);
     if (w == 0) {
         kda::tmem_alloc(tmem_slot, K2_TMEM_COLS);
         kda::tmem_relinquish();
     }
     if (tid == 0) {
-        for (int s = 0; s < K2_NS; ++s) kda::mbar_init(full + s, 1);
+        for (int s = 0; s < K2_NA; ++s) { kda::mbar_init(fullA + s, 1); kda::mbar_init(emptyA + s, 1); }
+        // a B stage is free once the state update has read it (one commit) and
+        // the eight warps of lanes 64..127 have read their U0 rows
+        for (int s = 0; s < K2_NB; ++s) { kda::mbar_init(fullB + s, 1); kda::mbar_init(emptyB + s, 9); }
+        // an O stage is free once the eight warps of lanes 0..63 have stored its rows
+        for (int s = 0; s < K2_NO; ++s) { kda::mbar_init(fullO + s, 1); kda::mbar_init(emptyO + s, 8); }
         kda::mbar_init(bar_p, 1);
         kda::mbar_init(bar_s, 1);
-        kda::mbar_init(bar_o, 1);
         kda::fence_barrier_init();
     }
     kda::tc_fence_before();
     __syncthreads();
     kda::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const bool issuer = (w == K2_ISSUER_WARP);
-    const int quad = w & 3, half = (w >> 2) & 1;
-    const int row = 32 * quad + lane;                       // TMEM lane = state row / P row
-    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-    const uint32_t tS = tmem + lane_off + 32 * half;        // this warp's 32 state columns (X at +64)
-    auto tP = [&](int c) { return tmem + lane_off + 128 + 128 * (c & 1) + 32 * half; };   // S_hi part; S_lo at +64
-
-    auto issue = [&](int c) {
-        const int st = c % K2_NS;
-        uint8_t* stage = sm + st * K2_STAGE;
-        const uint8_t* src = ws_blocks + ((size_t)(first + cb + c) * H + h) * WS_BLOCK;
-        kda::mbar_arrive_expect_tx(full + st, COPY_BYTES);
-        kda::bulk_g2s(stage + ST_A1, src + WS_A1, 32768, full + st);
-        kda::bulk_g2s(stage + ST_KR, src + WS_KR, 16384, full + st);
-        kda::bulk_g2s(stage + ST_MQ, src + WS_MQ, 16384, full + st);
-        kda::bulk_g2s(stage + ST_U0, src + WS_U0 + (uint32_t)tile * C * NT * 4, C * NT * 4, full + st);
-        kda::bulk_g2s(stage + ST_AL, src + WS_AL, DK * 4, full + st);
-    };
     auto wait = [&](uint64_t* b, uint32_t parity) {
         if (!kda::mbar_wait(b, parity, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
     };
 
-    // initial state slice -> TMEM (X = 0); first stages in flight
-    if (!issuer) {
-        float s[32];
-        if (S0) {
-            const float4* src =
-                reinterpret_cast<const float4*>(S0 + (((size_t)n * H + h) * DK + row) * DV + tile * NT + 32 * half);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float4 x = src[u];
-                s[4 * u] = x.x; s[4 * u + 1] = x.y; s[4 * u + 2] = x.z; s[4 * u + 3] = x.w;
-            }
-        } else {
-#pragma unroll
-            for (int u = 0; u < 32; ++u) s[u] = 0.f;
-        }
-        kda::tmem_st32(tS, s);
-#pragma unroll
-        for (int u = 0; u < 32; ++u) s[u] = 0.f;
-        kda::tmem_st32(tS + 64, s);
-        kda::tmem_wait_st();
-    } else if (lane == 0) {
-        for (int c = 0; c < min(K2_NS, nloc); ++c) issue(c);
-    }
-    kda::tc_fence_before();
-    __syncthreads();
-    kda::tc_fence_after();
-
-    const uint32_t sSB = kda::smem_u32(sm + K2_SB), sUB = kda::smem_u32(sm + K2_UB);
-    // O of chunk c, lanes 64..127 (after bar_o(c)): M_lo U -> shared memory (bf16;
-    // it is a low-order correction), then release the lanes 0..63 warps
-    auto o_low_share = [&](int c) {
-        kda::tc_fence_after();
-        float a[32], b[32];
-        kda::tmem_ld32(tP(c), a);
-        kda::tmem_ld32(tP(c) + 64, b);
-        kda::tmem_wait_ld();
-#pragma unroll
-        for (int u = 0; u < 32; ++u) a[u] += b[u];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-            *reinterpret_cast<uint4*>(sm + K2_XO + kda::sw128(row - 64, 32 * half + 8 * cc, 64)) = pack8(a + 8 * cc);
-        kda::tc_fence_before();
-        named_bar_arrive(3, 256);
-    };
-    // O of chunk c, lanes 0..63 (after bar_o(c)): both blocks + the M_lo U share
-    auto o_rows = [&](int c) {
-        kda::tc_fence_after();
-        float a[32], b[32];
-        kda::tmem_ld32(tP(c), a);
-        kda::tmem_ld32(tP(c) + 64, b);
-        kda::tmem_wait_ld();
-#pragma unroll
-        for (int u = 0; u < 32; ++u) a[u] += b[u];
-        kda::tc_fence_before();
-        named_bar_sync(3, 256);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const uint4 x = *reinterpret_cast<const uint4*>(sm + K2_XO + kda::sw128(row, 32 * half + 8 * cc, 64));
-            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 f = kda::unpack_bf16x2(xs[u]);
-                a[8 * cc + 2 * u] += f.x;
-                a[8 * cc + 2 * u + 1] += f.y;
-            }
-        }
-        if (row < len - (cb + c) * C) {
-            uint4* dst = reinterpret_cast<uint4*>(O + ((size_t)(bos + (cb + c) * C + row) * H + h) * DV + tile * NT +
-                                                  32 * half);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) dst[cc] = pack8(a + 8 * cc);
-        }
-    };
-
-    for (int c = 0; c < nloc; ++c) {
-        const int st = c % K2_NS;
-        uint8_t* stage = sm + st * K2_STAGE;
-        if (!issuer) {
-            // ---- S_in = S + X -> bf16 operand; S <- Diag(a_last) S_in, X <- 0
-            wait(full + st, (uint32_t)((c / K2_NS) & 1));
-            if (c > 0) wait(bar_s, (uint32_t)((c - 1) & 1));
-            kda::tc_fence_after();
-            float s[32], x[32];
-            kda::tmem_ld32(tS, s);
-            kda::tmem_ld32(tS + 64, x);
-            kda::tmem_wait_ld();
-#pragma unroll
-            for (int u = 0; u < 32; ++u) s[u] += x[u];
-            if (ckpt_every > 0 && cb + c > 0 && ((cb + c) * C) % ckpt_every == 0)   // state after (cb + c) chunks
-                put_ckpt(ck_base + (cb + c) * C / ckpt_every - 1, s, row, 32 * half);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(row, 32 * half + 8 * cc, 128)) = pack8(s + 8 * cc);
-            kda::fence_proxy_async_smem();
-            kda::tc_fence_before();
-            named_bar_sync(1, K2_THREADS);
-            // S <- Diag(a_last) S_in, X <- 0 while the P product runs (done before barrier 2)
-            const float al = reinterpret_cast<const float*>(stage + ST_AL)[row];
-#pragma unroll
-            for (int u = 0; u < 32; ++u) { s[u] *= al; x[u] = 0.f; }
-            kda::tmem_st32(tS, s);
-            kda::tmem_st32(tS + 64, x);
-            kda::tmem_wait_st();
-            // bar_o(c - 1) is observed by every conversion warp before barrier 2
-            // lets bar_o(c) be committed (a parity wait cannot skip a phase)
-            if (c > 0) wait(bar_o, (uint32_t)((c - 1) & 1));
-            if (quad >= 2) {
-                // ---- U = U0 - W S_in -> high/low bf16 operand; W rows of P <- 0
-                const int r = row - 64;
-                wait(bar_p, (uint32_t)(c & 1));
-                kda::tc_fence_after();
-                float ph[32];
-                kda::tmem_ld32(tP(c), ph);
-                kda::tmem_wait_ld();
-                const float4* u0 = reinterpret_cast<const float4*>(stage + ST_U0 + r * NT * 4);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const float4 x0 = u0[(8 * half + 2 * cc) ^ (r & 7)], x1 = u0[(8 * half + 2 * cc + 1) ^ (r & 7)];
-                    float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w}, lo[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) f[u] -= ph[8 * cc + u];
-                    split8(f, lo);
-                    const uint32_t off = kda::sw128(r, 32 * half + 8 * cc, 64);
-                    *reinterpret_cast<uint4*>(sm + K2_UB + off) = pack8(f);
-                    *reinterpret_cast<uint4*>(sm + K2_UB + 8192 + off) = pack8(lo);
+    if (w == K2_PRODUCER_WARP) {
+        // ---------------- bulk copies, in the order the chunks need them
+        if (lane == 0) {
+            auto issueA = [&](int k) {
+                const int st = k % K2_NA;
+                if (k >= K2_NA) wait(emptyA + st, (uint32_t)(((k - K2_NA) / K2_NA) & 1));
+                kda::mbar_arrive_expect_tx(fullA + st, K2_ASTAGE);
+                kda::bulk_g2s(sm + st * K2_ASTAGE, block_of(k) + WS_A1, K2_ASTAGE, fullA + st);
+            };
+            auto issueB = [&](int k) {
+                const int st = k % K2_NB;
+                if (k >= K2_NB) wait(emptyB + st, (uint32_t)(((k - K2_NB) / K2_NB) & 1));
+                uint8_t* dst = sm + K2_B0 + st * K2_BSTAGE;
+                const uint8_t* src = block_of(k);
+                kda::mbar_arrive_expect_tx(fullB + st, K2_BSTAGE);
+                if (tile == 0) {
+                    kda::bulk_g2s(dst, src + WS_KR, K2_BSTAGE, fullB + st);
+                } else {
+                    kda::bulk_g2s(dst, src + WS_KR, 16384, fullB + st);
+                    kda::bulk_g2s(dst + 16384, src + ws_u0(tile), TILE_F32, fullB + st);
                 }
-#pragma unroll
-                for (int u = 0; u < 32; ++u) ph[u] = 0.f;
-                kda::tmem_st32(tP(c), ph);
-                kda::tmem_wait_st();
-                kda::fence_proxy_async_smem();
-                kda::tc_fence_before();
-                named_bar_arrive(2, K2_THREADS);
-                if (c > 0) o_low_share(c - 1);              // O of chunk c - 1: M_lo U share
-            } else {
-                kda::tc_fence_before();
-                named_bar_arrive(2, K2_THREADS);
-                if (c > 0) o_rows(c - 1);                   // O of chunk c - 1 (overlaps the U conversion)
+            };
+            auto issueO = [&](int k) {
+                const int st = k % K2_NO;
+                if (k >= K2_NO) wait(emptyO + st, (uint32_t)(((k - K2_NO) / K2_NO) & 1));
+                kda::mbar_arrive_expect_tx(fullO + st, K2_OSTAGE);
+                kda::bulk_g2s(sm + K2_O0 + st * K2_OSTAGE, block_of(k) + ws_u0(tile) + TILE_F32, K2_OSTAGE, fullO + st);
+            };
+            for (int k = 0; k < nloc; ++k) {
+                issueA(k);
+                issueB(k);
+                issueO(k);
             }
-        } else {
-            named_bar_sync(1, K2_THREADS);
-            if (lane == 0) {                                // P = [Q_decay; W] S_in
-                wait(full + st, (uint32_t)((c / K2_NS) & 1));
+        }
+    } else if (w == K2_ISSUER_WARP) {
+        // ---------------- MMAs
+        const uint32_t sSB = kda::smem_u32(sm + K2_SB), sUB = kda::smem_u32(sm + K2_UB);
+        named_bar_sync(1, K2_SYNC);                        // initial state in TMEM
+        for (int c = 0; c < nloc; ++c) {
+            const int sa = c % K2_NA, sb = c % K2_NB;
+            if (lane == 0) wait(fullA + sa, (uint32_t)((c / K2_NA) & 1));
+            __syncwarp();
+            named_bar_sync(1, K2_SYNC);
+            if (lane == 0) {                                // P = [Q'; W] S_in
                 kda::tc_fence_after();
-                const uint32_t sA1 = kda::smem_u32(stage + ST_A1);
+                const uint32_t sA1 = kda::smem_u32(sm + sa * K2_ASTAGE);
                 const uint32_t idesc = kda::idesc_bf16(128, NT, 0, 1);
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     const uint64_t ad = kda::sw128_desc(sA1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
                     const uint64_t bd = kda::sw128_desc(sSB + s * 2048, 16384, 1024);
-                    kda::umma_bf16(tmem + 128 + 128 * (c & 1), ad, bd, idesc, s > 0 ? 1u : 0u);
+                    kda::umma_bf16(tmem + 128 + 64 * (c & 1), ad, bd, idesc, s > 0 ? 1u : 0u);
                 }
                 kda::umma_commit(bar_p);
-                // the previous chunk's stage is free once its last MMA (the O product) is done
-                if (c >= 1) {
-                    wait(bar_o, (uint32_t)((c - 1) & 1));
-                    if (c - 1 + K2_NS < nloc) issue(c - 1 + K2_NS);
-                }
+                kda::umma_commit(emptyA + sa);
+                wait(fullB + sb, (uint32_t)((c / K2_NB) & 1));
             }
             __syncwarp();
-            named_bar_sync(2, K2_THREADS);
-            if (lane == 0) {
+            named_bar_sync(2, K2_SYNC);
+            if (lane == 0) {                                // [S | X] += K_restore^T [U_hi | U_lo]
                 kda::tc_fence_after();
-                const uint32_t sKR = kda::smem_u32(stage + ST_KR), sMQ = kda::smem_u32(stage + ST_MQ);
+                const uint32_t sKR = kda::smem_u32(sm + K2_B0 + sb * K2_BSTAGE);
                 const uint32_t id_s = kda::idesc_bf16(128, 2 * NT, 1, 1);
-                const uint32_t id_o = kda::idesc_bf16(128, NT, 0, 1);
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {               // [S | X] += K_restore^T [U_hi | U_lo]
+                for (int s = 0; s < 4; ++s) {
                     const uint64_t ad = kda::sw128_desc(sKR + s * 2048, 8192, 1024);
                     const uint64_t bd = kda::sw128_desc(sUB + s * 2048, 8192, 1024);
                     kda::umma_bf16(tmem, ad, bd, id_s, 1u);
                 }
                 kda::umma_commit(bar_s);
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {      // P += [M_hi; M_lo] U_hi;  P' = [M_hi; M_lo] U_lo
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const uint64_t ad = kda::sw128_desc(sMQ + s * 32, 16, 1024);
-                        const uint64_t bd = kda::sw128_desc(sUB + part * 8192 + s * 2048, 8192, 1024);
-                        kda::umma_bf16(tmem + 128 + 128 * (c & 1) + 64 * part, ad, bd, id_o,
-                                       (part == 0 || s > 0) ? 1u : 0u);
-                    }
-                }
-                kda::umma_commit(bar_o);
+                kda::umma_commit(emptyB + sb);
             }
             __syncwarp();
         }
-    }
-    if (!issuer) {
-        if (nloc > 0) {
-            // barrier 3 must not see two arrivals of the lanes 64..127 warps before
-            // the lanes 0..63 warps have passed it for chunk nloc - 2
-            named_bar_sync(4, 256);
-            wait(bar_o, (uint32_t)((nloc - 1) & 1));
-            if (quad >= 2) o_low_share(nloc - 1);
-            else o_rows(nloc - 1);
-            wait(bar_s, (uint32_t)((nloc - 1) & 1));
+    } else {
+        // ---------------- conversion warps
+        const int quad = w & 3, grp = w >> 2;
+        const int row = 32 * quad + lane;                       // TMEM lane = state row / P row
+        const int col0 = K2_CW * grp;                           // this warp's first column of the slice
+        const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+        const uint32_t tS = tmem + lane_off + col0;             // this warp's state columns (X at +64)
+        const uint32_t tP = tmem + lane_off + 128 + col0;       // ... of P (buffer of chunk parity at +64)
+        // O rows of chunk co (lanes 0..63 warps): P of that chunk is complete (the
+        // state update issued after it is); its O0 stage is staged over and stored
+        auto out_rows = [&](int co) {
+            const int so = co % K2_NO;
+            wait(fullO + so, (uint32_t)((co / K2_NO) & 1));
+            kda::tc_fence_after();
+            float ph[K2_CW];
+            kda::tmem_ld16(tP + 64 * (co & 1), ph);
+            kda::tmem_wait_ld();
+            uint8_t* o0b = sm + K2_O0 + so * K2_OSTAGE;
+            const float4* o0 = reinterpret_cast<const float4*>(o0b + row * NT * 4);
+            uint4 ov[K2_CW / 8];
+#pragma unroll
+            for (int cc = 0; cc < K2_CW / 8; ++cc) {
+                const int j = (col0 + 8 * cc) / 4;
+                const float4 x0 = o0[j ^ (row & 7)], x1 = o0[(j + 1) ^ (row & 7)];
+                float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int u = 0; u < 8; ++u) f[u] += ph[8 * cc + u];
+                ov[cc] = pack8(f);
+            }
+            named_bar_sync(3, K2_CONV_WARPS * 16);             // every O warp has read O0
+#pragma unroll
+            for (int cc = 0; cc < K2_CW / 8; ++cc) {
+                const int k = (col0 + 8 * cc) / 8;               // 16-byte chunk of the 128-byte row
+                *reinterpret_cast<uint4*>(o0b + row * 128 + ((k ^ (row & 7)) << 4)) = ov[cc];
+            }
+            named_bar_sync(3, K2_CONV_WARPS * 16);             // the staged tile is complete
+            const int wo = (grp << 1) | quad;                    // 0..7: rows 8 wo .. 8 wo + 7
+            const int valid = len - (cb + co) * C;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int rr = 8 * wo + i;
+                if (rr < valid) {
+                    const uint32_t x = *reinterpret_cast<const uint32_t*>(
+                        o0b + rr * 128 + (((lane >> 2) ^ (rr & 7)) << 4) + 4 * (lane & 3));
+                    *reinterpret_cast<uint32_t*>(O + ((size_t)(bos + (cb + co) * C + rr) * H + h) * DV + tile * NT +
+                                                 2 * lane) = x;
+                }
+            }
+            kda::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(emptyO + so);
+        };
+        {
+            // initial state slice -> TMEM (X = 0)
+            float s[K2_CW];
+            if (S0) {
+                const float4* src = reinterpret_cast<const float4*>(S0 + (((size_t)n * H + h) * DK + row) * DV +
+                                                                    tile * NT + col0);
+#pragma unroll
+                for (int u = 0; u < K2_CW / 4; ++u) {
+                    const float4 x = src[u];
+                    s[4 * u] = x.x; s[4 * u + 1] = x.y; s[4 * u + 2] = x.z; s[4 * u + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < K2_CW; ++u) s[u] = 0.f;
+            }
+            kda::tmem_st16(tS, s);
+#pragma unroll
+            for (int u = 0; u < K2_CW; ++u) s[u] = 0.f;
+            kda::tmem_st16(tS + 64, s);
+            kda::tmem_wait_st();
+            kda::tc_fence_before();
+            named_bar_sync(1, K2_SYNC);
         }
-        kda::tc_fence_after();
-        const bool end_ckpt = ckpt_every > 0 && nloc > 0 && cb + nloc == nch && len % ckpt_every == 0;
-        if (S_final || end_ckpt) {
-            float s[32], x[32];
-            kda::tmem_ld32(tS, s);
-            kda::tmem_ld32(tS + 64, x);
+        float al_next = nloc > 0 ? reinterpret_cast<const float*>(block_of(0) + WS_AL)[row] : 1.f;
+        for (int c = 0; c < nloc; ++c) {
+            const float al = al_next;
+            if (c + 1 < nloc) al_next = reinterpret_cast<const float*>(block_of(c + 1) + WS_AL)[row];
+            // ---- S_in = S + X -> bf16 operand
+            if (c > 0) wait(bar_s, (uint32_t)((c - 1) & 1));
+            kda::tc_fence_after();
+            float s[K2_CW], x[K2_CW];
+            kda::tmem_ld16(tS, s);
+            kda::tmem_ld16(tS + 64, x);
             kda::tmem_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 32; ++u) s[u] += x[u];
-            if (end_ckpt) put_ckpt(ck_base + len / ckpt_every - 1, s, row, 32 * half);
+            for (int u = 0; u < K2_CW; ++u) s[u] += x[u];
+#pragma unroll
+            for (int cc = 0; cc < K2_CW / 8; ++cc)
+                *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(row, col0 + 8 * cc, 128)) = pack8(s + 8 * cc);
+            kda::fence_proxy_async_smem();
+            kda::tc_fence_before();
+            named_bar_sync(1, K2_SYNC);
+            if (ckpt_every > 0 && cb + c > 0 && ((cb + c) * C) % ckpt_every == 0)   // state after (cb + c) chunks
+                put_ckpt(ck_base + (cb + c) * C / ckpt_every - 1, s, row, col0);
+            // ---- S <- Diag(a_last) S_in, X <- 0 while the P product runs
+#pragma unroll
+            for (int u = 0; u < K2_CW; ++u) { s[u] *= al; x[u] = 0.f; }
+            kda::tmem_st16(tS, s);
+            kda::tmem_st16(tS + 64, x);
+            kda::tmem_wait_st();
+            if (quad >= 2) {
+                // ---- U = U0 - W S_in -> high/low bf16 operand
+                const int sb = c % K2_NB;
+                const uint8_t* bst = sm + K2_B0 + sb * K2_BSTAGE;
+                wait(fullB + sb, (uint32_t)((c / K2_NB) & 1));
+                wait(bar_p, (uint32_t)(c & 1));
+                kda::tc_fence_after();
+                const int r = row - 64;
+                float ph[K2_CW];
+                kda::tmem_ld16(tP + 64 * (c & 1), ph);
+                kda::tmem_wait_ld();
+                const float4* u0 = reinterpret_cast<const float4*>(bst + 16384 + r * NT * 4);
+#pragma unroll
+                for (int cc = 0; cc < K2_CW / 8; ++cc) {
+                    const int j = (col0 + 8 * cc) / 4;              // 16-byte chunk of the row
+                    const float4 x0 = u0[j ^ (r & 7)], x1 = u0[(j + 1) ^ (r & 7)];
+                    float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) f[u] -= ph[8 * cc + u];
+                    uint4 hi, lo;
+                    split_pack8(f, hi, lo);
+                    const uint32_t off = kda::sw128(r, col0 + 8 * cc, 64);
+                    *reinterpret_cast<uint4*>(sm + K2_UB + off) = hi;
+                    *reinterpret_cast<uint4*>(sm + K2_UB + 8192 + off) = lo;
+                }
+                kda::fence_proxy_async_smem();
+                kda::tc_fence_before();
+                named_bar_arrive(2, K2_SYNC);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(emptyB + sb);         // this warp's U0 rows are read
+            } else {
+                kda::tc_fence_before();
+                named_bar_arrive(2, K2_SYNC);
+                if (c > 0) out_rows(c - 1);                     // the previous chunk's output
+            }
+        }
+        if (nloc > 0) wait(bar_s, (uint32_t)((nloc - 1) & 1));
+        kda::tc_fence_after();
+        if (quad < 2 && nloc > 0) out_rows(nloc - 1);
+        const bool end_ckpt = ckpt_every > 0 && nloc > 0 && cb + nloc == nch && len % ckpt_every == 0;
+        if (S_final || end_ckpt) {
+            float s[K2_CW], x[K2_CW];
+            kda::tmem_ld16(tS, s);
+            kda::tmem_ld16(tS + 64, x);
+            kda::tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < K2_CW; ++u) s[u] += x[u];
+            if (end_ckpt) put_ckpt(ck_base + len / ckpt_every - 1, s, row, col0);
             if (S_final) {
                 float4* dst = reinterpret_cast<float4*>(S_final + (((size_t)n * H + h) * DK + row) * DV +
-                                                        tile * NT + 32 * half);
+                                                        tile * NT + col0);
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
+                for (int u = 0; u < K2_CW / 4; ++u)
                     dst[u] = make_float4(s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]);
             }
         }

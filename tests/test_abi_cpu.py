@@ -98,6 +98,11 @@ def test_prefill_argument_checks(lib):
     need = lib.kda_prefill_workspace_size(1, 64, 2, 128, 128, 64, _lib.KDA_BF16)
     assert _prefill_raw(lib, ws=ctypes.c_void_p(0x100000), ws_bytes=need - 1, **tc) == E.KDA_ERR_WORKSPACE
     assert _prefill_raw(lib, ws=ctypes.c_void_p(0x100010), ws_bytes=need, **tc) == E.KDA_ERR_WORKSPACE
+    # tensor-core path: token rows move as 16-byte vectors, so unaligned tensors are refused
+    ws = dict(ws=ctypes.c_void_p(0x100000), ws_bytes=need, **tc)
+    for name in ("q", "k", "v", "g"):
+        assert _prefill_raw(lib, **{name: ctypes.c_void_p(0x1008)}, **ws) == E.KDA_ERR_INVALID_ARG, name
+    assert _prefill_raw(lib, O=ctypes.c_void_p(0x2008), **ws) == E.KDA_ERR_INVALID_ARG
 
 
 def test_prefill_ckpt_argument_checks(lib):
