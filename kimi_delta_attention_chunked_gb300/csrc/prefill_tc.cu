@@ -379,31 +379,39 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
         // ---------------- a1: loads and per-block cumulative log-decay
         const int p = w >> 2, b = w & 3;          // channel panel, row block
         const int ch = 64 * p + 2 * lane;          // this thread's two channels
-        float G0[16], G1[16], bt[16];
+        float G0[16], G1[16];
         uint32_t qv[16], kv[16];
+        // Every load is unconditional (rows past the chunk's end read its last row)
+        // so that all of them are in flight together; those rows are zeroed once
+        // the values arrive.
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
-            const int r = 16 * b + rr;
-            const bool ok = r < nrows;
-            const size_t tok = (size_t)tok0 + r;
+            const size_t tok = (size_t)tok0 + min(16 * b + rr, nrows - 1);
             const size_t off = (tok * H + h) * DK + ch;
-            float2 gg = ok ? *reinterpret_cast<const float2*>(g + off) : make_float2(0.f, 0.f);
+            const float2 gg = *reinterpret_cast<const float2*>(g + off);
             G0[rr] = gg.x;
             G1[rr] = gg.y;
-            qv[rr] = ok ? *reinterpret_cast<const uint32_t*>(q + off) : 0u;
-            kv[rr] = ok ? *reinterpret_cast<const uint32_t*>(k + off) : 0u;
-            bt[rr] = ok ? beta[tok * H + h] : 0.f;
+            qv[rr] = *reinterpret_cast<const uint32_t*>(q + off);
+            kv[rr] = *reinterpret_cast<const uint32_t*>(k + off);
         }
+        // beta of row 16 b + (lane % 16): one value per lane
+        float bt = beta[((size_t)tok0 + min(16 * b + (lane & 15), nrows - 1)) * H + h];
         uint4 vx[C * (DV / 8) / 256];              // this thread's share of the V tile
 #pragma unroll
         for (int i = 0; i < C * (DV / 8) / 256; ++i) {
             const int e = tid + 256 * i, t = e >> 4, cc = e & 15;
-            vx[i] = t < nrows ? *reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + t) * H + h) * DV + 8 * cc)
-                              : make_uint4(0u, 0u, 0u, 0u);
+            vx[i] = *reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + min(t, nrows - 1)) * H + h) * DV + 8 * cc);
         }
         // the previous item's output images must have left shared memory
         if (tid == 0) kda::bulk_wait_read_all();
         __syncthreads();
+        // rows past the chunk's end: zero inputs (log-decay 0, beta 0, q = k = 0)
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+            if (16 * b + rr >= nrows) { G0[rr] = 0.f; G1[rr] = 0.f; qv[rr] = 0u; kv[rr] = 0u; }
+        }
+        if (16 * b + (lane & 15) >= nrows) bt = 0.f;
+        else if (PROLOGUE) bt = kda::prologue_beta(bt);
         float* nrm = reinterpret_cast<float*>(sm + K1_NRM);
         if (PROLOGUE) {
             // fused prologue: gates from their pre-activations; squared norms of
@@ -413,7 +421,6 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
                 if (16 * b + rr < nrows) {
                     G0[rr] = kda::prologue_log_alpha(G0[rr]);
                     G1[rr] = kda::prologue_log_alpha(G1[rr]);
-                    bt[rr] = kda::prologue_beta(bt[rr]);
                 }
                 const float2 qf = kda::unpack_bf16x2(qv[rr]), kf = kda::unpack_bf16x2(kv[rr]);
                 float sq = fmaf(qf.x, qf.x, qf.y * qf.y), sk = fmaf(kf.x, kf.x, kf.y * kf.y);
@@ -432,7 +439,8 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
 #pragma unroll
         for (int i = 0; i < C * (DV / 8) / 256; ++i) {
             const int e = tid + 256 * i, t = e >> 4, cc = e & 15;
-            *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) = vx[i];
+            *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) =
+                t < nrows ? vx[i] : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int rr = 1; rr < 16; ++rr) { G0[rr] += G0[rr - 1]; G1[rr] += G1[rr - 1]; }
@@ -443,10 +451,7 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
         tot[b * 128 + ch + 1] = G1[15];
         first[b * 128 + ch] = G0[0];
         first[b * 128 + ch + 1] = G1[0];
-        if (p == 0 && lane == 0) {
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) beta_s[16 * b + rr] = bt[rr];
-        }
+        if (p == 0 && lane < 16) beta_s[16 * b + lane] = bt;
         __syncthreads();
 
         // global cumulative log-decay at each block start (Gs) and at the chunk end
@@ -484,7 +489,7 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
                 const float ik = rsqrtf(nrm[128 + r] + nrm[192 + r] + kda::kNormEps);
                 qf.x *= iq; qf.y *= iq; kf.x *= ik; kf.y *= ik;
             }
-            const float be = bt[rr];
+            const float be = beta_s[r];
             const float qt0 = qf.x * e0, qt1 = qf.y * e1;            // q~ (row factor)
             const float kh0 = be * kf.x * e0, kh1 = be * kf.y * e1;  // k^ = beta k (row factor)
             const float kt0 = kf.x * c0, kt1 = kf.y * c1;            // k (column factor, own block)
