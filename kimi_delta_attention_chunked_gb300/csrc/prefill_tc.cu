@@ -49,6 +49,9 @@
 //
 // Every wait on an asynchronous event is bounded; a wait that runs out records
 // KDA_ERR_TIMEOUT in the status word and the kernel runs to completion.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -80,7 +83,8 @@ constexpr uint32_t K1_BWU = 73728;           // [K_decay | V]: MN-major, K = 64 
 constexpr uint32_t K1_TOT = 106496;          // float [4][128] block totals of log-decay
 constexpr uint32_t K1_FIRST = 108544;        // float [4][128] first-row log-decay of each block
 constexpr uint32_t K1_BETA = 110592;         // float [64]
-constexpr uint32_t K1_BAR = 110848;          // MMA mbarrier (8 B), TMEM address (4 B), Q_decay copy mbarrier at +16
+constexpr uint32_t K1_BAR = 110848;          // MMA mbarrier (8 B), TMEM address (4 B), Q_decay copy mbarrier at +16,
+                                             // input copy mbarrier at +24
 constexpr uint32_t K1_NRM = 110912;          // fused prologue: float [q, k][channel half][64 rows] sums of squares
 constexpr uint32_t K1_BYTES = 111936;
 // aliases, valid once the Gram MMAs have completed
@@ -96,6 +100,12 @@ constexpr uint32_t K1_AI = 38912;            // [INV; X] Diag(beta), high bf16 p
 constexpr uint32_t K1_AIL = 55296;           // ... low bf16 part (both written once the X product is done)
 constexpr uint32_t K1_TMEM_COLS = 256;
 constexpr uint32_t K1_TX = 160;              // TMEM columns of X = M_qk INV (lanes 0..63)
+// input tiles of an item, copied by TMA over the Gram operands' space (read into
+// registers before the operands are written); V lands in its operand slot
+constexpr uint32_t K1_SG = 0;                // log-decay fp32 [64 tokens][128]
+constexpr uint32_t K1_SQ = 32768;            // q bf16 [64][128]
+constexpr uint32_t K1_SK = 49152;            // k bf16 [64][128]
+constexpr uint32_t K1_IN_BYTES = 32768 + 2 * 16384 + 16384;
 // output images, assembled once the last MMA has completed (everything below
 // K1_TOT is free then) and written to the workspace by two bulk copies
 constexpr uint32_t K1_OUT_A1 = 0;            // [Q'; W] image (rows 0..63 arrive as Q_decay from the workspace)
@@ -122,6 +132,7 @@ static_assert(ws_u0(0) == WS_KR + 16384, "slice 0's [K_restore^T | U0] is one co
 static_assert(K1_AIL + 16384 <= K1_BWU, "[INV; X] must stay inside the alias region");
 static_assert(K1_ML + 16384 <= K1_BWU && K1_IL + 8192 <= K1_IS, "X operands stay inside the alias region");
 static_assert(K1_OUT_UO + NTILES * 2 * TILE_F32 <= K1_TOT && K1_OUT_A1 + 32768 <= K1_OUT_UO, "output images");
+static_assert(K1_SK + 16384 <= K1_BWU && (K1_BWU + 16384) % 1024 == 0, "input tiles");
 static_assert(K1_IS + 64 * LDS_ * 4 <= K1_XS && K1_XS + 4096 <= K1_MH && 16384 + 8192 <= K1_XS,
               "Q_decay rows land in the free L / INV region while the last MMA runs");
 static_assert(WS_BLOCK % 1024 == 0 && WS_AL + DK * 4 <= WS_BLOCK, "workspace block");
@@ -299,8 +310,9 @@ __device__ __forceinline__ void gram_epilogue(uint32_t tmem, int lane, uint8_t* 
 
 template <bool PROLOGUE>
 __global__ void __launch_bounds__(256, 2)
-kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
-            const float* __restrict__ g, const float* __restrict__ beta, int H, int use_table,
+kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+            const float* __restrict__ beta, int H, int use_table,
             int fixed_len, int nch_per_seq, const int4* __restrict__ chunk_info,
             const int4* __restrict__ seq_info, int j_begin, int j_count, int n_x,
             uint8_t* __restrict__ ws_blocks, int* status) {
@@ -336,6 +348,7 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + K1_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + K1_BAR + 8);
     uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + K1_BAR + 16);
+    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + K1_BAR + 24);
     if (w == 0) {
         kda::tmem_alloc(tmem_slot, K1_TMEM_COLS);
         kda::tmem_relinquish();
@@ -343,6 +356,7 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
     if (tid == 0) {
         kda::mbar_init(bar, 1);
         kda::mbar_init(bar_q, 1);
+        kda::mbar_init(bar_ld, 1);
         kda::fence_barrier_init();
     }
     uint32_t n_done = 0;                          // items finished by this CTA (bar_q parity)
@@ -352,66 +366,53 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
     kda::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // The next item's inputs are prefetched into L2 while this one computes.
-    // Items run head-fastest, so the H heads of a chunk are processed by H
-    // neighbouring CTAs at about the same time: each prefetches its share of
-    // the chunk's token rows across all heads, which is contiguous in memory
-    // (four bulk prefetches instead of one per row and tensor).
-    auto prefetch = [&](long long it2) {
-        int t0, nr, sl, h2;
-        if (it2 >= n_items || !item(it2, t0, nr, sl, h2)) return;
-        const int per = (C + H - 1) / H;              // tokens per head slot
-        const int a0 = min(nr, h2 * per), a1 = min(nr, a0 + per);
-        if (a0 >= a1) return;
-        const size_t off = (size_t)(t0 + a0) * H * DK;
-        const uint32_t rows = (uint32_t)(a1 - a0) * (uint32_t)H;
-        kda::prefetch_l2(q + off, rows * DK * 2);
-        kda::prefetch_l2(k + off, rows * DK * 2);
-        kda::prefetch_l2(v + off, rows * DV * 2);
-        kda::prefetch_l2(g + off, rows * DK * 4);
-    };
     for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
         int tok0, nrows, slot, h;
         if (!item(it, tok0, nrows, slot, h)) continue;
         uint8_t* blk = ws_blocks + ((size_t)slot * H + h) * WS_BLOCK;
-        if (tid == 32 * 7) prefetch(it + gridDim.x);
 
         // ---------------- a1: loads and per-block cumulative log-decay
         const int p = w >> 2, b = w & 3;          // channel panel, row block
         const int ch = 64 * p + 2 * lane;          // this thread's two channels
         float G0[16], G1[16];
         uint32_t qv[16], kv[16];
-        // Every load is unconditional (rows past the chunk's end read its last row)
-        // so that all of them are in flight together; those rows are zeroed once
-        // the values arrive.
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            const size_t tok = (size_t)tok0 + min(16 * b + rr, nrows - 1);
-            const size_t off = (tok * H + h) * DK + ch;
-            const float2 gg = *reinterpret_cast<const float2*>(g + off);
-            G0[rr] = gg.x;
-            G1[rr] = gg.y;
-            qv[rr] = *reinterpret_cast<const uint32_t*>(q + off);
-            kv[rr] = *reinterpret_cast<const uint32_t*>(k + off);
+        // inputs: one TMA copy per tensor (V straight into its operand slot, both
+        // 64-channel panels) once the previous item's output images have left
+        // shared memory; rows past the end of the tensor read as zero
+        if (tid == 0) {
+            kda::bulk_wait_read_all();
+            kda::mbar_arrive_expect_tx(bar_ld, K1_IN_BYTES);
+            kda::tma_load_3d(sm + K1_SG, &tm_g, 0, h, tok0, bar_ld);
+            kda::tma_load_3d(sm + K1_SQ, &tm_q, 0, h, tok0, bar_ld);
+            kda::tma_load_3d(sm + K1_SK, &tm_k, 0, h, tok0, bar_ld);
+            kda::tma_load_3d(sm + K1_BWU + 16384, &tm_v, 0, h, tok0, bar_ld);
+            kda::tma_load_3d(sm + K1_BWU + 16384 + 8192, &tm_v, 64, h, tok0, bar_ld);
         }
         // beta of row 16 b + (lane % 16): one value per lane
         float bt = beta[((size_t)tok0 + min(16 * b + (lane & 15), nrows - 1)) * H + h];
-        uint4 vx[C * (DV / 8) / 256];              // this thread's share of the V tile
+        if (!kda::mbar_wait(bar_ld, n_done & 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
 #pragma unroll
-        for (int i = 0; i < C * (DV / 8) / 256; ++i) {
-            const int e = tid + 256 * i, t = e >> 4, cc = e & 15;
-            vx[i] = *reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + min(t, nrows - 1)) * H + h) * DV + 8 * cc);
+        for (int rr = 0; rr < 16; ++rr) {
+            const int r = 16 * b + rr;
+            const float2 gg = *reinterpret_cast<const float2*>(sm + K1_SG + r * 512 + ch * 4);
+            G0[rr] = gg.x;
+            G1[rr] = gg.y;
+            qv[rr] = *reinterpret_cast<const uint32_t*>(sm + K1_SQ + r * 256 + ch * 2);
+            kv[rr] = *reinterpret_cast<const uint32_t*>(sm + K1_SK + r * 256 + ch * 2);
         }
-        // the previous item's output images must have left shared memory
-        if (tid == 0) kda::bulk_wait_read_all();
-        __syncthreads();
-        // rows past the chunk's end: zero inputs (log-decay 0, beta 0, q = k = 0)
+        // rows past the chunk's end (another sequence's tokens, or zeros): zero
+        // inputs (log-decay 0, beta 0, q = k = v = 0)
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
             if (16 * b + rr >= nrows) { G0[rr] = 0.f; G1[rr] = 0.f; qv[rr] = 0u; kv[rr] = 0u; }
         }
         if (16 * b + (lane & 15) >= nrows) bt = 0.f;
         else if (PROLOGUE) bt = kda::prologue_beta(bt);
+        for (int e = tid; e < (C - nrows) * (DV / 8); e += 256) {
+            const int t = nrows + (e >> 4), cc = e & 15;
+            *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncthreads();                           // the input tiles are in registers
         float* nrm = reinterpret_cast<float*>(sm + K1_NRM);
         if (PROLOGUE) {
             // fused prologue: gates from their pre-activations; squared norms of
@@ -434,13 +435,6 @@ kda_tc_prep(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* 
                     nrm[128 + p * 64 + 16 * b + rr] = sk;
                 }
             }
-        }
-        // V slice -> right half of the [K_decay | V] operand (MN-major)
-#pragma unroll
-        for (int i = 0; i < C * (DV / 8) / 256; ++i) {
-            const int e = tid + 256 * i, t = e >> 4, cc = e & 15;
-            *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) =
-                t < nrows ? vx[i] : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int rr = 1; rr < 16; ++rr) { G0[rr] += G0[rr - 1]; G1[rr] += G1[rr - 1]; }
@@ -1123,6 +1117,40 @@ size_t state_bytes(int n_seq, int H) { return (size_t)n_seq * H * DK * DV * size
 
 long long slot_bound(int n_seq, int T_total) { return (long long)T_total / C + n_seq; }
 
+// ---- TMA descriptors for the [T, H, 128] input tensors.  cuTensorMapEncodeTiled
+// is a driver entry point, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor [T, H, 128] of `esize`-byte elements at `base`; box = `box_x` channels
+// of one head for 64 tokens, 128-byte swizzled when `swizzle` (box_x * esize = 128).
+cudaError_t make_input_map(CUtensorMap* m, const void* base, int esize, int H, int T, int box_x, bool swizzle) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)128 * esize, (cuuint64_t)H * 128 * esize};
+    const cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)C};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // ---- stream overlap: the prep of a later slice of chunks runs while the
 // state pass works through the previous slice.  Per device: one
 // high-priority stream for the state pass and a pool of events, created on
@@ -1215,15 +1243,20 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     e = cudaFuncSetAttribute(kda_tc_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
     if (e != cudaSuccess) return e;
 
+    CUtensorMap tm_q, tm_k, tm_v, tm_g;
+    if (a.T_total > 0) {
+        if ((e = make_input_map(&tm_q, a.q, 2, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
+        if ((e = make_input_map(&tm_k, a.k, 2, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
+        if ((e = make_input_map(&tm_v, a.v, 2, a.H, a.T_total, 64, true)) != cudaSuccess) return e;
+        if ((e = make_input_map(&tm_g, a.log_alpha, 4, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
+    }
     auto prep = [&](int j0, int jn, cudaStream_t st) {
-        if (jn <= 0 || a.total_chunks <= 0) return cudaSuccess;
+        if (jn <= 0 || a.total_chunks <= 0 || a.T_total <= 0) return cudaSuccess;
         const int gx = use_table ? a.total_chunks : a.n_seq * jn;
         const long long items = (long long)gx * a.H;
         const unsigned grid = (unsigned)std::min<long long>(items, 2LL * n_sm);   // two resident CTAs per SM
-        prep_kernel<<<grid, 256, prep_smem, st>>>(
-            static_cast<const bf16*>(a.q), static_cast<const bf16*>(a.k), static_cast<const bf16*>(a.v),
-            a.log_alpha, a.beta, a.H, use_table, fixed_len, nch_per, chunk_info, seq_info, j0, jn, gx, blocks,
-            a.status);
+        prep_kernel<<<grid, 256, prep_smem, st>>>(tm_q, tm_k, tm_v, tm_g, a.beta, a.H, use_table, fixed_len,
+                                                  nch_per, chunk_info, seq_info, j0, jn, gx, blocks, a.status);
         return cudaGetLastError();
     };
     auto chain = [&](int c0, int c1, const float* s_in, float* s_out, cudaStream_t st) {
