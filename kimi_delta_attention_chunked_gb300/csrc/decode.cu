@@ -162,9 +162,9 @@ kda_decode_multi_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, co
     constexpr int NPASS = (DK + RPP - 1) / RPP;
     __shared__ float s_k[kMaxVerify][DK], s_q[kMaxVerify][DK], s_a[kMaxVerify][DK];
     __shared__ float s_v[kMaxVerify][DV];
-    __shared__ float s_b[kMaxVerify];
-    __shared__ float4 s_x[RPP][LPR];
-    __shared__ float4 s_y[RPP][LPR];
+    __shared__ float s_b[kMaxVerify], s_kq[kMaxVerify];
+    __shared__ float4 s_x[2][RPP][LPR];               // partial reductions, alternating by token
+    __shared__ float4 s_y[2][RPP][LPR];
 
     const int n = blockIdx.x / H, h = blockIdx.x % H;
     const size_t unit = blockIdx.x;                   // n * H + h
@@ -193,8 +193,21 @@ kda_decode_multi_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, co
     }
     for (int t = tid; t < K; t += kThreads) s_b[t] = beta[((size_t)n * K + t) * H + h];
     __syncthreads();
+    // k_t . q_t of every token, one warp per token
+    {
+        const int w = tid >> 5, lane = tid & 31;
+        for (int t = w; t < K; t += kThreads / 32) {
+            float kq = 0.f;
+            for (int i = lane; i < DK; i += 32) kq = fmaf(s_k[t][i], s_q[t][i], kq);
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o2);
+            if (lane == 0) s_kq[t] = kq;
+        }
+    }
+    __syncthreads();
 
     for (int t = 0; t < K; ++t) {
+        const int pb = t & 1;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
 #pragma unroll
         for (int p = 0; p < NPASS; ++p) {
@@ -208,15 +221,16 @@ kda_decode_multi_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, co
                 y.z = fmaf(s[p].z, qi, y.z); y.w = fmaf(s[p].w, qi, y.w);
             }
         }
-        s_x[r0][c4] = x;
-        s_y[r0][c4] = y;
+        s_x[pb][r0][c4] = x;
+        s_y[pb][r0][c4] = y;
+        // one barrier per token: token t + 1 fills the other buffer, and token
+        // t + 2 reuses this one only after every thread passed token t + 1's barrier
         __syncthreads();
-        float4 X = make_float4(0.f, 0.f, 0.f, 0.f), Y = X;
+        float4 X = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int r = 0; r < RPP; ++r) {
-            const float4 a = s_x[r][c4], b = s_y[r][c4];
+            const float4 a = s_x[pb][r][c4];
             X.x += a.x; X.y += a.y; X.z += a.z; X.w += a.w;
-            Y.x += b.x; Y.y += b.y; Y.z += b.z; Y.w += b.w;
         }
         const float bt = s_b[t];
         float4 u;
@@ -232,8 +246,13 @@ kda_decode_multi_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, co
             }
         }
         if (o && r0 == 0) {
-            float kq = 0.f;
-            for (int i = 0; i < DK; ++i) kq = fmaf(s_k[t][i], s_q[t][i], kq);
+            float4 Y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int r = 0; r < RPP; ++r) {
+                const float4 b = s_y[pb][r][c4];
+                Y.x += b.x; Y.y += b.y; Y.z += b.z; Y.w += b.w;
+            }
+            const float kq = s_kq[t];
             TIn* ou = o + (((size_t)n * K + t) * H + h) * DV + 4 * c4;
             kda::io<TIn>::st(ou + 0, fmaf(kq, u.x, Y.x));
             kda::io<TIn>::st(ou + 1, fmaf(kq, u.y, Y.y));
@@ -247,7 +266,6 @@ kda_decode_multi_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, co
                 if (i < DK) __stcs(reinterpret_cast<float4*>(Su + (size_t)i * DV) + c4, s[p]);
             }
         }
-        __syncthreads();                               // s_x / s_y are reused by the next token
     }
 }
 
