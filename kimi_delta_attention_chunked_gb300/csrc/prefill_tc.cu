@@ -193,8 +193,8 @@ __device__ __forceinline__ void mm16(float (&acc)[8], const float* A, int lda, c
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.f;
     }
-#pragma unroll
-    for (int kk = 0; kk < 16; kk += 8) {
+#pragma unroll 1
+    for (int kk = 0; kk < 16; kk += 8) {      // rolled: this code is inlined at eight call sites
         uint32_t ab[4], as[4];
         split_tf32(A[g * lda + kk + t], ab[0], as[0]);
         split_tf32(A[(g + 8) * lda + kk + t], ab[1], as[1]);
@@ -270,40 +270,37 @@ kda_tc_schedule(const int32_t* __restrict__ cu, int n_seq, int T_total, int slot
 }
 
 // ============================================================== prep (a1-a3)
-template <int B>
-__device__ __forceinline__ void gram_epilogue(uint32_t tmem, int lane, uint8_t* mh, uint8_t* ml, float* LS) {
-    constexpr int N = 16 * (B + 1);
-    constexpr int OFF = 8 * B * (B + 1);
-    float v[N];
-#pragma unroll
-    for (int c = 0; c < N; c += 16) kda::tmem_ld16(tmem + ((uint32_t)(32 * B) << 16) + OFF + c, v + c);
-    kda::tmem_wait_ld();
-    if (lane < 16) {                          // M_qk row (diagonal included) -> high / low bf16 operand parts
-        const int r = 16 * B + lane;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            float f[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int t = 8 * cc + u;
-                f[u] = (t < N && t <= r) ? v[t < N ? t : 0] : 0.f;
-            }
-            uint4 hi, lo;
-            split_pack8(f, hi, lo);
-            *reinterpret_cast<uint4*>(mh + kda::sw128(r, 8 * cc, 64)) = hi;
-            *reinterpret_cast<uint4*>(ml + kda::sw128(r, 8 * cc, 64)) = lo;
+// One warp per row block B (0..3): TMEM lanes 32 B .. 32 B + 31 hold the
+// block's q~ rows (lanes 0..15) and k^ rows (lanes 16..31) against the first
+// 16 (B + 1) tokens, at columns 8 B (B + 1) ...  Writes the M_qk rows
+// (diagonal included) as high / low bf16 operand parts and the L rows (beta
+// folded in, strict) as fp32.  One rolled copy for all four blocks.
+__device__ __forceinline__ void gram_epilogue(uint32_t tmem, int B, int lane, uint8_t* mh, uint8_t* ml, float* LS) {
+    const int N = 16 * (B + 1), OFF = 8 * B * (B + 1);
+    const bool is_m = lane < 16;
+    const int r = 16 * B + (lane & 15);
+    const int lim = is_m ? r + 1 : r;             // columns t < lim are kept (lim <= N)
+#pragma unroll 1
+    for (int c = 0; c < 64; c += 16) {
+        float v[16];
+        if (c < N) {                              // warp-uniform
+            kda::tmem_ld16(tmem + ((uint32_t)(32 * B) << 16) + OFF + c, v);
+            kda::tmem_wait_ld();
         }
-    } else {                                  // L row (beta folded in), strict
-        const int r = 16 * B + lane - 16;
-        float* row = LS + r * LDS_;
 #pragma unroll
-        for (int t4 = 0; t4 < 64; t4 += 4) {
-            float4 x;
-            x.x = (t4 + 0 < N && t4 + 0 < r) ? v[t4 + 0 < N ? t4 + 0 : 0] : 0.f;
-            x.y = (t4 + 1 < N && t4 + 1 < r) ? v[t4 + 1 < N ? t4 + 1 : 0] : 0.f;
-            x.z = (t4 + 2 < N && t4 + 2 < r) ? v[t4 + 2 < N ? t4 + 2 : 0] : 0.f;
-            x.w = (t4 + 3 < N && t4 + 3 < r) ? v[t4 + 3 < N ? t4 + 3 : 0] : 0.f;
-            *reinterpret_cast<float4*>(row + t4) = x;
+        for (int u = 0; u < 16; ++u) v[u] = (c + u < lim) ? v[u] : 0.f;
+        if (is_m) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                uint4 hi, lo;
+                split_pack8(v + 8 * j, hi, lo);
+                *reinterpret_cast<uint4*>(mh + kda::sw128(r, c + 8 * j, 64)) = hi;
+                *reinterpret_cast<uint4*>(ml + kda::sw128(r, c + 8 * j, 64)) = lo;
+            }
+        } else {
+            float* row = LS + r * LDS_ + c;
+#pragma unroll
+            for (int u = 0; u < 16; u += 4) *reinterpret_cast<float4*>(row + u) = make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]);
         }
     }
 }
@@ -530,10 +527,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         float* LS = reinterpret_cast<float*>(sm + K1_LS);
         float* IS = reinterpret_cast<float*>(sm + K1_IS);
         float* XS = reinterpret_cast<float*>(sm + K1_XS);
-        if (w == 0) gram_epilogue<0>(tmem, lane, sm + K1_MH, sm + K1_ML, LS);
-        else if (w == 1) gram_epilogue<1>(tmem, lane, sm + K1_MH, sm + K1_ML, LS);
-        else if (w == 2) gram_epilogue<2>(tmem, lane, sm + K1_MH, sm + K1_ML, LS);
-        else if (w == 3) gram_epilogue<3>(tmem, lane, sm + K1_MH, sm + K1_ML, LS);
+        if (w < 4) gram_epilogue(tmem, w, lane, sm + K1_MH, sm + K1_ML, LS);
         kda::tc_fence_before();
         __syncthreads();
 
@@ -698,7 +692,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int quad = w & 3, r = 32 * (quad & 1) + lane;
         const uint32_t t_row = tmem + ((uint32_t)(32 * quad) << 16) + (w >= 4 ? 128u : 0u);
         if (w == 0 || w == 1) {                    // W rows -> rows 64..127 of [Q'; W]
-#pragma unroll
+#pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
                 float x[32];
                 kda::tmem_ld32(t_row + 32 * cb, x);
@@ -709,7 +703,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
         } else if (w == 2 || w == 3) {             // Q' = Q_decay - M_qk W -> rows 0..63 of [Q'; W]
             if (!kda::mbar_wait(bar_q, n_done & 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
-#pragma unroll
+#pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
                 float x[32];
                 kda::tmem_ld32(t_row + 32 * cb, x);
@@ -730,7 +724,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
         } else {                                   // U0 (warps 4, 5) or O0 (warps 6, 7) rows, fp32, per d_v slice
             const uint32_t part = w < 6 ? 0u : TILE_F32;
-#pragma unroll
+#pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
                 float x[32];
                 kda::tmem_ld32(t_row + 32 * cb, x);
