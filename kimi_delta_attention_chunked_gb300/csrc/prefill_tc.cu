@@ -460,14 +460,12 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (m == b) { myG0 = Gs0[m]; myG1 = Gs1[m]; }
         const float ap0 = __expf(myG0), ap1 = __expf(myG1);              // a at the block start
         const float R0 = __expf(acc0 - myG0), R1 = __expf(acc1 - myG1);  // a_last / a(block start)
-        float f0[4], f1[4];                                              // a(p_m) / a(p_b), m > b
-#pragma unroll
-        for (int m = 0; m < 4; ++m) { f0[m] = __expf(Gs0[m] - myG0); f1[m] = __expf(Gs1[m] - myG1); }
         if (b == 0) {
             *reinterpret_cast<float2*>(blk + WS_AL + 4 * ch) = make_float2(__expf(acc0), __expf(acc1));
         }
 
         // ---------------- a1: operands
+        float kts[32];                             // column factors k exp(G_pb - G_t) of the 16 rows
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
             const int r = 16 * b + rr;
@@ -486,14 +484,10 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const float kt0 = kf.x * c0, kt1 = kf.y * c1;            // k (column factor, own block)
             st_shared_u32(sm + K1_AG + kda::sw128(32 * b + rr, ch, 128), kda::pack_bf16x2(qt0, qt1));
             st_shared_u32(sm + K1_AG + kda::sw128(32 * b + 16 + rr, ch, 128), kda::pack_bf16x2(kh0, kh1));
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                if (m >= b) {
-                    const float s0 = (m == b) ? 1.f : f0[m], s1 = (m == b) ? 1.f : f1[m];
-                    st_shared_u32(sm + K1_BG + kda::sw128(8 * m * (m + 1) + r, ch, 160),
-                                  kda::pack_bf16x2(kt0 * s0, kt1 * s1));
-                }
-            }
+            // own block's column operand (block b of tile b); the later tiles below
+            st_shared_u32(sm + K1_BG + kda::sw128(8 * b * (b + 1) + r, ch, 160), kda::pack_bf16x2(kt0, kt1));
+            kts[2 * rr] = kt0;
+            kts[2 * rr + 1] = kt1;
             // Q_decay -> rows 0..63 of the [Q_decay; W] image
             *reinterpret_cast<uint32_t*>(blk + WS_A1 + kda::sw128(r, ch, 128)) = kda::pack_bf16x2(qt0 * ap0, qt1 * ap1);
             // K_decay -> left half of the [K_decay | V] operand
@@ -501,6 +495,18 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                           kda::pack_bf16x2(kf.x * e0 * ap0, kf.y * e1 * ap1));
             // K_restore -> K_restore^T image (MN-major: row = token, contiguous = channel)
             *reinterpret_cast<uint32_t*>(blk + WS_KR + kda::sw128(r, ch, 64)) = kda::pack_bf16x2(kt0 * R0, kt1 * R1);
+        }
+        // tiles m > b hold this block's column factors times a(p_m) / a(p_b) <= 1
+        // (a rolled loop keeps this replicated part of the code small)
+#pragma unroll 1
+        for (int m = b + 1; m < 4; ++m) {
+            const float gs0 = m == 1 ? Gs0[1] : (m == 2 ? Gs0[2] : Gs0[3]);
+            const float gs1 = m == 1 ? Gs1[1] : (m == 2 ? Gs1[2] : Gs1[3]);
+            const float s0 = __expf(gs0 - myG0), s1 = __expf(gs1 - myG1);
+            uint8_t* tile = sm + K1_BG + 1024 * m * (m + 1);        // row 8 m (m + 1), an 8-row atom boundary
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr)
+                st_shared_u32(tile + kda::sw128(16 * b + rr, ch, 160), kda::pack_bf16x2(kts[2 * rr] * s0, kts[2 * rr + 1] * s1));
         }
         kda::fence_proxy_async_all();              // shared operands and the Q_decay rows read back later
         kda::tc_fence_before();
