@@ -638,14 +638,13 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         // (the operand overlays the M_qk parts, which the X product has finished reading)
         if ((w & 2) == 0) {                        // warps 0, 1, 4, 5: X rows from TMEM lanes 0..63
             const int r = 32 * (w & 1) + lane, c0 = 32 * (w >> 2);
-            float x[32];
-            kda::tmem_ld32(tmem + ((uint32_t)(32 * (w & 1)) << 16) + K1_TX + c0, x);
-            kda::tmem_wait_ld();
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 float f[8];
+                kda::tmem_ld8(tmem + ((uint32_t)(32 * (w & 1)) << 16) + K1_TX + c0 + 8 * cc, f);
+                kda::tmem_wait_ld();
 #pragma unroll
-                for (int u = 0; u < 8; ++u) f[u] = x[8 * cc + u] * beta_s[c0 + 8 * cc + u];
+                for (int u = 0; u < 8; ++u) f[u] *= beta_s[c0 + 8 * cc + u];
                 uint4 hi, lo;
                 split_pack8(f, hi, lo);
                 *reinterpret_cast<uint4*>(sm + K1_AI + kda::sw128(64 + r, c0 + 8 * cc, 64)) = hi;
@@ -654,7 +653,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         } else {                                   // warps 2, 3, 6, 7: INV rows from shared memory
             const int li = 32 * (((w >> 2) << 1) | (w & 1)) + lane;
             const int r = li >> 1, c0 = 32 * (li & 1);
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 float f[8];
 #pragma unroll

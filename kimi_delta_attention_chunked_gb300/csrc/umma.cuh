@@ -124,7 +124,13 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// 32 lanes x 32 bit, 16 or 32 consecutive columns per thread (warp-collective).
+// 32 lanes x 32 bit, 8, 16 or 32 consecutive columns per thread (warp-collective).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* r) {
+    uint32_t* u = reinterpret_cast<uint32_t*>(r);
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
+                 : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* r) {
     uint32_t* u = reinterpret_cast<uint32_t*>(r);
     asm volatile(
