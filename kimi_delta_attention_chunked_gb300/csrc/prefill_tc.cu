@@ -464,49 +464,53 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             *reinterpret_cast<float2*>(blk + WS_AL + 4 * ch) = make_float2(__expf(acc0), __expf(acc1));
         }
 
-        // ---------------- a1: operands
-        float kts[32];                             // column factors k exp(G_pb - G_t) of the 16 rows
+        // ---------------- a1: operands, in two halves of 8 rows (fewer live registers)
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            const int r = 16 * b + rr;
-            const float e0 = __expf(G0[rr] - G0[0]), e1 = __expf(G1[rr] - G1[0]);   // <= 1
-            const float c0 = __fdividef(1.f, e0), c1 = __fdividef(1.f, e1);         // >= 1, <= e^75
-            float2 qf = kda::unpack_bf16x2(qv[rr]);
-            float2 kf = kda::unpack_bf16x2(kv[rr]);
-            if (PROLOGUE) {                        // unit-length q and k rows
-                const float iq = rsqrtf(nrm[r] + nrm[64 + r] + kda::kNormEps);
-                const float ik = rsqrtf(nrm[128 + r] + nrm[192 + r] + kda::kNormEps);
-                qf.x *= iq; qf.y *= iq; kf.x *= ik; kf.y *= ik;
+        for (int hf = 0; hf < 2; ++hf) {
+            float kts[16];                             // column factors k exp(G_pb - G_t) of the 8 rows
+#pragma unroll
+            for (int rr = 8 * hf; rr < 8 * hf + 8; ++rr) {
+                const int r = 16 * b + rr;
+                const float e0 = __expf(G0[rr] - G0[0]), e1 = __expf(G1[rr] - G1[0]);   // <= 1
+                const float c0 = __fdividef(1.f, e0), c1 = __fdividef(1.f, e1);         // >= 1, <= e^75
+                float2 qf = kda::unpack_bf16x2(qv[rr]);
+                float2 kf = kda::unpack_bf16x2(kv[rr]);
+                if (PROLOGUE) {                        // unit-length q and k rows
+                    const float iq = rsqrtf(nrm[r] + nrm[64 + r] + kda::kNormEps);
+                    const float ik = rsqrtf(nrm[128 + r] + nrm[192 + r] + kda::kNormEps);
+                    qf.x *= iq; qf.y *= iq; kf.x *= ik; kf.y *= ik;
+                }
+                const float be = beta_s[r];
+                const float qt0 = qf.x * e0, qt1 = qf.y * e1;            // q~ (row factor)
+                const float kh0 = be * kf.x * e0, kh1 = be * kf.y * e1;  // k^ = beta k (row factor)
+                const float kt0 = kf.x * c0, kt1 = kf.y * c1;            // k (column factor, own block)
+                st_shared_u32(sm + K1_AG + kda::sw128(32 * b + rr, ch, 128), kda::pack_bf16x2(qt0, qt1));
+                st_shared_u32(sm + K1_AG + kda::sw128(32 * b + 16 + rr, ch, 128), kda::pack_bf16x2(kh0, kh1));
+                // own block's column operand (block b of tile b); the later tiles below
+                st_shared_u32(sm + K1_BG + kda::sw128(8 * b * (b + 1) + r, ch, 160), kda::pack_bf16x2(kt0, kt1));
+                kts[2 * (rr - 8 * hf)] = kt0;
+                kts[2 * (rr - 8 * hf) + 1] = kt1;
+                // Q_decay -> rows 0..63 of the [Q_decay; W] image
+                *reinterpret_cast<uint32_t*>(blk + WS_A1 + kda::sw128(r, ch, 128)) = kda::pack_bf16x2(qt0 * ap0, qt1 * ap1);
+                // K_decay -> left half of the [K_decay | V] operand
+                st_shared_u32(sm + K1_BWU + kda::sw128(r, ch, 64),
+                              kda::pack_bf16x2(kf.x * e0 * ap0, kf.y * e1 * ap1));
+                // K_restore -> K_restore^T image (MN-major: row = token, contiguous = channel)
+                *reinterpret_cast<uint32_t*>(blk + WS_KR + kda::sw128(r, ch, 64)) = kda::pack_bf16x2(kt0 * R0, kt1 * R1);
             }
-            const float be = beta_s[r];
-            const float qt0 = qf.x * e0, qt1 = qf.y * e1;            // q~ (row factor)
-            const float kh0 = be * kf.x * e0, kh1 = be * kf.y * e1;  // k^ = beta k (row factor)
-            const float kt0 = kf.x * c0, kt1 = kf.y * c1;            // k (column factor, own block)
-            st_shared_u32(sm + K1_AG + kda::sw128(32 * b + rr, ch, 128), kda::pack_bf16x2(qt0, qt1));
-            st_shared_u32(sm + K1_AG + kda::sw128(32 * b + 16 + rr, ch, 128), kda::pack_bf16x2(kh0, kh1));
-            // own block's column operand (block b of tile b); the later tiles below
-            st_shared_u32(sm + K1_BG + kda::sw128(8 * b * (b + 1) + r, ch, 160), kda::pack_bf16x2(kt0, kt1));
-            kts[2 * rr] = kt0;
-            kts[2 * rr + 1] = kt1;
-            // Q_decay -> rows 0..63 of the [Q_decay; W] image
-            *reinterpret_cast<uint32_t*>(blk + WS_A1 + kda::sw128(r, ch, 128)) = kda::pack_bf16x2(qt0 * ap0, qt1 * ap1);
-            // K_decay -> left half of the [K_decay | V] operand
-            st_shared_u32(sm + K1_BWU + kda::sw128(r, ch, 64),
-                          kda::pack_bf16x2(kf.x * e0 * ap0, kf.y * e1 * ap1));
-            // K_restore -> K_restore^T image (MN-major: row = token, contiguous = channel)
-            *reinterpret_cast<uint32_t*>(blk + WS_KR + kda::sw128(r, ch, 64)) = kda::pack_bf16x2(kt0 * R0, kt1 * R1);
-        }
-        // tiles m > b hold this block's column factors times a(p_m) / a(p_b) <= 1
-        // (a rolled loop keeps this replicated part of the code small)
+            // tiles m > b hold this block's column factors times a(p_m) / a(p_b) <= 1
+            // (a rolled loop keeps this replicated part of the code small)
 #pragma unroll 1
-        for (int m = b + 1; m < 4; ++m) {
-            const float gs0 = m == 1 ? Gs0[1] : (m == 2 ? Gs0[2] : Gs0[3]);
-            const float gs1 = m == 1 ? Gs1[1] : (m == 2 ? Gs1[2] : Gs1[3]);
-            const float s0 = __expf(gs0 - myG0), s1 = __expf(gs1 - myG1);
-            uint8_t* tile = sm + K1_BG + 1024 * m * (m + 1);        // row 8 m (m + 1), an 8-row atom boundary
+            for (int m = b + 1; m < 4; ++m) {
+                const float gs0 = m == 1 ? Gs0[1] : (m == 2 ? Gs0[2] : Gs0[3]);
+                const float gs1 = m == 1 ? Gs1[1] : (m == 2 ? Gs1[2] : Gs1[3]);
+                const float s0 = __expf(gs0 - myG0), s1 = __expf(gs1 - myG1);
+                uint8_t* tile = sm + K1_BG + 1024 * m * (m + 1);        // row 8 m (m + 1), an 8-row atom boundary
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr)
-                st_shared_u32(tile + kda::sw128(16 * b + rr, ch, 160), kda::pack_bf16x2(kts[2 * rr] * s0, kts[2 * rr + 1] * s1));
+                for (int rr = 0; rr < 8; ++rr)
+                    st_shared_u32(tile + kda::sw128(16 * b + 8 * hf + rr, ch, 160),
+                                  kda::pack_bf16x2(kts[2 * rr] * s0, kts[2 * rr + 1] * s1));
+            }
         }
         kda::fence_proxy_async_all();              // shared operands and the Q_decay rows read back later
         kda::tc_fence_before();
