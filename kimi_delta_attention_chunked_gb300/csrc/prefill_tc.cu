@@ -811,7 +811,14 @@ __global__ void __launch_bounds__(K2_THREADS, 1)
 kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, int nch_per_seq,
              int c_begin, int c_end, const uint8_t* __restrict__ ws_blocks, const float* __restrict__ S0, int H,
              bf16* __restrict__ O, float* __restrict__ S_final, int ckpt_every, float* __restrict__ ckpt,
-             int ckpt_cap, int* status) {
+             int ckpt_cap, int* status, int seg_pass1, float* __restrict__ S_final_map) {
+    // seg_pass1 (segment scan, first pass): blockIdx.z = 0 runs each segment
+    // from a zero state (its affine offset, into S_final), blockIdx.z = 1 from
+    // the identity with U0 taken as zero (its linear map, into S_final_map);
+    // neither writes O.
+    const bool run_map = seg_pass1 && blockIdx.z == 1;
+    const bool write_o = !seg_pass1;
+    if (run_map) S_final = S_final_map;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     const int tile = blockIdx.x % NTILES, n = blockIdx.x / NTILES, h = blockIdx.y;
@@ -988,7 +995,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int rr = 8 * wo + i;
-                if (rr < valid) {
+                if (write_o && rr < valid) {
                     const uint32_t x = *reinterpret_cast<const uint32_t*>(
                         o0b + rr * 128 + (((lane >> 2) ^ (rr & 7)) << 4) + 4 * (lane & 3));
                     *reinterpret_cast<uint32_t*>(O + ((size_t)(bos + (cb + co) * C + rr) * H + h) * DV + tile * NT +
@@ -1002,7 +1009,10 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         {
             // initial state slice -> TMEM (X = 0)
             float s[K2_CW];
-            if (S0) {
+            if (run_map) {
+#pragma unroll
+                for (int u = 0; u < K2_CW; ++u) s[u] = (row == tile * NT + col0 + u) ? 1.f : 0.f;
+            } else if (S0 && !seg_pass1) {
                 const float4* src = reinterpret_cast<const float4*>(S0 + (((size_t)n * H + h) * DK + row) * DV +
                                                                     tile * NT + col0);
 #pragma unroll
@@ -1064,7 +1074,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
 #pragma unroll
                 for (int cc = 0; cc < K2_CW / 8; ++cc) {
                     const int j = (col0 + 8 * cc) / 4;              // 16-byte chunk of the row
-                    const float4 x0 = u0[j ^ (r & 7)], x1 = u0[(j + 1) ^ (r & 7)];
+                    float4 x0 = u0[j ^ (r & 7)], x1 = u0[(j + 1) ^ (r & 7)];
+                    if (run_map) { x0 = make_float4(0.f, 0.f, 0.f, 0.f); x1 = x0; }
                     float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
                     for (int u = 0; u < 8; ++u) f[u] -= ph[8 * cc + u];
@@ -1111,6 +1122,127 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     if (w == 0) kda::tmem_dealloc(tmem, K2_TMEM_COLS);
 }
 
+// ============================================================== segment scan
+// For few (sequence, head) chains and long sequences the state pass leaves most
+// SMs idle.  The chunk-level map S -> A_c S + B_c (A_c = Diag(a_last) -
+// K_restore^T W, B_c = K_restore^T U0) composes over a segment of chunks into
+// S -> A_p S + B_p, so each sequence is cut into segments of at most L chunks:
+// pass 1 runs the state pass on every segment twice in one launch (from zero:
+// B_p; from the identity with U0 taken as zero: A_p), a scan forms each
+// segment's true starting state, and pass 3 runs the state pass again from it,
+// writing O.  Each pass is short; the scan is sequential only over segments.
+
+// Segment tables: seg_info[s] = (token start, length, first chunk slot, chunks)
+// for the segments of every sequence in order; seq_seg[n] = (first segment,
+// segments).  Entries up to s_max that no sequence uses get zero chunks.
+__global__ void __launch_bounds__(1024)
+kda_tc_segments(const int4* __restrict__ seq_info, int use_table, int fixed_len, int nch_per_seq, int n_seq,
+                int L, int s_max, int4* __restrict__ seg_info, int2* __restrict__ seq_seg, int* status) {
+    __shared__ int part[1024];
+    __shared__ int total;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    auto info = [&](int n) {
+        return use_table ? seq_info[n] : make_int4(n * fixed_len, fixed_len, n * nch_per_seq, nch_per_seq);
+    };
+    const int per = (n_seq + nt - 1) / nt;
+    const int s0 = min(tid * per, n_seq), s1 = min(s0 + per, n_seq);
+    int cnt = 0;
+    for (int n = s0; n < s1; ++n) cnt += (info(n).w + L - 1) / L;
+    part[tid] = cnt;
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int i = 0; i < nt; ++i) { const int c = part[i]; part[i] = acc; acc += c; }
+        total = min(acc, s_max);
+        if (acc > s_max) kda::record_status(status, KDA_ERR_INVALID_ARG);
+    }
+    __syncthreads();
+    int sidx = part[tid];
+    for (int n = s0; n < s1; ++n) {
+        const int4 si = info(n);
+        const int nseg = min((si.w + L - 1) / L, max(0, s_max - sidx));
+        seq_seg[n] = make_int2(sidx, nseg);
+        for (int j = 0; j < nseg; ++j) {
+            const int c0 = j * L;
+            seg_info[sidx + j] = make_int4(si.x + c0 * C, min(si.y - c0 * C, L * C), si.z + c0, min(L, si.w - c0));
+        }
+        sidx += nseg;
+    }
+    for (int e = total + tid; e < s_max; e += nt) seg_info[e] = make_int4(0, 0, 0, 0);
+}
+
+// Scan over the segments of one sequence, for one head and 32 state columns:
+// S_start[first] = S0, S_start[p + 1] = A_p S_start[p] + B_p, S_final = the
+// state after the last segment.  fp32 on CUDA cores (A_p in shared memory).
+constexpr int SC_COLS = 32;
+constexpr int SC_LDA = DK + 1;                   // padded row of A: conflict-free column reads
+constexpr uint32_t SC_SMEM = (DK * SC_LDA + DK * SC_COLS) * 4;
+
+__global__ void __launch_bounds__(256)
+kda_tc_seg_scan(const int2* __restrict__ seq_seg, const float* __restrict__ A, const float* __restrict__ B,
+                const float* __restrict__ S0, float* __restrict__ S_start, float* __restrict__ S_final, int H) {
+    extern __shared__ float sc_smem[];
+    float* As = sc_smem;                         // [DK][SC_LDA]
+    float* Ss = sc_smem + DK * SC_LDA;           // [DK][SC_COLS]
+    const int n = blockIdx.x, h = blockIdx.y, c0 = SC_COLS * blockIdx.z;
+    const int tid = threadIdx.x, i = tid >> 1, j0 = 16 * (tid & 1);   // this thread's row and 16 columns
+    auto mat = [&](const float* base, int idx) { return base + ((size_t)idx * H + h) * DK * DV; };
+    auto matw = [&](float* base, int idx) { return base + ((size_t)idx * H + h) * DK * DV; };
+    {
+        float4* srow = reinterpret_cast<float4*>(Ss + i * SC_COLS + j0);
+        const float4* src = S0 ? reinterpret_cast<const float4*>(mat(S0, n) + (size_t)i * DV + c0 + j0) : nullptr;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) srow[u] = src ? src[u] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    const int2 ss = seq_seg[n];
+    for (int p = 0; p < ss.y; ++p) {
+        const int sg = ss.x + p;
+        // this segment's starting state; then its map A_p into shared memory
+        const float4* srow = reinterpret_cast<const float4*>(Ss + i * SC_COLS + j0);
+        float4* dst = reinterpret_cast<float4*>(matw(S_start, sg) + (size_t)i * DV + c0 + j0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = srow[u];
+        const float4* a4 = reinterpret_cast<const float4*>(mat(A, sg));
+        for (int e = tid; e < DK * DK / 4; e += 256) {
+            const float4 x = a4[e];
+            const int r = (4 * e) / DK, k = (4 * e) % DK;
+            As[r * SC_LDA + k] = x.x; As[r * SC_LDA + k + 1] = x.y; As[r * SC_LDA + k + 2] = x.z;
+            As[r * SC_LDA + k + 3] = x.w;
+        }
+        float acc[16];
+        const float4* b4 = reinterpret_cast<const float4*>(mat(B, sg) + (size_t)i * DV + c0 + j0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float4 x = b4[u];
+            acc[4 * u] = x.x; acc[4 * u + 1] = x.y; acc[4 * u + 2] = x.z; acc[4 * u + 3] = x.w;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int k = 0; k < DK; ++k) {
+            const float a = As[i * SC_LDA + k];
+            const float4* sk = reinterpret_cast<const float4*>(Ss + k * SC_COLS + j0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 x = sk[u];
+                acc[4 * u] = fmaf(a, x.x, acc[4 * u]); acc[4 * u + 1] = fmaf(a, x.y, acc[4 * u + 1]);
+                acc[4 * u + 2] = fmaf(a, x.z, acc[4 * u + 2]); acc[4 * u + 3] = fmaf(a, x.w, acc[4 * u + 3]);
+            }
+        }
+        __syncthreads();
+        float4* sw = reinterpret_cast<float4*>(Ss + i * SC_COLS + j0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sw[u] = make_float4(acc[4 * u], acc[4 * u + 1], acc[4 * u + 2], acc[4 * u + 3]);
+        __syncthreads();
+    }
+    if (S_final) {
+        const float4* srow = reinterpret_cast<const float4*>(Ss + i * SC_COLS + j0);
+        float4* dst = reinterpret_cast<float4*>(matw(S_final, n) + (size_t)i * DV + c0 + j0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = srow[u];
+    }
+}
+
 size_t header_bytes(int n_seq, long long slots) {
     const size_t raw = 16u * (size_t)slots + 16u * (size_t)n_seq;
     return (raw + 1023) & ~size_t(1023);
@@ -1119,6 +1251,31 @@ size_t header_bytes(int n_seq, long long slots) {
 size_t state_bytes(int n_seq, int H) { return (size_t)n_seq * H * DK * DV * sizeof(float); }
 
 long long slot_bound(int n_seq, int T_total) { return (long long)T_total / C + n_seq; }
+
+// Segment-scan plan, a function of the problem's shape only (so that the
+// workspace size is too): possible when one state pass has at most 32 CTAs;
+// the segments are sized so that the first pass (two runs per segment) has at
+// most 128 CTAs, and are at least 16 chunks long.
+struct SegPlan {
+    bool possible = false;
+    int s_target = 0;                            // segments aimed at
+    int s_max = 0;                               // table / buffer capacity
+};
+SegPlan seg_plan(int n_seq, int H) {
+    SegPlan p;
+    if ((long long)NTILES * n_seq * H > 32) return p;
+    p.possible = true;
+    p.s_target = std::max(n_seq, 128 / (2 * NTILES * H));
+    p.s_max = p.s_target + n_seq;
+    return p;
+}
+constexpr int kMinSegChunks = 16;
+size_t seg_table_bytes(const SegPlan& p, int n_seq) {
+    return p.possible ? ((16u * (size_t)p.s_max + 8u * (size_t)n_seq + 1023) & ~size_t(1023)) : 0;
+}
+size_t seg_state_bytes(const SegPlan& p, int H) {
+    return p.possible ? 3u * (size_t)p.s_max * H * DK * DV * sizeof(float) : 0;
+}
 
 // ---- TMA descriptors for the [T, H, 128] input tensors.  cuTensorMapEncodeTiled
 // is a driver entry point, looked up once through the runtime.
@@ -1201,7 +1358,9 @@ bool tc_supported(int dk, int dv, int chunk, kda_dtype dt) {
 size_t tc_workspace_bytes(int n_seq, int T_total, int H, int chunk) {
     (void)chunk;
     const long long ub = slot_bound(n_seq, T_total);
-    return header_bytes(n_seq, ub) + state_bytes(n_seq, H) + (size_t)ub * H * WS_BLOCK;
+    const SegPlan sp = seg_plan(n_seq, H);
+    return header_bytes(n_seq, ub) + state_bytes(n_seq, H) + (size_t)ub * H * WS_BLOCK + seg_table_bytes(sp, n_seq) +
+           seg_state_bytes(sp, H);
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a) {
@@ -1228,7 +1387,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
                                                    cudaSuccess)
         return cudaGetLastError();
     const long long chain_ctas = (long long)NTILES * a.n_seq * a.H;
-    const bool overlap = chain_ctas * 4 <= n_sm && !(use_table && a.max_chunks <= 0);
+    // segment scan: few chains, long sequences, no checkpoints
+    const SegPlan sp = seg_plan(a.n_seq, a.H);
+    const int seg_L = sp.possible ? std::max(kMinSegChunks, (a.total_chunks + sp.s_target - 1) / std::max(1, sp.s_target))
+                                  : 0;
+    const bool use_seg = sp.possible && a.ckpt_every == 0 && a.total_chunks > 0 && seg_L < max_chunks;
+    uint8_t* seg_base = blocks + (size_t)ub * a.H * WS_BLOCK;
+    int4* seg_info = reinterpret_cast<int4*>(seg_base);
+    int2* seq_seg = reinterpret_cast<int2*>(seg_base + 16u * (size_t)sp.s_max);
+    float* seg_B = reinterpret_cast<float*>(seg_base + seg_table_bytes(sp, a.n_seq));
+    float* seg_A = seg_B + (size_t)sp.s_max * a.H * DK * DV;
+    float* seg_S = seg_A + (size_t)sp.s_max * a.H * DK * DV;
+    const bool overlap = !use_seg && chain_ctas * 4 <= n_sm && !(use_table && a.max_chunks <= 0);
     const int n_slices = overlap ? std::max(1, std::min(kMaxSlices, max_chunks / 16)) : 1;
     const int slice = n_slices > 1 ? (max_chunks + n_slices - 1) / n_slices : max_chunks;
 
@@ -1244,6 +1414,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kda_tc_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kda_tc_seg_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM);
     if (e != cudaSuccess) return e;
 
     CUtensorMap tm_q, tm_k, tm_v, tm_g;
@@ -1265,9 +1437,33 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     auto chain = [&](int c0, int c1, const float* s_in, float* s_out, cudaStream_t st) {
         kda_tc_chain<<<dim3(NTILES * a.n_seq, a.H), K2_THREADS, chain_smem, st>>>(
             seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
-            a.ckpt_every, a.ckpt, a.ckpt_cap, a.status);
+            a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr);
         return cudaGetLastError();
     };
+
+    if (use_seg) {
+        if ((e = prep(0, max_chunks, a.stream)) != cudaSuccess) return e;
+        trace_mark(a.stream);
+        kda_tc_segments<<<1, 1024, 0, a.stream>>>(seq_info, use_table, fixed_len, nch_per, a.n_seq, seg_L, sp.s_max,
+                                                  seg_info, seq_seg, a.status);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // pass 1: every segment from zero (-> seg_B) and as a map from the identity (-> seg_A)
+        kda_tc_chain<<<dim3(NTILES * sp.s_max, a.H, 2), K2_THREADS, chain_smem, a.stream>>>(
+            seg_info, 1, 0, 0, 0, INT32_MAX, blocks, nullptr, a.H, static_cast<bf16*>(a.O), seg_B, 0, nullptr, 0,
+            a.status, 1, seg_A);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // pass 2: starting state of every segment, and the final states
+        kda_tc_seg_scan<<<dim3(a.n_seq, a.H, DV / SC_COLS), 256, SC_SMEM, a.stream>>>(seq_seg, seg_A, seg_B, a.S0,
+                                                                                       seg_S, a.S_final, a.H);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // pass 3: every segment from its starting state, writing O
+        kda_tc_chain<<<dim3(NTILES * sp.s_max, a.H), K2_THREADS, chain_smem, a.stream>>>(
+            seg_info, 1, 0, 0, 0, INT32_MAX, blocks, seg_S, a.H, static_cast<bf16*>(a.O), nullptr, 0, nullptr, 0,
+            a.status, 0, nullptr);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        trace_mark(a.stream);
+        return cudaSuccess;
+    }
 
     if (n_slices == 1) {
         if ((e = prep(0, max_chunks, a.stream)) != cudaSuccess) return e;

@@ -129,13 +129,42 @@ def test_tc_split_prefill_equals_one_prefill():
 
 
 def test_tc_overlapped_slices_few_heads():
-    """Few chains and many chunks: the prep of later chunk slices overlaps the
-    state pass of earlier ones (two streams); the state crosses slice borders."""
+    """Few chains and many chunks (17 heads: 34 state-pass CTAs, too many for the
+    segment scan): the prep of later chunk slices overlaps the state pass of
+    earlier ones (two streams); the state crosses slice borders."""
+    dev = need_gpu()
+    w = inputs.Workload("tc", "prefill", H=17, dk=128, dv=128, dtype=torch.bfloat16, chunk=64, s0_std=0.02)
+    for lengths in ([64 * 64], [64 * 40 + 17]):
+        _, _, _, eo, es = run_case(w, dev, lengths=lengths, seed=15, heads=(15, 17))
+        assert eo <= 5e-3 and es <= 5e-3, (lengths, eo, es)
+
+
+@pytest.mark.parametrize("host_cu", [True, False])
+def test_tc_segment_scan_few_heads(host_cu):
+    """Two heads and long sequences: each sequence is cut into segments of 16
+    chunks; pass 1 gives every segment's affine map, a scan gives its starting
+    state, pass 3 its outputs.  Ragged tails, an empty sequence, random S0, and
+    device-only lengths."""
     dev = need_gpu()
     w = inputs.Workload("tc", "prefill", H=2, dk=128, dv=128, dtype=torch.bfloat16, chunk=64, s0_std=0.02)
-    for lengths in ([64 * 64], [64 * 40 + 17, 3000]):
-        _, _, _, eo, es = run_case(w, dev, lengths=lengths, seed=15)
+    for lengths in ([64 * 200 + 37], [5000, 64, 0, 3001], [64 * 64]):
+        _, _, _, eo, es = run_case(w, dev, lengths=lengths, seed=16, host_cu=host_cu)
         assert eo <= 5e-3 and es <= 5e-3, (lengths, eo, es)
+
+
+def test_tc_segment_scan_equal_lengths():
+    """cu_seqlens = NULL (no chunk table): one sequence of 8320 tokens, one head,
+    random S0, split into segments."""
+    dev = need_gpu()
+    w = inputs.Workload("tc", "prefill", T=8320, B=1, H=1, dk=128, dv=128, dtype=torch.bfloat16, chunk=64,
+                        s0_std=0.02)
+    d = inputs.make_prefill(w, device=dev, seed=17)
+    O, Sf = kda.kda_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=d["S0"])
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_device_status() == 0
+    O_ref, Sf_ref = oracle.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=d["S0"])
+    assert rel_err(O, O_ref) <= 5e-3
+    assert rel_err(Sf, Sf_ref) <= 5e-3
 
 
 # ------------------------------------------------------------- full-size workloads
