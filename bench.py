@@ -245,6 +245,32 @@ def time_verify(kda, inputs, steps, warmup, stream, dev, K=8, N=256, H=32, D=128
     return ms, bytes_call
 
 
+def time_few_heads(kda, inputs, steps, warmup, stream, dev, H=2, T=262144, seed=0):
+    """One long sequence with few heads (the per-GPU share under head
+    parallelism): the state pass is cut into segments and scanned."""
+    w = inputs.Workload("few_heads", "prefill", T=T, B=1, H=H, dk=128, dv=128, dtype=torch.bfloat16, chunk=64)
+    d = inputs.make_prefill(w, device=dev, seed=seed)
+    ws = torch.empty(kda.kda_prefill_workspace_size(1, T, H, 128, 128, 64, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    O = torch.empty_like(d["v"])
+    Sf = torch.empty((1, H, 128, 128), dtype=torch.float32, device=dev)
+    call = lambda: kda.kda_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], O=O, S_final=Sf,
+                                   workspace=ws, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            call()
+        end.record(stream)
+        torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    return {"workload": f"prefill_bf16_T{T}_H{H}_D128", "value": T / (ms / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms, "note": "segment scan of the state pass (few chains, long sequence)"}
+
+
 def time_e2e(kda, d, steps, stream, dev):
     """Through the C ABI from pinned host buffers: every step uploads its inputs,
     runs the prefill and reads O and S_final back.  Steps are pipelined the way
@@ -344,6 +370,7 @@ def run_gpu(args):
         dec_steps = max(args.steps, args.decode_steps)
         dms, dsteps = time_decode(kda, wd, inputs, dec_steps, args.warmup, stream, dev, seed=rank)
         vms, vbytes = time_verify(kda, inputs, max(args.steps, 50), args.warmup, stream, dev, seed=rank)
+        few = time_few_heads(kda, inputs, max(3, args.steps // 4), args.warmup, stream, dev, seed=rank)
     ms = barrier_max(ms, world, dev)
     dms = barrier_max(dms, world, dev)
     vms = barrier_max(vms, world, dev)
@@ -393,6 +420,7 @@ def run_gpu(args):
                                 "achieved": vbytes / (vms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
                                 "frac": vbytes / (vms / 1e3) / 1e9 / hbm, "traffic": None,
                                 "bytes_per_launch": vbytes}},
+        "few_heads_long": few,
         "e2e": {"value": replica_throughput(T, e2e_steps, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelining": "2 buffer sets; uploads on 2 copy streams overlap the previous step's prefill"},
