@@ -265,6 +265,17 @@ KDA_API kda_status kda_decode_multi(const void* q, const void* k, const void* v,
 KDA_API kda_status kda_get_last_device_status(cudaStream_t stream);
 
 /*
+ * Check of the failure detection above (the pages have no counterpart; it
+ * computes nothing of KDA): one kernel waits on an mbarrier that nothing
+ * completes, with the same bounded wait the kernels use, for at most
+ * `limit_cycles` SM clock cycles (0 ... ~4e9, the kernels' own limit of about
+ * two seconds).  Afterwards kda_get_last_device_status returns KDA_ERR_TIMEOUT
+ * and the device stays usable.  KDA_ERR_INVALID_ARG for a limit outside that
+ * range, before anything is launched.
+ */
+KDA_API kda_status kda_check_wait_timeout(long long limit_cycles, cudaStream_t stream);
+
+/*
  * Tracing hook.  While set, every kda_prefill / kda_decode call made from the
  * calling host thread records the given CUDA events (cudaEvent_t handles,
  * created by the caller) on its stream at the boundaries between the kernels

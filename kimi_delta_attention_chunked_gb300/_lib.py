@@ -20,7 +20,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUD
 KDA_FP32, KDA_BF16 = 0, 1
 SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_ckpt", "kda_prefill_fused",
            "kda_prefill_noalloc", "kda_decode", "kda_decode_fused", "kda_decode_multi",
-           "kda_get_last_device_status", "kda_set_trace_events", "kda_status_string")
+           "kda_get_last_device_status", "kda_check_wait_timeout", "kda_set_trace_events", "kda_status_string")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lock = threading.Lock()
@@ -62,6 +62,8 @@ def load():
         lib.kda_decode_multi.restype = I
         lib.kda_get_last_device_status.argtypes = [P]
         lib.kda_get_last_device_status.restype = I
+        lib.kda_check_wait_timeout.argtypes = [ctypes.c_longlong, P]
+        lib.kda_check_wait_timeout.restype = I
         lib.kda_set_trace_events.argtypes = [P, I]
         lib.kda_set_trace_events.restype = I
         lib.kda_status_string.argtypes = [I]
@@ -316,6 +318,15 @@ def kda_set_trace_events(events):
         st = lib.kda_set_trace_events(arr, len(events))
     if st != KDA_OK:
         raise KDAError(st, "kda_set_trace_events")
+
+
+def kda_check_wait_timeout(limit_cycles: int, stream=None, device=None) -> None:
+    """Runs one bounded wait that nothing completes (see include/kda.h); the
+    next kda_get_last_device_status() then reports KDA_ERR_TIMEOUT."""
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    st = load().kda_check_wait_timeout(int(limit_cycles), _stream(stream, dev))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_check_wait_timeout")
 
 
 def kda_get_last_device_status(stream=None, device=None) -> int:

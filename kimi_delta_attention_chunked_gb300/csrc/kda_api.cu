@@ -8,6 +8,7 @@
 #include <cstdio>
 
 #include "common.cuh"
+#include "umma.cuh"
 
 namespace {
 
@@ -21,6 +22,17 @@ int* status_ptr() {
         return nullptr;
     }
     return static_cast<int*>(p);
+}
+
+// Failure-detection check: one mbarrier that nothing arrives at, waited on with
+// the kernels' own bounded wait; running out records KDA_ERR_TIMEOUT.
+__global__ void kda_wait_check_kernel(int* status, long long limit) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        kda::mbar_init(&bar, 1);
+        kda::fence_barrier_init();
+        if (!kda::mbar_wait(&bar, 0, limit)) kda::record_status(status, kda::kDevTimeout);
+    }
 }
 
 bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
@@ -244,6 +256,12 @@ kda_status kda_decode_multi(const void* q, const void* k, const void* v, const f
     const cudaError_t e = kda_host::launch_decode_multi(a, K, commit_len);
     kda_host::trace_mark(stream);
     return from_cuda(e);
+}
+
+kda_status kda_check_wait_timeout(long long limit_cycles, cudaStream_t stream) {
+    if (limit_cycles < 0 || limit_cycles > kda::kWaitCycles) return KDA_ERR_INVALID_ARG;
+    kda_wait_check_kernel<<<1, 32, 0, stream>>>(status_ptr(), limit_cycles);
+    return from_cuda(cudaGetLastError());
 }
 
 kda_status kda_get_last_device_status(cudaStream_t stream) {

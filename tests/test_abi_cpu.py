@@ -39,6 +39,12 @@ def test_every_declared_symbol_is_exported(lib):
     assert exported == sorted(declared_functions())
 
 
+def test_wait_check_rejects_bad_limits_before_launch(lib):
+    # checked on the host: nothing is launched (no GPU is needed for this)
+    assert lib.kda_check_wait_timeout(-1, None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_check_wait_timeout(1 << 40, None) == _lib.KDA_ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     for code in range(6):
         s = kda.kda_status_string(code)
