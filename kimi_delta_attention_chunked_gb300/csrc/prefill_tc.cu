@@ -35,12 +35,16 @@
 //      needs: [Q'; W], K_restore^T, U0, O0, a_last.
 //
 //  kda_tc_chain  one CTA per (sequence, head, 64-column slice of d_v);
-//      a4/a5  for each chunk in order (operands streamed by bulk copies,
-//          two stages deep), with S kept in TMEM in fp32:
+//      a4/a5  for each chunk in order (operands streamed by bulk copies into
+//          rings two and three stages deep), with S kept in TMEM in fp32:
 //             P  = [Q'; W] S_in                         (MMA, M = 128)
 //             U  = U0 - P_w                             (W S_in = K_decay part)
 //             O  = P_q + O0
 //             S  = Diag(a_last) S_in + K_restore^T U    (MMA, accumulate)
+//
+// With few chains and long sequences the state pass runs as a segment scan
+// instead (kda_tc_segments, two passes of kda_tc_chain around kda_tc_seg_scan;
+// see the section "segment scan" below).
 //
 // Precision: MMA operands are bf16 with fp32 accumulation.  The operands
 // whose rounding dominated the error budget -- [INV; X] Diag(beta) and U --
