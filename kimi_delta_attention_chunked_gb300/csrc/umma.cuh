@@ -105,11 +105,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, 
         : "memory");
 }
 
-// Hint: bring `bytes` (multiple of 16, 16-byte aligned) at `src` into L2.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // ---------------------------------------------------------------- TMEM
 // Allocation / deallocation are warp-collective.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
@@ -150,17 +145,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* r) {
           "=r"(u[23]), "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]),
           "=r"(u[30]), "=r"(u[31])
         : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* r) {
-    const uint32_t* u = reinterpret_cast<const uint32_t*>(r);
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]), "r"(u[8]),
-        "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15]), "r"(u[16]),
-        "r"(u[17]), "r"(u[18]), "r"(u[19]), "r"(u[20]), "r"(u[21]), "r"(u[22]), "r"(u[23]), "r"(u[24]),
-        "r"(u[25]), "r"(u[26]), "r"(u[27]), "r"(u[28]), "r"(u[29]), "r"(u[30]), "r"(u[31])
-        : "memory");
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* r) {
     const uint32_t* u = reinterpret_cast<const uint32_t*>(r);
