@@ -19,6 +19,7 @@ build) on a bounded sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -39,6 +40,38 @@ METRIC = "KDA prefill tokens/s and decode steps/s (H=32,d=128) on 1 GB300; % roo
 BYTES_TOKEN_HEAD = 3 * 256 + 512 + 4 + 256
 # contraction flops per token-head (8 C D + 6 D^2 with C = 64, D = 128), without the inverse
 FLOPS_TOKEN_HEAD = 8 * 64 * 128 + 6 * 128 * 128
+
+
+# DRAM bytes per launch (dram__bytes_read.sum, dram__bytes_write.sum, in MB) of
+# the ncu captures summarised under profiles/, taken on the workloads this
+# script times.  An entry counts only while every source it was built from
+# still hashes to the recorded prefix (sha256 of the file); after any edit to
+# them the traffic reads null until a new capture replaces the entry.
+PROFILED_TRAFFIC = {
+    "kda_tc_prep": {
+        "read_mb": 336.688128, "write_mb": 479.177728, "profile": "profiles/prefill_tc_T8192_H32_D128.md",
+        "sources": {"csrc/prefill_tc.cu": "ce2a20be72a45dd8", "csrc/umma.cuh": "f70da77c79c8c26e",
+                    "csrc/common.cuh": "10fad8ef65a72b1e"}},
+    "kda_decode_kernel": {
+        "read_mb": 547.525376, "write_mb": 478.725120, "profile": "profiles/decode_N256_H32_D128.md",
+        "sources": {"csrc/decode.cu": "ca2b6a97d7eeaad3", "csrc/common.cuh": "10fad8ef65a72b1e"}},
+    "kda_decode_multi_kernel": {
+        "read_mb": 621.046784, "write_mb": 492.997888, "profile": "profiles/decode_N256_H32_D128.md",
+        "sources": {"csrc/decode.cu": "ca2b6a97d7eeaad3", "csrc/common.cuh": "10fad8ef65a72b1e"}},
+}
+
+
+def profiled_traffic(kernel, table=None):
+    """(bytes per launch, profile path) for ``kernel`` if its capture matches
+    the current sources, else (None, reason)."""
+    e = (PROFILED_TRAFFIC if table is None else table).get(kernel)
+    if e is None:
+        return None, "no capture"
+    for rel, sha in e["sources"].items():
+        path = os.path.join(ROOT, "kimi_delta_attention_chunked_gb300", rel)
+        if not os.path.exists(path) or hashlib.sha256(open(path, "rb").read()).hexdigest()[:len(sha)] != sha:
+            return None, f"{rel} changed since the capture"
+    return (e["read_mb"] + e["write_mb"]) * 1e6, e["profile"]
 
 
 def peaks():
@@ -390,6 +423,7 @@ def run_gpu(args):
     # internal stream), timed from the first prep launch to the last one's end
     prep_bytes = T * H * (3 * 256 + 512 + 4)               # q, k, v, log_alpha, beta read once
     dom = ("kda_tc_prep", prep_ms, prep_bytes)
+    traffic = {name: profiled_traffic(name) for name in ("kda_tc_prep", "kda_decode_kernel", "kda_decode_multi_kernel")}
     achieved = dom[2] / (dom[1] / 1e3) / 1e9
     step_bytes = T * H * BYTES_TOKEN_HEAD + H * 128 * 128 * 4
     dec_bytes_step = wd.B * wd.H * (8 * wd.dk * wd.dv + 3 * 256 + 512 + 4 + 256)
@@ -404,7 +438,8 @@ def run_gpu(args):
                    "state": "fp32, S0 = 0", "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"inputs {in_bytes / 1e6:.0f} MB per step > 129 MB L2 (no flush)"},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None, "peak_source": peak_src,
+                     "frac": achieved / hbm, "traffic": traffic["kda_tc_prep"][0],
+                     "traffic_source": traffic["kda_tc_prep"][1], "peak_source": peak_src,
                      "bytes_per_launch": dom[2], "launch_ms": dom[1]},
         "step_roofline": {"bound": "hbm", "bytes_per_step": step_bytes,
                           "achieved": step_bytes / (ms_step / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
@@ -414,14 +449,18 @@ def run_gpu(args):
         "decode": {"workload": DECODE, "value": replica_throughput(1, dsteps, world, dms), "unit": "steps/s",
                    "steps": dsteps, "ms_per_step": dec_ms_step,
                    "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": dec_achieved,
-                                "peak": hbm, "unit": "GB/s", "frac": dec_achieved / hbm, "traffic": None,
+                                "peak": hbm, "unit": "GB/s", "frac": dec_achieved / hbm,
+                                "traffic": traffic["kda_decode_kernel"][0],
+                                "traffic_source": traffic["kda_decode_kernel"][1],
                                 "bytes_per_launch": dec_bytes_step},
                    "l2": "fp32 state 537 MB > L2; fresh token set per step"},
         "verify": {"workload": "verify_bf16_N256_K8_H32_D128", "value": replica_throughput(1, 1, world, vms),
                    "unit": "calls/s", "ms_per_call": vms,
                    "roofline": {"bound": "hbm", "kernel": "kda_decode_multi_kernel",
                                 "achieved": vbytes / (vms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
-                                "frac": vbytes / (vms / 1e3) / 1e9 / hbm, "traffic": None,
+                                "frac": vbytes / (vms / 1e3) / 1e9 / hbm,
+                                "traffic": traffic["kda_decode_multi_kernel"][0],
+                                "traffic_source": traffic["kda_decode_multi_kernel"][1],
                                 "bytes_per_launch": vbytes}},
         "few_heads_long": few,
         "e2e": {"value": replica_throughput(T, e2e_steps, world, e2e_ms), "unit": "tokens/s",

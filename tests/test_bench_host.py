@@ -69,3 +69,19 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1"],
                        capture_output=True, text=True, timeout=120, env=env, cwd=ROOT)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_profiled_traffic_matches_the_summaries_and_is_dropped_after_an_edit():
+    sys.path.insert(0, ROOT)
+    import bench
+    for kernel, e in bench.PROFILED_TRAFFIC.items():
+        text = open(os.path.join(ROOT, e["profile"])).read()
+        for mb in (e["read_mb"], e["write_mb"]):
+            assert f"{mb:.1f} MB" in text, (kernel, mb)           # the figure the summary shows
+        assert kernel.split("_kernel")[0] in text
+    # a source that no longer hashes to the recorded prefix voids the entry
+    e = dict(bench.PROFILED_TRAFFIC["kda_tc_prep"])
+    e["sources"] = dict(e["sources"], **{"csrc/prefill_tc.cu": "0000000000000000"})
+    traffic, why = bench.profiled_traffic("kda_tc_prep", {"kda_tc_prep": e})
+    assert traffic is None and "prefill_tc.cu" in why
+    assert bench.profiled_traffic("no_such_kernel") == (None, "no capture")
