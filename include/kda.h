@@ -135,7 +135,8 @@ KDA_API kda_status kda_prefill(const void* q, const void* k, const void* v,
  * ckpt_every     positive multiple of chunk: a checkpoint is the state after
  *                the first m * ckpt_every tokens of a sequence (m = 1, 2, ...,
  *                as long as m * ckpt_every <= its length)
- * ckpt           [ckpt_capacity, H, dk, dv] float device array; checkpoint m of
+ * ckpt           [ckpt_capacity, H, dk, dv] float device array, 16-byte
+ *                aligned (else KDA_ERR_INVALID_ARG); checkpoint m of
  *                sequence n goes to index sum_{n' < n} floor(len_n' /
  *                ckpt_every) + m - 1
  * ckpt_capacity  number of checkpoints ckpt holds; when the lengths are known
@@ -225,8 +226,10 @@ KDA_API kda_status kda_decode_fused(const void* q, const void* k, const void* v,
  *
  * q, k       [N, H, dk] dtype;  v [N, H, dv] dtype
  * log_alpha  [N, H, dk] float;  beta [N, H] float
- * S          [N, H, dk, dv] float, read and overwritten in place
+ * S          [N, H, dk, dv] float, read and overwritten in place; 16-byte
+ *            aligned (it moves as float4 vectors), else KDA_ERR_INVALID_ARG
  * o          [N, H, dv] dtype, written; must not alias an input.
+ * N = 0 returns KDA_OK and launches nothing.
  */
 KDA_API kda_status kda_decode(const void* q, const void* k, const void* v,
                       const float* log_alpha, const float* beta, float* S,
@@ -244,8 +247,10 @@ KDA_API kda_status kda_decode(const void* q, const void* k, const void* v,
  *
  * q, k       [N, K, H, dk] dtype;  v [N, K, H, dv] dtype
  * log_alpha  [N, K, H, dk] float;  beta [N, K, H] float
- * S          [N, H, dk, dv] float, read, and written after commit_len tokens
+ * S          [N, H, dk, dv] float, read, and written after commit_len tokens;
+ *            16-byte aligned, else KDA_ERR_INVALID_ARG
  * commit_len [N] int32 device array, values clamped to [0, K]; NULL = K
+ * K > 16 is KDA_ERR_UNSUPPORTED; N = 0 or K = 0 returns KDA_OK.
  * o          [N, K, H, dv] dtype, or NULL to skip the outputs
  * A typical use calls it twice: once with commit_len all 0 to get the
  * outputs, then, once the accepted lengths are known, with o = NULL and
@@ -282,7 +287,8 @@ KDA_API kda_status kda_check_wait_timeout(long long limit_cycles, cudaStream_t s
  * it launches, all on the caller's stream: event 0 before the first kernel;
  * for the tensor-core prefill, event 1 once every chunk-prep kernel has run
  * and event 2 when the state pass (which may run partly on an internal
- * stream, overlapped with later chunk preps) has joined back; for the
+ * stream, overlapped with later chunk preps, or as a segment scan of three
+ * kernels for few long sequences) has finished on the caller's stream; for the
  * CUDA-core prefill and the decode, event 1 after their one kernel.  Events beyond
  * n_events are skipped.  Pass (NULL, 0) to stop.  Returns KDA_ERR_INVALID_ARG
  * for n_events < 0 or a NULL array with n_events > 0.  The array must stay
