@@ -40,6 +40,10 @@ METRIC = "KDA prefill tokens/s and decode steps/s (H=32,d=128) on 1 GB300; % roo
 BYTES_TOKEN_HEAD = 3 * 256 + 512 + 4 + 256
 # contraction flops per token-head (8 C D + 6 D^2 with C = 64, D = 128), without the inverse
 FLOPS_TOKEN_HEAD = 8 * 64 * 128 + 6 * 128 * 128
+# the same with the chunk inverse counted as 12 C^2 per token-head
+FLOPS_TOKEN_HEAD_INV = FLOPS_TOKEN_HEAD + 12 * 64 * 64
+# the nominal HBM3e bandwidth, reported beside the measured peak for the decode step
+HBM_NOMINAL_GBS = 8000.0
 
 
 # DRAM bytes per launch (dram__bytes_read.sum, dram__bytes_write.sum, in MB) of
@@ -445,11 +449,13 @@ def run_gpu(args):
                           "achieved": step_bytes / (ms_step / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
                           "frac": step_bytes / (ms_step / 1e3) / 1e9 / hbm,
                           "tflops": T * H * FLOPS_TOKEN_HEAD / (ms_step / 1e3) / 1e12,
+                          "tflops_with_inverse": T * H * FLOPS_TOKEN_HEAD_INV / (ms_step / 1e3) / 1e12,
                           "kernel_ms": {"kda_tc_prep_span": prep_ms, "state_pass_tail": chain_ms}},
         "decode": {"workload": DECODE, "value": replica_throughput(1, dsteps, world, dms), "unit": "steps/s",
                    "steps": dsteps, "ms_per_step": dec_ms_step,
                    "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": dec_achieved,
                                 "peak": hbm, "unit": "GB/s", "frac": dec_achieved / hbm,
+                                "frac_of_nominal_8tbs": dec_achieved / HBM_NOMINAL_GBS,
                                 "traffic": traffic["kda_decode_kernel"][0],
                                 "traffic_source": traffic["kda_decode_kernel"][1],
                                 "bytes_per_launch": dec_bytes_step},

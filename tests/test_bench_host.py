@@ -85,3 +85,67 @@ def test_profiled_traffic_matches_the_summaries_and_is_dropped_after_an_edit():
     traffic, why = bench.profiled_traffic("kda_tc_prep", {"kda_tc_prep": e})
     assert traffic is None and "prefill_tc.cu" in why
     assert bench.profiled_traffic("no_such_kernel") == (None, "no capture")
+
+
+def test_bench_line_assembly_without_a_gpu(monkeypatch, capsys):
+    """bench.run_gpu with every device call faked: the JSON line carries the
+    contract's keys and derives its figures from the timings it was given."""
+    sys.path.insert(0, ROOT)
+    import types
+    import bench
+    from kimi_delta_attention_chunked_gb300 import build, inputs
+    import kimi_delta_attention_chunked_gb300 as kda
+
+    class Clocks:
+        def __init__(self, gpu):
+            pass
+
+        def __enter__(self):
+            return self
+
+        def __exit__(self, *exc):
+            return False
+
+        def summary(self):
+            return {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 5}
+
+    T, H = 8192, 32
+
+    def fake_prefill(w, device=None, seed=0, lengths=None):
+        small = lambda *s: torch.zeros(*s)
+        return {"T": T, "q": small(4, 2), "k": small(4, 2), "v": small(4, 2), "log_alpha": small(4, 2),
+                "beta": small(4), "S0": None}
+
+    monkeypatch.setattr(bench, "ClockSampler", Clocks)
+    monkeypatch.setattr(bench, "time_prefill", lambda *a, **k: (9.0, 0.25, 0.2, 40))
+    monkeypatch.setattr(bench, "time_decode", lambda *a, **k: (168.0, 1000))
+    monkeypatch.setattr(bench, "time_verify", lambda *a, **k: (0.368, 1_100_000_000))
+    monkeypatch.setattr(bench, "time_few_heads", lambda *a, **k: {"value": 1.0})
+    monkeypatch.setattr(bench, "time_e2e", lambda *a, **k: (20.0, 336_592_896, 69_206_016))
+    monkeypatch.setattr(build, "build", lambda *a, **k: None)
+    monkeypatch.setattr(kda, "load", lambda *a, **k: None)
+    monkeypatch.setattr(inputs, "make_prefill", fake_prefill)
+    monkeypatch.setattr(torch.cuda, "set_device", lambda *a: None)
+    monkeypatch.setattr(torch.cuda, "synchronize", lambda *a: None)
+    monkeypatch.setattr(torch.cuda, "Stream", lambda *a, **k: None)
+    for var in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+    args = types.SimpleNamespace(steps=20, warmup=3, decode_steps=1000, no_cpu_baseline=True, oracle_tokens=8192,
+                                 oracle_seconds=10.0)
+    assert bench.run_gpu(args) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "clocks", "gpu_launches"):
+        assert key in line, key
+    assert line["value"] == pytest.approx(T * 20 / 9.0e-3)
+    assert line["ms_per_step"] == pytest.approx(9.0 / 20)
+    r = line["roofline"]
+    assert r["achieved"] == pytest.approx(r["bytes_per_launch"] / 0.25e-3 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+    assert set(r) >= {"bound", "achieved", "peak", "unit", "frac", "traffic"}
+    assert line["step_roofline"]["tflops_with_inverse"] > line["step_roofline"]["tflops"]
+    dec = line["decode"]
+    assert dec["value"] == pytest.approx(1000 / 0.168)
+    assert dec["roofline"]["frac_of_nominal_8tbs"] < dec["roofline"]["frac"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 336_592_896
+    assert line["gpu_launches"] == 40 and line["config"]["workload"] == bench.PREFILL
