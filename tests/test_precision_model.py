@@ -125,3 +125,19 @@ def test_rounding_points_meet_the_bf16_bar(mu, s0_std):
     # with every operand carried as one bf16 part the bar is missed
     assert eo_1 > BAR, eo_1
     assert es_1 > 1.5 * es, (es_1, es)
+
+
+def test_dominant_rounding_terms():
+    """Where the remaining error sits: with the Gram operands exact the O error
+    falls to the store's alone; with K_restore exact the S error nearly vanishes."""
+    q, k, v, g, beta, S0 = workload(3, 1024 + 37, 0.0, 0.0)
+    O_ref, S_ref = oracle.prefill(q[:, None], k[:, None], v[:, None], g[:, None], beta[:, None], S0=S0[None, None])
+    O_ref, S_ref = O_ref[:, 0], S_ref[0, 0]
+    err = lambda OS: (rel(OS[0], O_ref), rel(OS[1], S_ref))
+    eo, es = err(model(q, k, v, g, beta, S0))
+    eo_store, _ = err(model(q, k, v, g, beta, S0, exact=set(POINTS) - {"o_store"}))
+    eo_gram, _ = err(model(q, k, v, g, beta, S0, exact={"gram"}))
+    _, es_kr = err(model(q, k, v, g, beta, S0, exact={"k_restore"}))
+    assert eo > 1.2 * eo_store
+    assert eo_gram <= 1.05 * eo_store, (eo_gram, eo_store)
+    assert es_kr < 0.1 * es, (es_kr, es)
