@@ -105,6 +105,43 @@ def _check_dev(name, t, device, dtype=None):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _check_shape(name, t, shape):
+    """The kernels index every tensor from the sizes passed through the C ABI
+    (which sees only pointers), so a tensor of another shape would be read or
+    written out of bounds: refuse it here."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _token_shapes(q, v, lead):
+    """(dk, dv) of q [*lead, dk] and v [*lead, dv], checking their leading dims."""
+    if q.dim() != len(lead) + 1 or v.dim() != len(lead) + 1:
+        raise ValueError(f"q and v must have {len(lead) + 1} dims, got {q.dim()} and {v.dim()}")
+    if tuple(v.shape[:-1]) != tuple(q.shape[:-1]):
+        raise ValueError(f"v {tuple(v.shape)} does not match q {tuple(q.shape)} in its leading dims")
+    return q.shape[-1], v.shape[-1]
+
+
+def _check_prefill_shapes(q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, O, S_final):
+    """Shapes of a prefill call (include/kda.h): q, k, log_alpha [T, H, dk];
+    v, O [T, H, dv]; beta [T, H]; S0, S_final [n_seq, H, dk, dv];
+    cu_seqlens [n_seq + 1] (and its host copy).  Returns (T, H, dk, dv, n_seq)."""
+    dk, dv = _token_shapes(q, v, ("T", "H"))
+    T, H = q.shape[0], q.shape[1]
+    _check_shape("k", k, (T, H, dk))
+    _check_shape("log_alpha", log_alpha, (T, H, dk))
+    _check_shape("beta", beta, (T, H))
+    if cu_seqlens is not None and (cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2):
+        raise ValueError("cu_seqlens must be a 1-D tensor of n_seq + 1 >= 2 offsets")
+    n_seq = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if cu_seqlens is not None and cu_seqlens_host is not None and len(cu_seqlens_host) != n_seq + 1:
+        raise ValueError(f"cu_seqlens_host must hold {n_seq + 1} offsets, got {len(cu_seqlens_host)}")
+    _check_shape("S0", S0, (n_seq, H, dk, dv))
+    _check_shape("O", O, (T, H, dv))
+    _check_shape("S_final", S_final, (n_seq, H, dk, dv))
+    return T, H, dk, dv, n_seq
+
+
 def kda_prefill_workspace_size(n_seq: int, T_total: int, H: int, dk: int, dv: int, chunk: int,
                                dtype: torch.dtype) -> int:
     return int(load().kda_prefill_workspace_size(n_seq, T_total, H, dk, dv, chunk, _dtype_code(dtype)))
@@ -132,16 +169,15 @@ def _prefill(entry, q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, c
              stream, want_state):
     lib = load()
     dev = q.device
-    T, H, dk = q.shape
-    dv = v.shape[-1]
-    for name, t in (("q", q), ("k", k), ("v", v)):
+    T, H, dk, dv, n_seq = _check_prefill_shapes(q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, O,
+                                                S_final)
+    for name, t in (("q", q), ("k", k), ("v", v), ("O", O)):
         _check_dev(name, t, dev, q.dtype)
     _check_dev("log_alpha", log_alpha, dev, torch.float32)
     _check_dev("beta", beta, dev, torch.float32)
     _check_dev("cu_seqlens", cu_seqlens, dev, torch.int32)
-    n_seq = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
-    if S0 is not None:
-        _check_dev("S0", S0, dev, torch.float32)
+    _check_dev("S0", S0, dev, torch.float32)
+    _check_dev("S_final", S_final, dev, torch.float32)
     if O is None:
         O = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
     if S_final is None and want_state:
@@ -151,6 +187,7 @@ def _prefill(entry, q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, c
         host = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
     dt = _dtype_code(q.dtype)
     need = int(lib.kda_prefill_workspace_size(n_seq, T, H, dk, dv, chunk, dt))
+    _check_dev("workspace", workspace, dev)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -175,16 +212,17 @@ def kda_prefill_ckpt(q, k, v, log_alpha, beta, ckpt_every, S0=None, cu_seqlens=N
     buffer the lengths must be known here (``cu_seqlens_host``, or one sequence)."""
     lib = load()
     dev = q.device
-    T, H, dk = q.shape
-    dv = v.shape[-1]
-    for name, t in (("q", q), ("k", k), ("v", v)):
+    T, H, dk, dv, n_seq = _check_prefill_shapes(q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, O,
+                                                S_final)
+    if ckpt is not None and (ckpt.dim() != 4 or tuple(ckpt.shape[1:]) != (H, dk, dv)):
+        raise ValueError(f"ckpt must have shape (n, {H}, {dk}, {dv}), got {tuple(ckpt.shape)}")
+    for name, t in (("q", q), ("k", k), ("v", v), ("O", O)):
         _check_dev(name, t, dev, q.dtype)
     _check_dev("log_alpha", log_alpha, dev, torch.float32)
     _check_dev("beta", beta, dev, torch.float32)
     _check_dev("cu_seqlens", cu_seqlens, dev, torch.int32)
-    n_seq = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
-    if S0 is not None:
-        _check_dev("S0", S0, dev, torch.float32)
+    _check_dev("S0", S0, dev, torch.float32)
+    _check_dev("S_final", S_final, dev, torch.float32)
     if ckpt is None:
         if cu_seqlens is None:
             lens = [T]
@@ -204,6 +242,7 @@ def kda_prefill_ckpt(q, k, v, log_alpha, beta, ckpt_every, S0=None, cu_seqlens=N
         host = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
     dt = _dtype_code(q.dtype)
     need = int(lib.kda_prefill_workspace_size(n_seq, T, H, dk, dv, chunk, dt))
+    _check_dev("workspace", workspace, dev)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -224,16 +263,15 @@ def kda_prefill_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, cu_s
     here is only a convenience of this binding.  Returns (O, S_final)."""
     lib = load()
     dev = q.device
-    T, H, dk = q.shape
-    dv = v.shape[-1]
-    for name, t in (("q", q), ("k", k), ("v", v)):
+    T, H, dk, dv, n_seq = _check_prefill_shapes(q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, O,
+                                                S_final)
+    for name, t in (("q", q), ("k", k), ("v", v), ("O", O)):
         _check_dev(name, t, dev, q.dtype)
     _check_dev("log_alpha", log_alpha, dev, torch.float32)
     _check_dev("beta", beta, dev, torch.float32)
     _check_dev("cu_seqlens", cu_seqlens, dev, torch.int32)
-    n_seq = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
-    if S0 is not None:
-        _check_dev("S0", S0, dev, torch.float32)
+    _check_dev("S0", S0, dev, torch.float32)
+    _check_dev("S_final", S_final, dev, torch.float32)
     if O is None:
         O = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
     if S_final is None:
@@ -262,9 +300,14 @@ def kda_decode_fused(q, k, v, gate, beta_logit, S, o=None, stream=None):
 def _decode(entry, q, k, v, log_alpha, beta, S, o, stream):
     lib = load()
     dev = q.device
-    N, H, dk = q.shape
-    dv = v.shape[-1]
-    for name, t in (("q", q), ("k", k), ("v", v)):
+    dk, dv = _token_shapes(q, v, ("N", "H"))
+    N, H = q.shape[0], q.shape[1]
+    _check_shape("k", k, (N, H, dk))
+    _check_shape("log_alpha", log_alpha, (N, H, dk))
+    _check_shape("beta", beta, (N, H))
+    _check_shape("S", S, (N, H, dk, dv))
+    _check_shape("o", o, (N, H, dv))
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
         _check_dev(name, t, dev, q.dtype)
     _check_dev("log_alpha", log_alpha, dev, torch.float32)
     _check_dev("beta", beta, dev, torch.float32)
@@ -284,9 +327,15 @@ def kda_decode_multi(q, k, v, log_alpha, beta, S, commit_len=None, o=None, want_
     the device or None = all K).  Returns o [N, K, H, dv] (None if want_o is False)."""
     lib = load()
     dev = q.device
-    N, K, H, dk = q.shape
-    dv = v.shape[-1]
-    for name, t in (("q", q), ("k", k), ("v", v)):
+    dk, dv = _token_shapes(q, v, ("N", "K", "H"))
+    N, K, H = q.shape[0], q.shape[1], q.shape[2]
+    _check_shape("k", k, (N, K, H, dk))
+    _check_shape("log_alpha", log_alpha, (N, K, H, dk))
+    _check_shape("beta", beta, (N, K, H))
+    _check_shape("S", S, (N, H, dk, dv))
+    _check_shape("commit_len", commit_len, (N,))
+    _check_shape("o", o, (N, K, H, dv))
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
         _check_dev(name, t, dev, q.dtype)
     _check_dev("log_alpha", log_alpha, dev, torch.float32)
     _check_dev("beta", beta, dev, torch.float32)
