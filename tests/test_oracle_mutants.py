@@ -54,3 +54,47 @@ def test_pins_catch_mutant(name, tmp_path):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin caught mutant {name}"
+
+
+# Mistakes in the fused prologue, caught by the prologue's own pins
+# (tests/test_oracle_prologue.py), run against the mutant build.
+PROLOGUE_MUTANTS = {
+    "eps_outside_sqrt": ("return 1.0 / sqrt(ss + 1e-6);", "return 1.0 / (sqrt(ss) + 1e-6);"),
+    "softplus_sign": ("const double lg = -log1p(exp(a));", "const double lg = -log1p(exp(-a));"),
+    "no_lower_clamp": ("return lg < -5.0 ? -5.0 :", "return lg < -50.0 ? -50.0 :"),
+    "sigmoid_sign": ("return 1.0 / (1.0 + exp(-b));", "return 1.0 / (1.0 + exp(b));"),
+    "k_scaled_by_q_norm": ("const double ks = prologue ? prologue_unit_scale(k32, dk) : 1.0;",
+                           "const double ks = prologue ? prologue_unit_scale(q32, dk) : 1.0;"),
+    "gate_not_activated": ("gt[i] = prologue ? prologue_log_alpha((double)g32[i]) : (double)g32[i];",
+                           "gt[i] = (double)g32[i];"),
+}
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(PROLOGUE_MUTANTS))
+def test_prologue_pins_catch_mutant(name, tmp_path, monkeypatch):
+    import test_oracle_prologue as pp
+    old, new = PROLOGUE_MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation anchor for {name} not found"
+    src = tmp_path / f"{name}.c"
+    src.write_text(text.replace(old, new, 1))
+    lib = oracle.bind(oracle.compile_source(str(src), str(tmp_path / f"lib{name}.so")))
+    monkeypatch.setattr(oracle, "_load", lambda: lib)
+    pins = [getattr(pp, n) for n in dir(pp) if n.startswith("test_")]
+    caught = []
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no prologue pin caught mutant {name}"
+
+
+def test_prologue_pins_pass_on_the_oracle():
+    """The same loop over the unmodified oracle raises nothing (the mutant test
+    above is not vacuous)."""
+    import test_oracle_prologue as pp
+    for n in dir(pp):
+        if n.startswith("test_"):
+            getattr(pp, n)()
