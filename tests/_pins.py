@@ -19,7 +19,8 @@ P5  the chunked matrix form ("Kimi K3: the manos, the mythos, the legendos",
 P6  orthonormal keys with beta = 1 and no decay turn S into a lookup table whose
     row i holds the last value written under key e_i;
 P7  splitting a sequence and carrying the state equals one run; a packed
-    varlen batch equals separate runs (the chunk unrolling holds from any
+    varlen batch equals separate runs, with per-sequence S0 and without one
+    (each sequence then starts from zero; the chunk unrolling holds from any
     starting state).
 """
 from __future__ import annotations
@@ -169,6 +170,14 @@ def pin_p7_split_and_varlen(run, seed=7):
         On, Sfn = run(q[a:e], k[a:e], v[a:e], g[a:e], b[a:e], S0=S0v[n:n + 1])
         assert rel(Ov[a:e], On) < 1e-15 if e > a else True
         assert np.array_equal(Sfv[n], Sfn[0])
+    # ... and without S0 every sequence starts from a zero state, not from the
+    # state its predecessor left
+    Oz, Sfz = run(q, k, v, g, b, cu_seqlens=cu)
+    for n in range(4):
+        a, e = cu[n], cu[n + 1]
+        On, Sfn = run(q[a:e], k[a:e], v[a:e], g[a:e], b[a:e])
+        assert rel(Oz[a:e], On) < 1e-15 if e > a else True
+        assert np.array_equal(Sfz[n], Sfn[0])
 
 
 ALL_PINS = [pin_p1_product_form, pin_p2_no_write, pin_p3_scalar_gate, pin_p4_exact_write,

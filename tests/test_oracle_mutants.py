@@ -20,6 +20,15 @@ MUTANTS = {
     "readout_uses_k": ("const double qi = (double)qt[i];", "const double qi = (double)kt[i];"),
     "first_token_skipped": ("for (int64_t t = bos; t < eos; ++t) {", "for (int64_t t = bos + 1; t < eos; ++t) {"),
     "s0_ignored": ("if (S0_nh)\n", "if (0)\n"),
+    "state_carried_across_sequences": ("    else\n        memset(S, 0, sizeof(double) * (size_t)dk * dv);",
+                                       "    else if (bos == 0)\n        memset(S, 0, sizeof(double) * (size_t)dk * dv);"),
+    "readout_before_write": (
+        "        /* Delta-rule write: S += k_t (beta_t (v_t - v_old))^T. */",
+        "        if (O) {\n            double* ot = O + ((size_t)t * Hs + hs) * dv;\n"
+        "            for (int j = 0; j < dv; ++j) ot[j] = 0.0;\n"
+        "            for (int i = 0; i < dk; ++i) for (int j = 0; j < dv; ++j) ot[j] += S[(size_t)i*dv+j] * qt[i];\n"
+        "        }\n"
+        "        /* Delta-rule write: S += k_t (beta_t (v_t - v_old))^T. */"),
     "vold_before_decay": (
         "        /* Decay old memory: row i of S times alpha_t[i]. */",
         "        for (int j = 0; j < dv; ++j) x[j] = 0.0;\n"
@@ -34,7 +43,12 @@ def test_pins_catch_mutant(name, tmp_path):
     old, new = MUTANTS[name]
     text = open(SRC).read()
     assert text.count(old) >= 1, f"mutation anchor for {name} not found"
-    if name == "vold_before_decay":
+    if name == "readout_before_write":
+        # read out from the decayed state before the write; the read-out after the write is dropped
+        text = text.replace(old, new, 1)
+        text = text.replace("        /* Read-out o_t = S_t^T q_t (after the write). */\n        if (O) {",
+                            "        /* Read-out o_t = S_t^T q_t (after the write). */\n        if (0) {", 1)
+    elif name == "vold_before_decay":
         # compute v_old from the undecayed state, then skip the later v_old pass
         text = text.replace(old, new, 1)
         text = text.replace("        /* v_old = Sbar^T k_t. */\n        for (int j = 0; j < dv; ++j) x[j] = 0.0;\n"
