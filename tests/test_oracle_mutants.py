@@ -20,6 +20,9 @@ MUTANTS = {
     "readout_uses_k": ("const double qi = (double)qt[i];", "const double qi = (double)kt[i];"),
     "first_token_skipped": ("for (int64_t t = bos; t < eos; ++t) {", "for (int64_t t = bos + 1; t < eos; ++t) {"),
     "s0_ignored": ("if (S0_nh)\n", "if (0)\n"),
+    "gate_on_columns": ("for (int j = 0; j < dv; ++j) Si[j] *= a;",
+                        "for (int j = 0; j < dv; ++j) Si[j] *= exp((double)gt[j]);"),
+    "beta_squared": ("x[j] = bt * ((double)vt[j] - x[j]);", "x[j] = bt * bt * ((double)vt[j] - x[j]);"),
     "state_carried_across_sequences": ("    else\n        memset(S, 0, sizeof(double) * (size_t)dk * dv);",
                                        "    else if (bos == 0)\n        memset(S, 0, sizeof(double) * (size_t)dk * dv);"),
     "readout_before_write": (
