@@ -13,7 +13,11 @@
  * section "The KDA update, in plain words").  The gate is passed as
  * log_alpha = ln(alpha_t), expected in [-5, 0): the log-decay bound stated on
  * that page.  Values outside it are computed but not guaranteed to meet the
- * accuracy target.
+ * accuracy target.  Known limit of the bf16 tensor-core path: when almost no
+ * channel decays (log_alpha near 0 everywhere) the state pass's bf16 operands
+ * accumulate rounding over the whole sequence, and a model of its rounding
+ * puts the output error past the bf16 target (5e-3 relative to max|o|) after
+ * about a thousand tokens.
  *
  * Two entry points compute it:
  *   kda_prefill -- many tokens at once in the chunked form ("Kimi K3: the
