@@ -82,13 +82,20 @@ def gram(rows, cols_k, G, incl, rnd):
     return out
 
 
-def model(q, k, v, g, beta, S0, split=True, exact=(), as_tf32=()):
+def model(q, k, v, g, beta, S0, split=True, exact=(), as_tf32=(), as_pair=()):
     """Outputs and final state of the chunked form with the kernels' rounding
     points.  split=False carries every operand as a single bf16 part; the
     points named in ``exact`` (from POINTS) are not rounded at all, those in
-    ``as_tf32`` are rounded to tf32 instead of bf16."""
+    ``as_tf32`` are rounded to tf32 instead of bf16, and single-part points in
+    ``as_pair`` are carried as a high/low bf16 pair."""
     exact_fn = lambda x: np.asarray(x, dtype=np.float64)
-    pick = lambda name, f: exact_fn if name in exact else (tf32 if name in as_tf32 else f)
+
+    def pick(name, f):
+        if name in exact:
+            return exact_fn
+        if name in as_tf32:
+            return tf32
+        return hilo if name in as_pair else f
     two = hilo if split else bf
     T = q.shape[0]
     O = np.zeros((T, D))
@@ -161,7 +168,8 @@ def test_no_decay_extreme():
     K_restore) accumulate error over the whole sequence.  The model puts O past
     the bar at ~1000 tokens with the rounding points as built; with those four
     operands in tf32 it is back inside, and with the staged K_decay and Gram
-    operands in tf32 too it is near the floor set by the bf16 store of O."""
+    operands in tf32 too it is near the floor set by the bf16 store of O.
+    S_in and K_restore as high/low bf16 pairs also bring it back inside."""
     q, k, v, g, beta, S0 = workload(5, 1024 + 37, 0.0, 0.02)
     g = np.full_like(g, np.float32(-1e-4)).astype(np.float64)
     O_ref, S_ref = oracle.prefill(q[:, None], k[:, None], v[:, None], g[:, None], beta[:, None], S0=S0[None, None])
@@ -171,9 +179,12 @@ def test_no_decay_extreme():
     eo, es = err(model(q, k, v, g, beta, S0))
     eo_t, es_t = err(model(q, k, v, g, beta, S0, as_tf32=state_pass))
     eo_t2, es_t2 = err(model(q, k, v, g, beta, S0, as_tf32=state_pass | {"k_decay", "gram"}))
+    eo_p, es_p = err(model(q, k, v, g, beta, S0, as_pair={"s_in", "k_restore"}))
     eo_store, _ = err(model(q, k, v, g, beta, S0, exact=set(POINTS) - {"o_store"}))
     print(f"no decay: as built O {eo:.2e} S {es:.2e}; tf32 state pass O {eo_t:.2e} S {es_t:.2e}; "
-          f"+ tf32 K_decay, Gram O {eo_t2:.2e} S {es_t2:.2e}; O store alone {eo_store:.2e}")
+          f"+ tf32 K_decay, Gram O {eo_t2:.2e} S {es_t2:.2e}; S_in, K_restore pairs O {eo_p:.2e} S {es_p:.2e}; "
+          f"O store alone {eo_store:.2e}")
     assert eo > BAR                                   # as built: past the bar in the model
     assert eo_t <= 0.85 * BAR and es_t <= 0.5 * BAR
     assert eo_t2 <= 1.15 * eo_store
+    assert eo_p <= 0.9 * BAR and es_p <= 0.5 * BAR
