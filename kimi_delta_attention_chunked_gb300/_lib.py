@@ -131,8 +131,8 @@ def _check_prefill_shapes(q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_h
     _check_shape("k", k, (T, H, dk))
     _check_shape("log_alpha", log_alpha, (T, H, dk))
     _check_shape("beta", beta, (T, H))
-    if cu_seqlens is not None and (cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2):
-        raise ValueError("cu_seqlens must be a 1-D tensor of n_seq + 1 >= 2 offsets")
+    if cu_seqlens is not None and (cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1):
+        raise ValueError("cu_seqlens must be a 1-D tensor of n_seq + 1 offsets")
     n_seq = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
     if cu_seqlens is not None and cu_seqlens_host is not None and len(cu_seqlens_host) != n_seq + 1:
         raise ValueError(f"cu_seqlens_host must hold {n_seq + 1} offsets, got {len(cu_seqlens_host)}")

@@ -45,8 +45,10 @@ def test_prefill_refuses_mismatched_shapes(name, bad):
 def test_prefill_refuses_bad_offsets():
     with pytest.raises(ValueError, match="cu_seqlens_host"):
         call_prefill(cu_seqlens_host=[0, 70])
-    with pytest.raises(ValueError, match="cu_seqlens"):
-        call_prefill(cu_seqlens=torch.tensor([70], dtype=torch.int32), cu_seqlens_host=None, S0=None)
+    with pytest.raises(ValueError, match="cu_seqlens must be"):
+        call_prefill(cu_seqlens=torch.tensor([[0, 30, 70]], dtype=torch.int32), cu_seqlens_host=None, S0=None)
+    with pytest.raises(ValueError, match="cu_seqlens must be"):
+        call_prefill(cu_seqlens=torch.zeros(0, dtype=torch.int32), cu_seqlens_host=None, S0=None)
     with pytest.raises(ValueError, match="dims"):
         call_prefill(q=torch.zeros(70, 3, 2, 16), v=torch.zeros(70, 3, 2, 16))
 
