@@ -44,6 +44,9 @@ FLOPS_TOKEN_HEAD = 8 * 64 * 128 + 6 * 128 * 128
 FLOPS_TOKEN_HEAD_INV = FLOPS_TOKEN_HEAD + 12 * 64 * 64
 # the nominal HBM3e bandwidth, reported beside the measured peak for the decode step
 HBM_NOMINAL_GBS = 8000.0
+# one fp32 state of one (sequence, head), d_k = d_v = 128
+STATE_BYTES = 128 * 128 * 4
+PARTS = ("prefill", "decode", "verify", "few", "varlen", "long", "e2e")
 
 
 # DRAM bytes per launch (dram__bytes_read.sum, dram__bytes_write.sum, in MB) of
@@ -307,8 +310,74 @@ def time_few_heads(kda, inputs, steps, warmup, stream, dev, H=2, T=262144, seed=
         end.record(stream)
         torch.cuda.synchronize()
     ms = start.elapsed_time(end) / steps
-    return {"workload": f"prefill_bf16_T{T}_H{H}_D128", "value": T / (ms / 1e3), "unit": "tokens/s",
-            "ms_per_step": ms, "note": "segment scan of the state pass (few chains, long sequence)"}
+    out = {"workload": f"prefill_bf16_T{T}_H{H}_D128", "value": T / (ms / 1e3), "unit": "tokens/s",
+           "ms_per_step": ms, "note": "segment scan of the state pass (few chains, long sequence)"}
+    out["roofline"] = step_roofline(T * H * BYTES_TOKEN_HEAD + H * STATE_BYTES, ms)
+    return out
+
+
+def step_roofline(bytes_per_step, ms, hbm=None):
+    """HBM roofline of one whole prefill call: compulsory bytes (inputs, O,
+    states) over the measured time, against the measured copy bandwidth."""
+    hbm = hbm or peaks()[0]
+    achieved = bytes_per_step / (ms / 1e3) / 1e9
+    return {"bound": "hbm", "bytes_per_step": bytes_per_step, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "floor_ms": bytes_per_step / (hbm * 1e9) * 1e3}
+
+
+def time_prefill_workload(kda, inputs, name, steps, warmup, stream, dev, seed=0):
+    """One of the larger prefill workloads (packed varlen with random initial
+    states; the 1,048,576-token sequence), inputs resident in HBM, the same
+    call a user makes.  Each workload's tensors are freed before returning."""
+    w = inputs.WORKLOADS[name]
+    d = inputs.make_prefill(w, device=dev, seed=seed)
+    T, H, n_seq = d["T"], w.H, len(d["lengths"])
+    ws = torch.empty(kda.kda_prefill_workspace_size(n_seq, T, H, 128, 128, 64, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    O = torch.empty_like(d["v"])
+    Sf = torch.empty((n_seq, H, 128, 128), dtype=torch.float32, device=dev)
+    call = lambda: kda.kda_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=d["S0"],
+                                   cu_seqlens=d["cu_seqlens"] if w.varlen else None,
+                                   cu_seqlens_host=d["cu_seqlens_host"] if w.varlen else None,
+                                   O=O, S_final=Sf, workspace=ws, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            call()
+        end.record(stream)
+        torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    state_io = (2 if d["S0"] is not None else 1) * n_seq * H * STATE_BYTES
+    out = {"workload": name, "value": T / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+           "tokens": T, "sequences": n_seq, "lengths": d["lengths"] if w.varlen else None,
+           "roofline": step_roofline(T * H * BYTES_TOKEN_HEAD + state_io, ms)}
+    del d, ws, O, Sf
+    torch.cuda.empty_cache()
+    return out
+
+
+def link_bandwidth(dev, nbytes=1 << 30, reps=3):
+    """Pinned host <-> device copy rates (GB/s) on this machine, each direction
+    alone, best of ``reps``: the roofline of the end-to-end number."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    g = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, (dst, src) in (("h2d_gbs", (g, h)), ("d2h_gbs", (h, g))):
+        best = float("inf")
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            dst.copy_(src, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        out[name] = nbytes / (best / 1e3) / 1e9
+    del h, g
+    return out
 
 
 def time_e2e(kda, d, steps, stream, dev):
@@ -394,87 +463,101 @@ def run_gpu(args):
     kda.load()
     hbm, bf16_tf, peak_src = peaks()
     stream = torch.cuda.Stream(device=dev)
+    parts = set(getattr(args, "parts", None) or PARTS)
 
     wp = inputs.WORKLOADS[PREFILL]
     d = inputs.make_prefill(wp, device=dev, seed=rank)
     d["S0"] = None
     T, H = d["T"], wp.H
     in_bytes = sum(d[n].numel() * d[n].element_size() for n in ("q", "k", "v", "log_alpha", "beta"))
+    traffic = {name: profiled_traffic(name) for name in ("kda_tc_prep", "kda_decode_kernel", "kda_decode_multi_kernel")}
+    line = {"metric": METRIC, "value": None, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": PREFILL, "B": 1, "T": T, "H": H, "dk": 128, "dv": 128, "chunk": 64,
+                       "state": "fp32, S0 = 0", "parallelism": "replicas" if world > 1 else "single",
+                       "l2": f"inputs {in_bytes / 1e6:.0f} MB per step > 129 MB L2 (no flush)"}}
+    if parts != set(PARTS):
+        line["parts"] = sorted(parts)
 
     sync_barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        ms, prep_ms, chain_ms, launches = time_prefill(kda, d, args.steps, args.warmup, stream, dev)
-        sync_barrier(world)
-        wd = inputs.WORKLOADS[DECODE]
-        dec_steps = max(args.steps, args.decode_steps)
-        dms, dsteps = time_decode(kda, wd, inputs, dec_steps, args.warmup, stream, dev, seed=rank)
-        vms, vbytes = time_verify(kda, inputs, max(args.steps, 50), args.warmup, stream, dev, seed=rank)
-        few = time_few_heads(kda, inputs, max(3, args.steps // 4), args.warmup, stream, dev, seed=rank)
-    ms = barrier_max(ms, world, dev)
-    dms = barrier_max(dms, world, dev)
-    vms = barrier_max(vms, world, dev)
-    e2e_steps = max(6, args.steps // 2)
-    e2e_ms, h2d, d2h = time_e2e(kda, d, e2e_steps, stream, dev)
-    e2e_ms = barrier_max(e2e_ms, world, dev)
-
-
-    tok_per_step = T * world
-    value = replica_throughput(T, args.steps, world, ms)
-    ms_step = ms / args.steps
-    # roofline of the dominant kernel: the chunk-prep kernels, whose launches run
-    # back to back on the caller's stream (the state pass overlaps them on an
-    # internal stream), timed from the first prep launch to the last one's end
-    prep_bytes = T * H * (3 * 256 + 512 + 4)               # q, k, v, log_alpha, beta read once
-    dom = ("kda_tc_prep", prep_ms, prep_bytes)
-    traffic = {name: profiled_traffic(name) for name in ("kda_tc_prep", "kda_decode_kernel", "kda_decode_multi_kernel")}
-    achieved = dom[2] / (dom[1] / 1e3) / 1e9
-    step_bytes = T * H * BYTES_TOKEN_HEAD + H * 128 * 128 * 4
-    dec_bytes_step = wd.B * wd.H * (8 * wd.dk * wd.dv + 3 * 256 + 512 + 4 + 256)
-    dec_ms_step = dms / dsteps
-    dec_achieved = dec_bytes_step / (dec_ms_step / 1e3) / 1e9
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": PREFILL, "B": 1, "T": T, "H": H, "dk": 128, "dv": 128, "chunk": 64,
-                   "state": "fp32, S0 = 0", "parallelism": "replicas" if world > 1 else "single",
-                   "l2": f"inputs {in_bytes / 1e6:.0f} MB per step > 129 MB L2 (no flush)"},
-        "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic["kda_tc_prep"][0],
-                     "traffic_source": traffic["kda_tc_prep"][1], "peak_source": peak_src,
-                     "bytes_per_launch": dom[2], "launch_ms": dom[1]},
-        "step_roofline": {"bound": "hbm", "bytes_per_step": step_bytes,
-                          "achieved": step_bytes / (ms_step / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
-                          "frac": step_bytes / (ms_step / 1e3) / 1e9 / hbm,
-                          "tflops": T * H * FLOPS_TOKEN_HEAD / (ms_step / 1e3) / 1e12,
-                          "tflops_with_inverse": T * H * FLOPS_TOKEN_HEAD_INV / (ms_step / 1e3) / 1e12,
-                          "kernel_ms": {"kda_tc_prep_span": prep_ms, "state_pass_tail": chain_ms}},
-        "decode": {"workload": DECODE, "value": replica_throughput(1, dsteps, world, dms), "unit": "steps/s",
-                   "steps": dsteps, "ms_per_step": dec_ms_step,
-                   "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": dec_achieved,
-                                "peak": hbm, "unit": "GB/s", "frac": dec_achieved / hbm,
-                                "frac_of_nominal_8tbs": dec_achieved / HBM_NOMINAL_GBS,
-                                "traffic": traffic["kda_decode_kernel"][0],
-                                "traffic_source": traffic["kda_decode_kernel"][1],
-                                "bytes_per_launch": dec_bytes_step},
-                   "l2": "fp32 state 537 MB > L2; fresh token set per step"},
-        "verify": {"workload": "verify_bf16_N256_K8_H32_D128", "value": replica_throughput(1, 1, world, vms),
-                   "unit": "calls/s", "ms_per_call": vms,
-                   "roofline": {"bound": "hbm", "kernel": "kda_decode_multi_kernel",
-                                "achieved": vbytes / (vms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
-                                "frac": vbytes / (vms / 1e3) / 1e9 / hbm,
-                                "traffic": traffic["kda_decode_multi_kernel"][0],
-                                "traffic_source": traffic["kda_decode_multi_kernel"][1],
-                                "bytes_per_launch": vbytes}},
-        "few_heads_long": few,
-        "e2e": {"value": replica_throughput(T, e2e_steps, world, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipelining": "2 buffer sets; uploads on 2 copy streams overlap the previous step's prefill"},
-        "gpu_launches": launches * world,
-        "clocks": clk.summary(),
-    }
+        if "prefill" in parts:
+            ms, prep_ms, chain_ms, launches = time_prefill(kda, d, args.steps, args.warmup, stream, dev)
+            ms = barrier_max(ms, world, dev)
+            ms_step = ms / args.steps
+            # roofline of the dominant kernel: the chunk-prep launches, which run
+            # back to back on the caller's stream, timed from the first prep
+            # launch to the last one's end
+            prep_bytes = T * H * (3 * 256 + 512 + 4)               # q, k, v, log_alpha, beta read once
+            achieved = prep_bytes / (prep_ms / 1e3) / 1e9
+            step_bytes = T * H * BYTES_TOKEN_HEAD + H * STATE_BYTES
+            line.update({
+                "value": replica_throughput(T, args.steps, world, ms), "ms_per_step": ms_step,
+                "roofline": {"bound": "hbm", "kernel": "kda_tc_prep", "achieved": achieved, "peak": hbm,
+                             "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic["kda_tc_prep"][0],
+                             "traffic_source": traffic["kda_tc_prep"][1], "peak_source": peak_src,
+                             "bytes_per_launch": prep_bytes, "launch_ms": prep_ms},
+                "step_roofline": dict(step_roofline(step_bytes, ms_step, hbm),
+                                      tflops=T * H * FLOPS_TOKEN_HEAD / (ms_step / 1e3) / 1e12,
+                                      tflops_with_inverse=T * H * FLOPS_TOKEN_HEAD_INV / (ms_step / 1e3) / 1e12,
+                                      kernel_ms={"kda_tc_prep_span": prep_ms, "state_pass_tail": chain_ms}),
+                "gpu_launches": launches * world})
+            sync_barrier(world)
+        if "decode" in parts:
+            wd = inputs.WORKLOADS[DECODE]
+            dms, dsteps = time_decode(kda, wd, inputs, max(args.steps, args.decode_steps), args.warmup, stream, dev,
+                                      seed=rank)
+            dms = barrier_max(dms, world, dev)
+            dec_bytes_step = wd.B * wd.H * (8 * wd.dk * wd.dv + 3 * 256 + 512 + 4 + 256)
+            dec_ms_step = dms / dsteps
+            dec_achieved = dec_bytes_step / (dec_ms_step / 1e3) / 1e9
+            line["decode"] = {
+                "workload": DECODE, "value": replica_throughput(1, dsteps, world, dms), "unit": "steps/s",
+                "steps": dsteps, "ms_per_step": dec_ms_step,
+                "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": dec_achieved,
+                             "peak": hbm, "unit": "GB/s", "frac": dec_achieved / hbm,
+                             "frac_of_nominal_8tbs": dec_achieved / HBM_NOMINAL_GBS,
+                             "traffic": traffic["kda_decode_kernel"][0],
+                             "traffic_source": traffic["kda_decode_kernel"][1], "bytes_per_launch": dec_bytes_step},
+                "l2": "fp32 state 537 MB > L2; fresh token set per step"}
+            torch.cuda.empty_cache()
+        if "verify" in parts:
+            vms, vbytes = time_verify(kda, inputs, max(args.steps, 50), args.warmup, stream, dev, seed=rank)
+            vms = barrier_max(vms, world, dev)
+            line["verify"] = {
+                "workload": "verify_bf16_N256_K8_H32_D128", "value": replica_throughput(1, 1, world, vms),
+                "unit": "calls/s", "ms_per_call": vms,
+                "roofline": {"bound": "hbm", "kernel": "kda_decode_multi_kernel",
+                             "achieved": vbytes / (vms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                             "frac": vbytes / (vms / 1e3) / 1e9 / hbm,
+                             "traffic": traffic["kda_decode_multi_kernel"][0],
+                             "traffic_source": traffic["kda_decode_multi_kernel"][1], "bytes_per_launch": vbytes}}
+        if "few" in parts:
+            line["few_heads_long"] = time_few_heads(kda, inputs, max(3, args.steps // 4), args.warmup, stream, dev,
+                                                    seed=rank)
+        if "varlen" in parts:
+            line["varlen"] = time_prefill_workload(kda, inputs, "varlen_bf16_8seq_1K_32K_H32_D128",
+                                                   max(3, args.steps // 4), args.warmup, stream, dev, seed=rank)
+        if "long" in parts:
+            line["long_1M"] = time_prefill_workload(kda, inputs, "long_bf16_T1M_H32_D128", args.long_steps,
+                                                    min(args.warmup, 2), stream, dev, seed=rank)
+    line["clocks"] = clk.summary()
+    if "e2e" in parts:
+        e2e_steps = max(6, args.steps // 2)
+        e2e_ms, h2d, d2h = time_e2e(kda, d, e2e_steps, stream, dev)
+        e2e_ms = barrier_max(e2e_ms, world, dev)
+        link = link_bandwidth(dev)
+        e2e_step_ms = e2e_ms / e2e_steps
+        # with uploads and downloads on separate copy streams the copies of one
+        # step can at best run at the link's one-direction rates, in parallel
+        copy_floor_ms = max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9)) * 1e3
+        line["e2e"] = {"value": replica_throughput(T, e2e_steps, world, e2e_ms), "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms,
+                       "pipelining": "2 buffer sets; uploads on 2 copy streams overlap the previous step's prefill",
+                       "roofline": {"bound": "host link", "link_gbs": link, "copy_floor_ms": copy_floor_ms,
+                                    "frac": copy_floor_ms / e2e_step_ms}}
     if rank == 0 and not args.no_cpu_baseline:
         v, dt, cores, runs = oracle_sample(args.oracle_tokens, min_seconds=args.oracle_seconds, max_repeats=40)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -497,7 +580,13 @@ def main():
     ap.add_argument("--oracle-tokens", type=int, default=8192)
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--long-steps", type=int, default=3, help="timed steps of the 1,048,576-token prefill")
+    ap.add_argument("--parts", type=lambda x: [p for p in x.split(",") if p], default=None,
+                    help="comma list of " + ",".join(PARTS) + " (default: all)")
     args = ap.parse_args()
+    for p in args.parts or ():
+        if p not in PARTS:
+            ap.error(f"unknown part {p}")
     if args.warmup < 3 and args.impl == "kda":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

@@ -158,7 +158,9 @@ KDA_API kda_status kda_prefill_ckpt(const void* q, const void* k, const void* v,
 
 /*
  * Size of the fixed device array that kda_prefill_noalloc uses as its
- * workspace (bytes).  Every GPU that loads the library holds it until exit.
+ * workspace (bytes).  Under CUDA's lazy module loading (the default) a device
+ * reserves it when the first kda_prefill_noalloc call on that device loads
+ * the code that holds it, and keeps it until the process exits.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
@@ -175,10 +177,14 @@ KDA_API kda_status kda_prefill_ckpt(const void* q, const void* k, const void* v,
  * KDA_NOALLOC_SCRATCH_BYTES; the call allocates nothing.
  *   - Returns KDA_ERR_WORKSPACE, before launching anything, when
  *     kda_prefill_workspace_size(...) for the problem exceeds
- *     KDA_NOALLOC_SCRATCH_BYTES (e.g. more than about 580 chunk-head slots
- *     on the tensor-core path: H = 32 heads of ~1100 tokens).
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     KDA_NOALLOC_SCRATCH_BYTES (e.g. more than about 500 chunk-head slots
+ *     on the tensor-core path: H = 32 heads of ~900 tokens).
+ *   - Every call looks up the array's device address on the current device
+ *     (the device of the tensors must be current).  The first call on a
+ *     device also loads the code that holds the array, which reserves its
+ *     64 MiB there (KDA_ERR_CUDA if that fails): make that first call at
+ *     start-up, before a fixed-pool runtime takes its pool and before any
+ *     stream capture.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents (nothing in it needs to start at zero).  Calls that overlap
  *     on the GPU race on it: order them on one stream.

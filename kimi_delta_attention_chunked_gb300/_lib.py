@@ -94,6 +94,14 @@ def _stream(stream, device):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _on(device, fn, *args):
+    """Call a C entry point with ``device`` current: the library picks the SM
+    count, its internal stream and the no-workspace array from the current
+    device, which must be the one that holds the tensors."""
+    with torch.cuda.device(device):
+        return fn(*args)
+
+
 def _check_dev(name, t, device, dtype=None):
     if t is None:
         return
@@ -191,9 +199,9 @@ def _prefill(entry, q, k, v, log_alpha, beta, S0, cu_seqlens, cu_seqlens_host, c
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = getattr(lib, entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
-                             _ptr(cu_seqlens), host, n_seq, T, H, dk, dv, chunk, dt, _ptr(O), _ptr(S_final),
-                             _ptr(workspace), ws_bytes, _stream(stream, dev))
+    st = _on(dev, getattr(lib, entry), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+             _ptr(cu_seqlens), host, n_seq, T, H, dk, dv, chunk, dt, _ptr(O), _ptr(S_final),
+             _ptr(workspace), ws_bytes, _stream(stream, dev))
     if st != KDA_OK:
         raise KDAError(st, entry)
     return O, S_final
@@ -246,10 +254,10 @@ def kda_prefill_ckpt(q, k, v, log_alpha, beta, ckpt_every, S0=None, cu_seqlens=N
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.kda_prefill_ckpt(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
-                              _ptr(cu_seqlens), host, n_seq, T, H, dk, dv, chunk, dt, _ptr(O), _ptr(S_final),
-                              int(ckpt_every), _ptr(ckpt), ckpt.shape[0] if ckpt.numel() else 0,
-                              _ptr(workspace), ws_bytes, _stream(stream, dev))
+    st = _on(dev, lib.kda_prefill_ckpt, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+             _ptr(cu_seqlens), host, n_seq, T, H, dk, dv, chunk, dt, _ptr(O), _ptr(S_final),
+             int(ckpt_every), _ptr(ckpt), ckpt.shape[0] if ckpt.numel() else 0,
+             _ptr(workspace), ws_bytes, _stream(stream, dev))
     if st != KDA_OK:
         raise KDAError(st, "kda_prefill_ckpt")
     return O, S_final, ckpt
@@ -279,9 +287,9 @@ def kda_prefill_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, cu_s
     host = None
     if cu_seqlens_host is not None:
         host = (ctypes.c_int32 * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
-    st = lib.kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
-                                 _ptr(cu_seqlens), host, n_seq, T, H, dk, dv, chunk, _dtype_code(q.dtype),
-                                 _ptr(O), _ptr(S_final), _stream(stream, dev))
+    st = _on(dev, lib.kda_prefill_noalloc, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+             _ptr(cu_seqlens), host, n_seq, T, H, dk, dv, chunk, _dtype_code(q.dtype),
+             _ptr(O), _ptr(S_final), _stream(stream, dev))
     if st != KDA_OK:
         raise KDAError(st, "kda_prefill_noalloc")
     return O, S_final
@@ -314,8 +322,8 @@ def _decode(entry, q, k, v, log_alpha, beta, S, o, stream):
     _check_dev("S", S, dev, torch.float32)
     if o is None:
         o = torch.empty((N, H, dv), dtype=q.dtype, device=dev)
-    st = getattr(lib, entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S), N, H, dk, dv,
-                             _dtype_code(q.dtype), _ptr(o), _stream(stream, dev))
+    st = _on(dev, getattr(lib, entry), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S), N, H,
+             dk, dv, _dtype_code(q.dtype), _ptr(o), _stream(stream, dev))
     if st != KDA_OK:
         raise KDAError(st, entry)
     return o
@@ -343,8 +351,8 @@ def kda_decode_multi(q, k, v, log_alpha, beta, S, commit_len=None, o=None, want_
     _check_dev("commit_len", commit_len, dev, torch.int32)
     if o is None and want_o:
         o = torch.empty((N, K, H, dv), dtype=q.dtype, device=dev)
-    st = lib.kda_decode_multi(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S), _ptr(commit_len),
-                              N, K, H, dk, dv, _dtype_code(q.dtype), _ptr(o), _stream(stream, dev))
+    st = _on(dev, lib.kda_decode_multi, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S),
+             _ptr(commit_len), N, K, H, dk, dv, _dtype_code(q.dtype), _ptr(o), _stream(stream, dev))
     if st != KDA_OK:
         raise KDAError(st, "kda_decode_multi")
     return o

@@ -9,14 +9,15 @@
 // inputs and outputs as kda_prefill, and uses the array below as the
 // workspace.  It allocates nothing.
 //
-// Limits and sharing: the array is KDA_NOALLOC_SCRATCH_BYTES (64 MiB) and is
-// held by every GPU that loads the library until the process exits.  All
-// calls on a device share it, and it keeps the previous call's contents (the
-// prefill writes every byte it reads, so nothing needs clearing).  Calls that
-// overlap on the GPU (different streams, or different host threads, without
-// ordering) race on it.
-#include <mutex>
-
+// Limits and sharing: the array is KDA_NOALLOC_SCRATCH_BYTES (64 MiB).  With
+// CUDA's lazy module loading (the default) it is reserved on a device when the
+// first call there loads this file's module, and it is then held until the
+// process exits; a caller with a fixed memory budget should make one call at
+// start-up, before its runtime takes its pool.  All calls on a device share
+// the array, and it keeps the previous call's contents (the prefill writes
+// every byte it reads, so nothing needs clearing).  Calls that overlap on the
+// GPU (different streams, or different host threads, without ordering) race
+// on it.
 #include "common.cuh"
 
 namespace {
@@ -25,27 +26,19 @@ constexpr size_t kScratchBytes = KDA_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the array on the current device, looked up once per
-// device (host code cannot use the array's name as a device address).
+// Device address of the array on the current device.  Host code cannot use
+// the array's name as a device address, so it is looked up, with the device
+// current, on every call: a cached address would go stale if the device's
+// primary context were torn down and created again (the module, and with it
+// the array, is then loaded anew).
 kda_status scratch_for_current_device(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) {
-            (void)cudaGetLastError();
-            return KDA_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+        (void)cudaGetLastError();
+        return KDA_ERR_CUDA;
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return KDA_OK;
 }
 

@@ -72,12 +72,19 @@ constexpr int NTILES = DV / NT;
 
 // ---- per (chunk, head) workspace block: images of shared-memory operands
 constexpr uint32_t WS_A1 = 0;                // [Q'; W]       K-major SW128, 128 rows, K = 128 (2 panels)
-constexpr uint32_t WS_KR = 32768;            // K_restore^T   MN-major SW128, K = 64 rows, M = 128 (2 panels)
-constexpr uint32_t TILE_F32 = C * NT * 4;    // one d_v slice of U0 or O0: fp32 [C][NT], 16-byte chunk j of row r at j ^ (r % 8)
-constexpr uint32_t WS_UO = 49152;            // per d_v slice t: U0 at WS_UO + 2 t TILE_F32, O0 = M_qk U0 right after it
+constexpr uint32_t WS_KR = 32768;            // K_restore^T high part, MN-major SW128, K = 64 rows, M = 128 (2 panels)
+constexpr uint32_t WS_KRL = 49152;           //   ... low part, same layout, right after it
+constexpr uint32_t TILE_F32 = C * NT * 4;    // one d_v slice of U0 or O0, fp32, in the order the chain loads it
+constexpr uint32_t WS_UO = 65536;            // per d_v slice t: U0 at WS_UO + 2 t TILE_F32, O0 right after it
 constexpr uint32_t WS_AL = WS_UO + NTILES * 2 * TILE_F32;   // a_last fp32 [DK]
-constexpr uint32_t WS_BLOCK = 115712;        // 113 KiB
-__host__ __device__ constexpr uint32_t ws_u0(int t) { return WS_UO + 2u * TILE_F32 * (uint32_t)t; }
+constexpr uint32_t WS_BLOCK = 132096;        // 129 KiB
+// Byte offset of element (r, c) (row r < 64, column c < 64 of one d_v slice)
+// in a U0 / O0 tile: the 16 columns [16 g, 16 g + 16) of a row are the four
+// 16-byte pieces one state-pass thread loads, piece j of all 64 rows stored
+// together, so that the 32 lanes of a warp load 512 contiguous bytes.
+__host__ __device__ constexpr uint32_t uo_off(uint32_t r, uint32_t c) {
+    return ((((c >> 4) * 4u + ((c >> 2) & 3u)) * 64u + r) * 4u + (c & 3u)) * 4u;
+}
 
 // ---- prep kernel shared memory
 constexpr uint32_t K1_AG = 0;                // Gram A: 128 rows [q~ b0 | k^ b0 | q~ b1 | ...], K = 128
@@ -88,7 +95,8 @@ constexpr uint32_t K1_TOT = 106496;          // float [4][128] block totals of l
 constexpr uint32_t K1_FIRST = 108544;        // float [4][128] first-row log-decay of each block
 constexpr uint32_t K1_BETA = 110592;         // float [64]
 constexpr uint32_t K1_BAR = 110848;          // MMA mbarrier (8 B), TMEM address (4 B), Q_decay copy mbarrier at +16,
-                                             // input copy mbarrier at +24
+                                             // input copy mbarrier at +24, abort flag (4 B) at +32, drain
+                                             // mbarrier at +40
 constexpr uint32_t K1_NRM = 110912;          // fused prologue: float [q, k][channel half][64 rows] sums of squares
 constexpr uint32_t K1_BYTES = 111936;
 // aliases, valid once the Gram MMAs have completed
@@ -117,30 +125,29 @@ constexpr uint32_t K1_OUT_UO = 32768;        // [U0 | O0] of both d_v slices, th
 
 // ---- chain kernel shared memory
 constexpr int K2_NA = 2;                     // [Q'; W] stages (released as soon as the P product is done)
-constexpr int K2_NB = 2;                     // [K_restore^T | U0] stages (released after the state update)
-constexpr int K2_NO = 3;                     // O0 stages (read one chunk later, when O is formed)
+constexpr int K2_NB = 2;                     // K_restore^T stages, high and low part (released after the state update)
 constexpr uint32_t K2_ASTAGE = 32768;
-constexpr uint32_t K2_BSTAGE = 16384 + TILE_F32;
-constexpr uint32_t K2_OSTAGE = TILE_F32;     // O0 fp32; the bf16 output rows are staged over it
-constexpr uint32_t K2_B0 = K2_NA * K2_ASTAGE;            // B ring: K_restore^T at +0, U0 at +16384
-constexpr uint32_t K2_O0 = K2_B0 + K2_NB * K2_BSTAGE;    // O ring
-constexpr uint32_t K2_SB = K2_O0 + K2_NO * K2_OSTAGE;    // S_in bf16, MN-major SW128, K = 128 rows, N = 64
-constexpr uint32_t K2_UB = K2_SB + 16384;                // [U_hi | U_lo] bf16, MN-major SW128, K = 64 rows, N = 2 x 64
-constexpr uint32_t K2_BAR = K2_UB + 16384;               // full / empty A, B, O; p; s; TMEM address
-constexpr uint32_t K2_BYTES = K2_BAR + 192;
-constexpr uint32_t K2_TMEM_COLS = 256;       // S [0, 64), X [64, 128), P (chunk parity) [128, 192), [192, 256)
+constexpr uint32_t K2_BSTAGE = 32768;
+constexpr uint32_t K2_B0 = K2_NA * K2_ASTAGE;            // B ring: high part at +0, low part at +16384
+constexpr uint32_t K2_SB = K2_B0 + K2_NB * K2_BSTAGE;    // [S_hi | S_lo] bf16, MN-major SW128, K = 128 rows, N = 2 x 64
+constexpr uint32_t K2_UB = K2_SB + 32768;                // [U_hi | U_lo] bf16, MN-major SW128, K = 64 rows, N = 2 x 64
+constexpr uint32_t K2_OS = K2_UB + 16384;                // one chunk's bf16 output rows [64][64] (16-byte pieces swizzled)
+constexpr uint32_t K2_BAR = K2_OS + 8192;                // full / empty A, B; p; s; drain; TMEM address; abort flag
+constexpr uint32_t K2_BYTES = K2_BAR + 128;
+constexpr uint32_t K2_TMEM_COLS = 512;       // S [0, 64), X [64, 128), P of even chunks [128, 256), of odd [256, 384)
 
-static_assert(K2_BSTAGE % 1024 == 0 && K2_O0 % 1024 == 0 && K2_SB % 1024 == 0 && K2_UB % 1024 == 0,
-              "SW128 operands are 1024-byte aligned");
-static_assert(ws_u0(0) == WS_KR + 16384, "slice 0's [K_restore^T | U0] is one contiguous copy");
+static_assert(K2_B0 % 1024 == 0 && K2_SB % 1024 == 0 && K2_UB % 1024 == 0, "SW128 operands are 1024-byte aligned");
+static_assert(WS_KRL == WS_KR + 16384, "both parts of K_restore^T are one contiguous copy");
 static_assert(K1_AIL + 16384 <= K1_BWU, "[INV; X] must stay inside the alias region");
 static_assert(K1_ML + 16384 <= K1_BWU && K1_IL + 8192 <= K1_IS, "X operands stay inside the alias region");
 static_assert(K1_OUT_UO + NTILES * 2 * TILE_F32 <= K1_TOT && K1_OUT_A1 + 32768 <= K1_OUT_UO, "output images");
+static_assert(K1_BAR + 48 <= K1_NRM, "prep barriers and flags");
 static_assert(K1_SK + 16384 <= K1_BWU && (K1_BWU + 16384) % 1024 == 0, "input tiles");
 static_assert(K1_IS + 64 * LDS_ * 4 <= K1_XS && K1_XS + 4096 <= K1_MH && 16384 + 8192 <= K1_XS,
               "Q_decay rows land in the free L / INV region while the last MMA runs");
 static_assert(WS_BLOCK % 1024 == 0 && WS_AL + DK * 4 <= WS_BLOCK, "workspace block");
 static_assert(K2_BYTES + 1024 + 256 <= 232448, "chain smem");
+static_assert(K2_BAR + 11 * 8 + 8 <= K2_BYTES, "chain barriers and flags");
 static_assert(2 * (K1_BYTES + 1024 + 1024) <= 233472, "prep must fit two CTAs per SM");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -148,6 +155,14 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 __device__ __forceinline__ void st_shared_u32(uint8_t* p, uint32_t x) { *reinterpret_cast<uint32_t*>(p) = x; }
+
+// (a, b) as a high / low pair of packed bf16x2 words: high = a, b truncated to
+// bf16, low = bf16 of the remainders (see split_pack8).
+__device__ __forceinline__ void split_pack2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+    hi = __byte_perm(ua, ub, 0x7632);
+    lo = kda::pack_bf16x2(a - __uint_as_float(ua & 0xFFFF0000u), b - __uint_as_float(ub & 0xFFFF0000u));
+}
 
 // x = hi + lo with hi = x truncated to bf16 and lo = bf16(x - hi): the pair
 // carries ~16 significant bits (|x - hi| < 2^-7 |x|, and lo is rounded to
@@ -350,6 +365,8 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + K1_BAR + 8);
     uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + K1_BAR + 16);
     uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + K1_BAR + 24);
+    volatile int* abort_f = reinterpret_cast<volatile int*>(sm + K1_BAR + 32);
+    uint64_t* bar_drain = reinterpret_cast<uint64_t*>(sm + K1_BAR + 40);
     if (w == 0) {
         kda::tmem_alloc(tmem_slot, K1_TMEM_COLS);
         kda::tmem_relinquish();
@@ -358,10 +375,21 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         kda::mbar_init(bar, 1);
         kda::mbar_init(bar_q, 1);
         kda::mbar_init(bar_ld, 1);
+        kda::mbar_init(bar_drain, 1);
         kda::fence_barrier_init();
+        *abort_f = 0;
     }
     uint32_t n_done = 0;                          // items finished by this CTA (bar_q parity)
     uint32_t bar_phase = 0;                       // completed phases of bar (three per item)
+    uint32_t n_loads = 0, n_qloads = 0;           // input / Q_decay copy phases issued (thread 0)
+    // Bounded wait; once it runs out (or another thread's did) the CTA stops
+    // taking items and drains what it has in flight before it exits.
+    auto wait = [&](uint64_t* b, uint32_t parity) {
+        if (!kda::mbar_wait_or_abort(b, parity, kda::kWaitCycles, abort_f)) {
+            kda::record_status(status, kda::kDevTimeout);
+            *abort_f = 1;
+        }
+    };
     kda::tc_fence_before();
     __syncthreads();
     kda::tc_fence_after();
@@ -388,10 +416,11 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             kda::tma_load_3d(sm + K1_SK, &tm_k, 0, h, tok0, bar_ld);
             kda::tma_load_3d(sm + K1_BWU + 16384, &tm_v, 0, h, tok0, bar_ld);
             kda::tma_load_3d(sm + K1_BWU + 16384 + 8192, &tm_v, 64, h, tok0, bar_ld);
+            ++n_loads;
         }
         // beta of row 16 b + (lane % 16): one value per lane
         float bt = beta[((size_t)tok0 + min(16 * b + (lane & 15), nrows - 1)) * H + h];
-        if (!kda::mbar_wait(bar_ld, n_done & 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        wait(bar_ld, n_done & 1);
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
             const int r = 16 * b + rr;
@@ -414,6 +443,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) = make_uint4(0u, 0u, 0u, 0u);
         }
         __syncthreads();                           // the input tiles are in registers
+        if (*abort_f) break;                       // read after the barrier: the same for every thread
         float* nrm = reinterpret_cast<float*>(sm + K1_NRM);
         if (PROLOGUE) {
             // fused prologue: gates from their pre-activations; squared norms of
@@ -499,8 +529,15 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 // K_decay -> left half of the [K_decay | V] operand
                 st_shared_u32(sm + K1_BWU + kda::sw128(r, ch, 64),
                               kda::pack_bf16x2(kf.x * e0 * ap0, kf.y * e1 * ap1));
-                // K_restore -> K_restore^T image (MN-major: row = token, contiguous = channel)
-                *reinterpret_cast<uint32_t*>(blk + WS_KR + kda::sw128(r, ch, 64)) = kda::pack_bf16x2(kt0 * R0, kt1 * R1);
+                // K_restore -> K_restore^T images, high and low bf16 parts (MN-major: row =
+                // token, contiguous = channel)
+                {
+                    uint32_t krh, krl;
+                    split_pack2(kt0 * R0, kt1 * R1, krh, krl);
+                    const uint32_t off = kda::sw128(r, ch, 64);
+                    *reinterpret_cast<uint32_t*>(blk + WS_KR + off) = krh;
+                    *reinterpret_cast<uint32_t*>(blk + WS_KRL + off) = krl;
+                }
             }
             // tiles m > b hold this block's column factors times a(p_m) / a(p_b) <= 1
             // (a rolled loop keeps this replicated part of the code small)
@@ -534,7 +571,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             kda::umma_commit(bar);
         }
-        if (!kda::mbar_wait(bar, bar_phase & 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        wait(bar, bar_phase & 1);
         ++bar_phase;
         kda::tc_fence_after();
 
@@ -639,7 +676,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
             kda::umma_commit(bar);
         }
-        if (!kda::mbar_wait(bar, bar_phase & 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        wait(bar, bar_phase & 1);
         ++bar_phase;
         kda::tc_fence_after();
         // [INV; X] Diag(beta) -> 128-row K-major A operand as high + low bf16 parts
@@ -696,8 +733,9 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             kda::mbar_arrive_expect_tx(bar_q, 16384);
             kda::bulk_g2s(sm + K1_OUT_A1, blk + WS_A1, 8192, bar_q);
             kda::bulk_g2s(sm + K1_OUT_A1 + 16384, blk + WS_A1 + 16384, 8192, bar_q);
+            ++n_qloads;
         }
-        if (!kda::mbar_wait(bar, bar_phase & 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        wait(bar, bar_phase & 1);
         ++bar_phase;
         kda::tc_fence_after();
 
@@ -715,7 +753,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     *reinterpret_cast<uint4*>(sm + K1_OUT_A1 + kda::sw128(64 + r, 32 * cb + 8 * u, 128)) = pack8(x + 8 * u);
             }
         } else if (w == 2 || w == 3) {             // Q' = Q_decay - M_qk W -> rows 0..63 of [Q'; W]
-            if (!kda::mbar_wait(bar_q, n_done & 1, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+            wait(bar_q, n_done & 1);
 #pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
                 float x[32];
@@ -742,11 +780,12 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 float x[32];
                 kda::tmem_ld32(t_row + 32 * cb, x);
                 kda::tmem_wait_ld();
-                const int j = 32 * cb, tile = j / NT;
-                float4* dst = reinterpret_cast<float4*>(sm + K1_OUT_UO + (ws_u0(tile) - WS_UO) + part + r * NT * 4);
+                const int tile = (32 * cb) / NT, c0 = (32 * cb) % NT;
+                uint8_t* dst = sm + K1_OUT_UO + 2 * TILE_F32 * tile + part;
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    dst[((j % NT) / 4 + u) ^ (r & 7)] = make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+                    *reinterpret_cast<float4*>(dst + uo_off(r, c0 + 4 * u)) =
+                        make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
             }
         }
         kda::fence_proxy_async_smem();
@@ -760,7 +799,20 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         ++n_done;
     }
-    if (tid == 0) kda::bulk_wait_all();           // the workspace is complete when the kernel ends
+    if (tid == 0) {
+        if (*abort_f) {
+            // a wait ran out: let the copies and MMAs already issued finish
+            // (bounded again) before the shared memory and TMEM are released
+            if (n_loads) (void)kda::mbar_wait(bar_ld, (n_loads - 1) & 1, kda::kWaitCycles);
+            if (n_qloads) (void)kda::mbar_wait(bar_q, (n_qloads - 1) & 1, kda::kWaitCycles);
+            kda::umma_commit(bar_drain);           // arrives once every MMA issued so far is done
+            (void)kda::mbar_wait(bar_drain, 0, kda::kWaitCycles);
+        }
+        kda::bulk_wait_all();                      // the workspace is complete when the kernel ends
+    }
+    kda::tc_fence_before();
+    __syncthreads();
+    kda::tc_fence_after();
     if (w == 0) kda::tmem_dealloc(tmem, K1_TMEM_COLS);
 }
 
@@ -769,23 +821,31 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 //   [0, 64)      S, the fp32 state slice (TMEM lane = key channel)
 //   [64, 128)    X, the low-part share K_restore^T U_lo of the state update,
 //                folded into S when the state is next read
-//   [128, 192)   P = [Q'; W] S_in: lanes 0..63 Q' S_in, lanes 64..127 W S_in
-// MMAs per chunk (12 instructions):
-//   P        = [Q'; W] S_in                 K = 128, N = 64   -> commit(p)
-//   [S | X] += K_restore^T [U_hi | U_lo]    K = 64,  N = 128  -> commit(s)
-// with U = U0 - W S_in and O = Q' S_in + O0.  Q' = Q_decay - M_qk W and
-// O0 = M_qk U0 come from the prep kernel, so O = Q_decay S_in + M_qk U needs no
-// product of its own here.
-// Operands stream through three rings filled by bulk copies: [Q'; W] (needed
-// first, released when P is done), [K_restore^T | U0] (released after the
-// state update) and O0 (used one chunk later); a_last is read into registers
-// one chunk ahead.  P alternates between two TMEM buffers, so the output rows
-// of chunk c are formed while chunk c + 1 runs, off the sequential path.
+//   [128, 256)   P of even chunks, [256, 384) P of odd chunks:
+//                P = [Q'; W] [S_hi | S_lo]: columns 0..63 against the high
+//                part of S_in, 64..127 against its low part; lanes 0..63
+//                Q' S_in, lanes 64..127 W S_in
+// MMAs per chunk (16 instructions):
+//   P        = [Q'; W] [S_hi | S_lo]                        K = 128, N = 128 -> commit(p)
+//   [S | X] += K_hi^T [U_hi | U_lo] + K_lo^T [U_hi | U_lo]  K = 64,  N = 128 -> commit(s)
+// with U = U0 - W S_in, O = Q' S_in + O0, and S_in, K_restore and U each
+// carried as a high and a low bf16 part (x = hi + lo, |lo| <= 2^-8 |x|), so
+// that no operand of the sequential pass is rounded to a single bf16: the
+// pass carries its error from chunk to chunk, and at the no-decay end of the
+// gate range it would otherwise add up over the sequence.  Q' = Q_decay -
+// M_qk W and O0 = M_qk U0 come from the prep kernel, so O = Q_decay S_in +
+// M_qk U needs no product of its own here.
+// [Q'; W] and K_restore^T stream through two rings filled by bulk copies;
+// U0, O0 and a_last are loaded straight into the registers of the threads
+// that use them, a chunk ahead.  P alternates between two TMEM buffers, so the
+// output rows of chunk c are formed while chunk c + 1 runs, off the sequential
+// path.
 // Warp roles:
 //   warps 0-15 conversion warps; warp w reads TMEM lanes 32 (w % 4) .. +31 and
 //              columns 16 (w / 4) .. +15 of each 64-wide block (four warps per
 //              sub-partition, so that their latencies overlap).
-//              - all 16: S_in = S + X -> bf16 operand; then S <- Diag(a_last) S_in, X <- 0
+//              - all 16: S_in = S + X -> high/low bf16 operand; then
+//                S <- Diag(a_last) S_in, X <- 0
 //              - lanes 64..127 (w % 4 = 2, 3): U = U0 - W S_in -> high/low bf16 operand
 //              - lanes 0..63 (w % 4 = 0, 1): O rows of the previous chunk =
 //                Q' S_in + O0, staged in shared memory and stored row by row
@@ -793,6 +853,9 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 //   warp 17    lane 0 issues the bulk copies
 // Named barriers (warps 0-16): 1 = S_in ready; 2 = conversion warps arrive, the
 // issuer waits (U ready, state rescaled); 3 = the eight O warps (output staging).
+// A wait that runs out sets the CTA's abort flag: from then on no copy or MMA
+// is issued, every other wait returns at once, and before the CTA exits the
+// copies and MMAs already in flight are waited for (bounded again).
 constexpr int K2_CONV_WARPS = 16;
 constexpr int K2_CW = NT / (K2_CONV_WARPS / 4);   // state columns per conversion warp
 constexpr int K2_THREADS = 32 * (K2_CONV_WARPS + 2);
@@ -806,9 +869,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 }
 __device__ __forceinline__ void named_bar_arrive(int id, int count) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(kda::smem_u32(bar)) : "memory");
 }
 
 __global__ void __launch_bounds__(K2_THREADS, 1)
@@ -856,66 +916,60 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     uint64_t* emptyA = fullA + K2_NA;
     uint64_t* fullB = emptyA + K2_NA;
     uint64_t* emptyB = fullB + K2_NB;
-    uint64_t* fullO = emptyB + K2_NB;
-    uint64_t* emptyO = fullO + K2_NO;
-    uint64_t* bar_p = emptyO + K2_NO;
+    uint64_t* bar_p = emptyB + K2_NB;
     uint64_t* bar_s = bar_p + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 1);
+    uint64_t* bar_drain = bar_s + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + 1);
+    volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
     if (w == 0) {
         kda::tmem_alloc(tmem_slot, K2_TMEM_COLS);
         kda::tmem_relinquish();
     }
     if (tid == 0) {
+        // a stage is free once the MMAs that read it are done (one commit each)
         for (int s = 0; s < K2_NA; ++s) { kda::mbar_init(fullA + s, 1); kda::mbar_init(emptyA + s, 1); }
-        // a B stage is free once the state update has read it (one commit) and
-        // the eight warps of lanes 64..127 have read their U0 rows
-        for (int s = 0; s < K2_NB; ++s) { kda::mbar_init(fullB + s, 1); kda::mbar_init(emptyB + s, 9); }
-        // an O stage is free once the eight warps of lanes 0..63 have stored its rows
-        for (int s = 0; s < K2_NO; ++s) { kda::mbar_init(fullO + s, 1); kda::mbar_init(emptyO + s, 8); }
+        for (int s = 0; s < K2_NB; ++s) { kda::mbar_init(fullB + s, 1); kda::mbar_init(emptyB + s, 1); }
         kda::mbar_init(bar_p, 1);
         kda::mbar_init(bar_s, 1);
+        kda::mbar_init(bar_drain, 1);
         kda::fence_barrier_init();
+        *abort_f = 0;
     }
     kda::tc_fence_before();
     __syncthreads();
     kda::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     auto wait = [&](uint64_t* b, uint32_t parity) {
-        if (!kda::mbar_wait(b, parity, kda::kWaitCycles)) kda::record_status(status, kda::kDevTimeout);
+        if (!kda::mbar_wait_or_abort(b, parity, kda::kWaitCycles, abort_f)) {
+            kda::record_status(status, kda::kDevTimeout);
+            *abort_f = 1;
+        }
     };
 
     if (w == K2_PRODUCER_WARP) {
         // ---------------- bulk copies, in the order the chunks need them
         if (lane == 0) {
-            auto issueA = [&](int k) {
-                const int st = k % K2_NA;
-                if (k >= K2_NA) wait(emptyA + st, (uint32_t)(((k - K2_NA) / K2_NA) & 1));
-                kda::mbar_arrive_expect_tx(fullA + st, K2_ASTAGE);
-                kda::bulk_g2s(sm + st * K2_ASTAGE, block_of(k) + WS_A1, K2_ASTAGE, fullA + st);
-            };
-            auto issueB = [&](int k) {
-                const int st = k % K2_NB;
-                if (k >= K2_NB) wait(emptyB + st, (uint32_t)(((k - K2_NB) / K2_NB) & 1));
-                uint8_t* dst = sm + K2_B0 + st * K2_BSTAGE;
-                const uint8_t* src = block_of(k);
-                kda::mbar_arrive_expect_tx(fullB + st, K2_BSTAGE);
-                if (tile == 0) {
-                    kda::bulk_g2s(dst, src + WS_KR, K2_BSTAGE, fullB + st);
-                } else {
-                    kda::bulk_g2s(dst, src + WS_KR, 16384, fullB + st);
-                    kda::bulk_g2s(dst + 16384, src + ws_u0(tile), TILE_F32, fullB + st);
-                }
-            };
-            auto issueO = [&](int k) {
-                const int st = k % K2_NO;
-                if (k >= K2_NO) wait(emptyO + st, (uint32_t)(((k - K2_NO) / K2_NO) & 1));
-                kda::mbar_arrive_expect_tx(fullO + st, K2_OSTAGE);
-                kda::bulk_g2s(sm + K2_O0 + st * K2_OSTAGE, block_of(k) + ws_u0(tile) + TILE_F32, K2_OSTAGE, fullO + st);
-            };
-            for (int k = 0; k < nloc; ++k) {
-                issueA(k);
-                issueB(k);
-                issueO(k);
+            int nA = 0, nB = 0;                             // copies issued into each ring
+            for (int k = 0; k < nloc && !*abort_f; ++k) {
+                const int sa = k % K2_NA;
+                if (k >= K2_NA) wait(emptyA + sa, (uint32_t)(((k - K2_NA) / K2_NA) & 1));
+                if (*abort_f) break;
+                kda::mbar_arrive_expect_tx(fullA + sa, K2_ASTAGE);
+                kda::bulk_g2s(sm + sa * K2_ASTAGE, block_of(k) + WS_A1, K2_ASTAGE, fullA + sa);
+                ++nA;
+                const int sb = k % K2_NB;
+                if (k >= K2_NB) wait(emptyB + sb, (uint32_t)(((k - K2_NB) / K2_NB) & 1));
+                if (*abort_f) break;
+                kda::mbar_arrive_expect_tx(fullB + sb, K2_BSTAGE);
+                kda::bulk_g2s(sm + K2_B0 + sb * K2_BSTAGE, block_of(k) + WS_KR, K2_BSTAGE, fullB + sb);
+                ++nB;
+            }
+            if (*abort_f) {
+                // the last copy into each stage completes that stage's newest phase
+                for (int k = max(0, nA - K2_NA); k < nA; ++k)
+                    (void)kda::mbar_wait(fullA + k % K2_NA, (uint32_t)((k / K2_NA) & 1), kda::kWaitCycles);
+                for (int k = max(0, nB - K2_NB); k < nB; ++k)
+                    (void)kda::mbar_wait(fullB + k % K2_NB, (uint32_t)((k / K2_NB) & 1), kda::kWaitCycles);
             }
         }
     } else if (w == K2_ISSUER_WARP) {
@@ -927,30 +981,30 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             if (lane == 0) wait(fullA + sa, (uint32_t)((c / K2_NA) & 1));
             __syncwarp();
             named_bar_sync(1, K2_SYNC);
-            if (lane == 0) {                                // P = [Q'; W] S_in
+            if (lane == 0 && !*abort_f) {                   // P = [Q'; W] [S_hi | S_lo]
                 kda::tc_fence_after();
                 const uint32_t sA1 = kda::smem_u32(sm + sa * K2_ASTAGE);
-                const uint32_t idesc = kda::idesc_bf16(128, NT, 0, 1);
+                const uint32_t idesc = kda::idesc_bf16(128, 2 * NT, 0, 1);
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     const uint64_t ad = kda::sw128_desc(sA1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
                     const uint64_t bd = kda::sw128_desc(sSB + s * 2048, 16384, 1024);
-                    kda::umma_bf16(tmem + 128 + 64 * (c & 1), ad, bd, idesc, s > 0 ? 1u : 0u);
+                    kda::umma_bf16(tmem + 128 + 128 * (c & 1), ad, bd, idesc, s > 0 ? 1u : 0u);
                 }
                 kda::umma_commit(bar_p);
                 kda::umma_commit(emptyA + sa);
-                wait(fullB + sb, (uint32_t)((c / K2_NB) & 1));
             }
+            if (lane == 0) wait(fullB + sb, (uint32_t)((c / K2_NB) & 1));
             __syncwarp();
             named_bar_sync(2, K2_SYNC);
-            if (lane == 0) {                                // [S | X] += K_restore^T [U_hi | U_lo]
+            if (lane == 0 && !*abort_f) {                   // [S | X] += K_hi^T [U_hi | U_lo] + K_lo^T [U_hi | U_lo]
                 kda::tc_fence_after();
                 const uint32_t sKR = kda::smem_u32(sm + K2_B0 + sb * K2_BSTAGE);
                 const uint32_t id_s = kda::idesc_bf16(128, 2 * NT, 1, 1);
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t ad = kda::sw128_desc(sKR + s * 2048, 8192, 1024);
-                    const uint64_t bd = kda::sw128_desc(sUB + s * 2048, 8192, 1024);
+                for (int s = 0; s < 8; ++s) {
+                    const uint64_t ad = kda::sw128_desc(sKR + (s >> 2) * 16384 + (s & 3) * 2048, 8192, 1024);
+                    const uint64_t bd = kda::sw128_desc(sUB + (s & 3) * 2048, 8192, 1024);
                     kda::umma_bf16(tmem, ad, bd, id_s, 1u);
                 }
                 kda::umma_commit(bar_s);
@@ -958,6 +1012,11 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             }
             __syncwarp();
         }
+        if (lane == 0) {                                    // every MMA done before TMEM is released
+            kda::umma_commit(bar_drain);
+            (void)kda::mbar_wait(bar_drain, 0, kda::kWaitCycles);
+        }
+        __syncwarp();
     } else {
         // ---------------- conversion warps
         const int quad = w & 3, grp = w >> 2;
@@ -965,33 +1024,40 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         const int col0 = K2_CW * grp;                           // this warp's first column of the slice
         const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
         const uint32_t tS = tmem + lane_off + col0;             // this warp's state columns (X at +64)
-        const uint32_t tP = tmem + lane_off + 128 + col0;       // ... of P (buffer of chunk parity at +64)
+        const uint32_t tP = tmem + lane_off + 128 + col0;       // ... of P (buffer of chunk parity at +128)
+        const bool u_rows = quad >= 2;                          // lanes 64..127: U; lanes 0..63: O
+        // this thread's 16 values of U0 (U rows) or O0 (O rows) of local chunk c
+        auto load_uo = [&](int c, float* dst) {
+            const uint8_t* base = block_of(c) + WS_UO + 2 * TILE_F32 * tile + (u_rows ? 0u : TILE_F32);
+            const int r = u_rows ? row - 64 : row;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 x = *reinterpret_cast<const float4*>(base + uo_off(r, col0 + 4 * j));
+                dst[4 * j] = x.x; dst[4 * j + 1] = x.y; dst[4 * j + 2] = x.z; dst[4 * j + 3] = x.w;
+            }
+        };
         // O rows of chunk co (lanes 0..63 warps): P of that chunk is complete (the
-        // state update issued after it is); its O0 stage is staged over and stored
-        auto out_rows = [&](int co) {
-            const int so = co % K2_NO;
-            wait(fullO + so, (uint32_t)((co / K2_NO) & 1));
+        // state update issued after it is); staged in shared memory and stored
+        auto out_rows = [&](int co, const float* o0) {
             kda::tc_fence_after();
-            float ph[K2_CW];
-            kda::tmem_ld16(tP + 64 * (co & 1), ph);
+            float ph[K2_CW], pl[K2_CW];
+            kda::tmem_ld16(tP + 128 * (co & 1), ph);
+            kda::tmem_ld16(tP + 128 * (co & 1) + 64, pl);
             kda::tmem_wait_ld();
-            uint8_t* o0b = sm + K2_O0 + so * K2_OSTAGE;
-            const float4* o0 = reinterpret_cast<const float4*>(o0b + row * NT * 4);
             uint4 ov[K2_CW / 8];
 #pragma unroll
             for (int cc = 0; cc < K2_CW / 8; ++cc) {
-                const int j = (col0 + 8 * cc) / 4;
-                const float4 x0 = o0[j ^ (row & 7)], x1 = o0[(j + 1) ^ (row & 7)];
-                float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                float f[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) f[u] += ph[8 * cc + u];
+                for (int u = 0; u < 8; ++u) f[u] = o0[8 * cc + u] + (ph[8 * cc + u] + pl[8 * cc + u]);
                 ov[cc] = pack8(f);
             }
-            named_bar_sync(3, K2_CONV_WARPS * 16);             // every O warp has read O0
+            uint8_t* ost = sm + K2_OS;
+            named_bar_sync(3, K2_CONV_WARPS * 16);             // every O warp is done with the last staged rows
 #pragma unroll
             for (int cc = 0; cc < K2_CW / 8; ++cc) {
-                const int k = (col0 + 8 * cc) / 8;               // 16-byte chunk of the 128-byte row
-                *reinterpret_cast<uint4*>(o0b + row * 128 + ((k ^ (row & 7)) << 4)) = ov[cc];
+                const int k = (col0 + 8 * cc) / 8;               // 16-byte piece of the 128-byte row
+                *reinterpret_cast<uint4*>(ost + row * 128 + ((k ^ (row & 7)) << 4)) = ov[cc];
             }
             named_bar_sync(3, K2_CONV_WARPS * 16);             // the staged tile is complete
             const int wo = (grp << 1) | quad;                    // 0..7: rows 8 wo .. 8 wo + 7
@@ -1001,14 +1067,12 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 const int rr = 8 * wo + i;
                 if (write_o && rr < valid) {
                     const uint32_t x = *reinterpret_cast<const uint32_t*>(
-                        o0b + rr * 128 + (((lane >> 2) ^ (rr & 7)) << 4) + 4 * (lane & 3));
+                        ost + rr * 128 + (((lane >> 2) ^ (rr & 7)) << 4) + 4 * (lane & 3));
                     *reinterpret_cast<uint32_t*>(O + ((size_t)(bos + (cb + co) * C + rr) * H + h) * DV + tile * NT +
                                                  2 * lane) = x;
                 }
             }
             kda::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(emptyO + so);
         };
         {
             // initial state slice -> TMEM (X = 0)
@@ -1037,10 +1101,15 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             named_bar_sync(1, K2_SYNC);
         }
         float al_next = nloc > 0 ? reinterpret_cast<const float*>(block_of(0) + WS_AL)[row] : 1.f;
+        float uo_prev[K2_CW];                                   // O rows: O0 of the previous chunk
+#pragma unroll
+        for (int u = 0; u < K2_CW; ++u) uo_prev[u] = 0.f;
         for (int c = 0; c < nloc; ++c) {
             const float al = al_next;
             if (c + 1 < nloc) al_next = reinterpret_cast<const float*>(block_of(c + 1) + WS_AL)[row];
-            // ---- S_in = S + X -> bf16 operand
+            float uo[K2_CW];                                    // U0 (U rows) or O0 (O rows) of this chunk
+            load_uo(c, uo);
+            // ---- S_in = S + X -> high/low bf16 operand
             if (c > 0) wait(bar_s, (uint32_t)((c - 1) & 1));
             kda::tc_fence_after();
             float s[K2_CW], x[K2_CW];
@@ -1050,8 +1119,12 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
 #pragma unroll
             for (int u = 0; u < K2_CW; ++u) s[u] += x[u];
 #pragma unroll
-            for (int cc = 0; cc < K2_CW / 8; ++cc)
-                *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(row, col0 + 8 * cc, 128)) = pack8(s + 8 * cc);
+            for (int cc = 0; cc < K2_CW / 8; ++cc) {
+                uint4 hi, lo;
+                split_pack8(s + 8 * cc, hi, lo);
+                *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(row, col0 + 8 * cc, 128)) = hi;
+                *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(row, NT + col0 + 8 * cc, 128)) = lo;
+            }
             kda::fence_proxy_async_smem();
             kda::tc_fence_before();
             named_bar_sync(1, K2_SYNC);
@@ -1063,26 +1136,21 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             kda::tmem_st16(tS, s);
             kda::tmem_st16(tS + 64, x);
             kda::tmem_wait_st();
-            if (quad >= 2) {
+            if (u_rows) {
                 // ---- U = U0 - W S_in -> high/low bf16 operand
-                const int sb = c % K2_NB;
-                const uint8_t* bst = sm + K2_B0 + sb * K2_BSTAGE;
-                wait(fullB + sb, (uint32_t)((c / K2_NB) & 1));
                 wait(bar_p, (uint32_t)(c & 1));
                 kda::tc_fence_after();
                 const int r = row - 64;
-                float ph[K2_CW];
-                kda::tmem_ld16(tP + 64 * (c & 1), ph);
+                float ph[K2_CW], pl[K2_CW];
+                kda::tmem_ld16(tP + 128 * (c & 1), ph);
+                kda::tmem_ld16(tP + 128 * (c & 1) + 64, pl);
                 kda::tmem_wait_ld();
-                const float4* u0 = reinterpret_cast<const float4*>(bst + 16384 + r * NT * 4);
 #pragma unroll
                 for (int cc = 0; cc < K2_CW / 8; ++cc) {
-                    const int j = (col0 + 8 * cc) / 4;              // 16-byte chunk of the row
-                    float4 x0 = u0[j ^ (r & 7)], x1 = u0[(j + 1) ^ (r & 7)];
-                    if (run_map) { x0 = make_float4(0.f, 0.f, 0.f, 0.f); x1 = x0; }
-                    float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    float f[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) f[u] -= ph[8 * cc + u];
+                    for (int u = 0; u < 8; ++u)
+                        f[u] = (run_map ? 0.f : uo[8 * cc + u]) - (ph[8 * cc + u] + pl[8 * cc + u]);
                     uint4 hi, lo;
                     split_pack8(f, hi, lo);
                     const uint32_t off = kda::sw128(r, col0 + 8 * cc, 64);
@@ -1092,17 +1160,17 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 kda::fence_proxy_async_smem();
                 kda::tc_fence_before();
                 named_bar_arrive(2, K2_SYNC);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(emptyB + sb);         // this warp's U0 rows are read
             } else {
                 kda::tc_fence_before();
                 named_bar_arrive(2, K2_SYNC);
-                if (c > 0) out_rows(c - 1);                     // the previous chunk's output
+                if (c > 0) out_rows(c - 1, uo_prev);            // the previous chunk's output
+#pragma unroll
+                for (int u = 0; u < K2_CW; ++u) uo_prev[u] = uo[u];
             }
         }
         if (nloc > 0) wait(bar_s, (uint32_t)((nloc - 1) & 1));
         kda::tc_fence_after();
-        if (quad < 2 && nloc > 0) out_rows(nloc - 1);
+        if (!u_rows && nloc > 0) out_rows(nloc - 1, uo_prev);
         const bool end_ckpt = ckpt_every > 0 && nloc > 0 && cb + nloc == nch && len % ckpt_every == 0;
         if (S_final || end_ckpt) {
             float s[K2_CW], x[K2_CW];

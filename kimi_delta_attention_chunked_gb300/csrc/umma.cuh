@@ -57,6 +57,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
     return true;
 }
 
+// As mbar_wait, but also gives up as soon as *abort is non-zero: once one
+// thread of a CTA has given up waiting, the CTA issues no further
+// asynchronous work, so the other threads' waits would only run out too.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, long long limit,
+                                                   const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort || clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

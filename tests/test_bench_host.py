@@ -122,6 +122,13 @@ def test_bench_line_assembly_without_a_gpu(monkeypatch, capsys):
     monkeypatch.setattr(bench, "time_verify", lambda *a, **k: (0.368, 1_100_000_000))
     monkeypatch.setattr(bench, "time_few_heads", lambda *a, **k: {"value": 1.0})
     monkeypatch.setattr(bench, "time_e2e", lambda *a, **k: (20.0, 336_592_896, 69_206_016))
+    monkeypatch.setattr(bench, "link_bandwidth", lambda *a, **k: {"h2d_gbs": 400.0, "d2h_gbs": 400.0})
+    big = {}
+
+    def fake_workload(kda_, inputs_, name, steps, warmup, stream, dev, seed=0):
+        big[name] = steps
+        return {"workload": name, "ms_per_step": 1.0, "roofline": bench.step_roofline(6.8e9 * 1e-3 / 2, 1.0)}
+    monkeypatch.setattr(bench, "time_prefill_workload", fake_workload)
     monkeypatch.setattr(build, "build", lambda *a, **k: None)
     monkeypatch.setattr(kda, "load", lambda *a, **k: None)
     monkeypatch.setattr(inputs, "make_prefill", fake_prefill)
@@ -131,7 +138,7 @@ def test_bench_line_assembly_without_a_gpu(monkeypatch, capsys):
     for var in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
         monkeypatch.delenv(var, raising=False)
     args = types.SimpleNamespace(steps=20, warmup=3, decode_steps=1000, no_cpu_baseline=True, oracle_tokens=8192,
-                                 oracle_seconds=10.0)
+                                 oracle_seconds=10.0, long_steps=3, parts=None)
     assert bench.run_gpu(args) == 0
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
@@ -149,3 +156,10 @@ def test_bench_line_assembly_without_a_gpu(monkeypatch, capsys):
     assert dec["roofline"]["frac_of_nominal_8tbs"] < dec["roofline"]["frac"]
     assert line["e2e"]["h2d_bytes_per_step"] == 336_592_896
     assert line["gpu_launches"] == 40 and line["config"]["workload"] == bench.PREFILL
+    # the two larger prefill workloads carry their own rooflines
+    assert set(big) == {"varlen_bf16_8seq_1K_32K_H32_D128", "long_bf16_T1M_H32_D128"}
+    assert line["varlen"]["roofline"]["frac"] == pytest.approx(0.5 * 6.8e9 / 1e9 / bench.peaks()[0])
+    assert line["long_1M"]["workload"] == "long_bf16_T1M_H32_D128"
+    e = line["e2e"]
+    assert e["roofline"]["copy_floor_ms"] == pytest.approx(336_592_896 / 400e9 * 1e3)
+    assert e["roofline"]["frac"] == pytest.approx(e["roofline"]["copy_floor_ms"] / e["ms_per_step"])

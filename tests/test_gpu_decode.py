@@ -34,6 +34,44 @@ def test_decode_full_size_bf16():
     assert es <= tol_for(torch.bfloat16), es
 
 
+@pytest.mark.slow
+def test_decode_1000_consecutive_steps():
+    """The decode workload as benchmarked: 256 sequences x 32 heads, 1000
+    consecutive in-place steps, each with a fresh token set.  Every head of
+    eight sequences spread over the batch (256 (sequence, head) chains) is
+    checked against the oracle: o of every step, and the state after step 1000.
+    The oracle runs each chain's 1000 tokens as one sequence from the same
+    initial state (decode is the recurrence one token at a time)."""
+    dev = need_gpu()
+    w = inputs.WORKLOADS["decode_bf16_N256_H32_D128"]
+    steps = 1000
+    d = inputs.make_decode(w, device=dev, seed=0, n_token_sets=steps)
+    sel = torch.arange(0, w.B, w.B // 8, device=dev)[:8]          # 8 sequences x all 32 heads
+    S = d["S"].clone()
+    o_sel = []
+    for t in range(steps):
+        o = kda.kda_decode(d["q"][t], d["k"][t], d["v"][t], d["log_alpha"][t], d["beta"][t], S)
+        o_sel.append(o.index_select(0, sel))
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_device_status() == 0
+    # oracle input: chain n's tokens are its rows of the 1000 token sets, in order
+    pack = lambda xs: torch.stack([x.index_select(0, sel) for x in xs], dim=1).reshape(
+        (len(sel) * steps,) + tuple(xs[0].shape[1:])).contiguous()
+    cu = [i * steps for i in range(len(sel) + 1)]
+    O_ref, S_ref = oracle.prefill(pack(d["q"]), pack(d["k"]), pack(d["v"]), pack(d["log_alpha"]),
+                                  pack(d["beta"]), cu_seqlens=cu, S0=d["S"].index_select(0, sel))
+    o_gpu = torch.stack(o_sel, dim=1).double().cpu().numpy()           # [8, steps, H, dv]
+    O_ref = O_ref.reshape(o_gpu.shape)
+    assert np.all(np.isfinite(o_gpu))
+    # the bar per step (each step is one call): max |o - o_ref| / max |o_ref| over its outputs
+    eo = max(float(np.max(np.abs(o_gpu[:, t] - O_ref[:, t]))) / float(np.max(np.abs(O_ref[:, t])))
+             for t in range(steps))
+    es = rel_err(S.index_select(0, sel), S_ref)
+    print(f"PARITY decode 1000 steps, 256 chains: o={eo:.3e} S={es:.3e}")
+    assert eo <= tol_for(torch.bfloat16), eo
+    assert es <= tol_for(torch.bfloat16), es
+
+
 @pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (128, 64), (128, 128), (32, 128)])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_decode_shapes(dk, dv, dtype):

@@ -1,0 +1,45 @@
+"""Parity at the no-decay end of the admitted gate range.
+
+The workloads clamp the log-decay to [-5, -1e-4] (the (-5, 0) bound of "LLM
+architecture at trillion scale", section "The KDA update, in plain words").
+At the upper clamp, log alpha = -1e-4 on every channel, the state hardly
+decays: what the chunked form rounds in one chunk is carried through every
+later one, so this is where the tensor-core path's bf16 operands are tested
+hardest.  The error does not grow without bound (each delta-rule write
+replaces what the state held along its key), so 8192 tokens -- 128 chunks,
+many times the state's memory length -- covers the regime.  Both beta from the
+workload recipe and beta = 1 (the full write, where (I + L) is least well
+conditioned) are checked, on every state-pass launch shape: one pass over 32
+heads, and the segment scan over 2 heads.  O and S_final against the fp64
+oracle, at the 5e-3 bar of bf16 inputs."""
+import pytest
+import torch
+
+import oracle
+import kimi_delta_attention_chunked_gb300 as kda
+from kimi_delta_attention_chunked_gb300 import inputs
+from _gpu import need_gpu, rel_err
+
+pytestmark = pytest.mark.gpu
+
+T = 8192
+
+
+@pytest.mark.parametrize("beta", ["recipe", "one"])
+@pytest.mark.parametrize("H,dk", [(32, 128), (2, 128), (4, 64)], ids=["tc_32heads", "tc_segment_scan", "simt_bf16"])
+def test_no_decay_8192_tokens(beta, H, dk):
+    dev = need_gpu()
+    w = inputs.Workload("nodecay", "prefill", H=H, dk=dk, dv=dk, dtype=torch.bfloat16, chunk=64, s0_std=0.02)
+    d = inputs.make_prefill(w, device=dev, seed=41, lengths=[T])
+    d["log_alpha"].fill_(-1e-4)
+    if beta == "one":
+        d["beta"].fill_(1.0)
+    O, Sf = kda.kda_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=d["S0"],
+                            cu_seqlens=d["cu_seqlens"], cu_seqlens_host=d["cu_seqlens_host"], chunk=64)
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_device_status() == 0
+    O_ref, S_ref = oracle.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                  cu_seqlens=d["cu_seqlens_host"], S0=d["S0"])
+    eo, es = rel_err(O, O_ref), rel_err(Sf, S_ref)
+    print(f"PARITY no-decay beta={beta} H={H} dk={dk} T={T}: O={eo:.3e} S={es:.3e}")
+    assert eo <= 5e-3 and es <= 5e-3, (eo, es)
