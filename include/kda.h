@@ -70,7 +70,11 @@ typedef enum kda_status {
     KDA_ERR_UNSUPPORTED = 2,  /* shape / dtype / chunk combination not built     */
     KDA_ERR_WORKSPACE = 3,    /* workspace missing, too small or misaligned      */
     KDA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed             */
-    KDA_ERR_TIMEOUT = 5       /* a kernel gave up waiting (device status only)    */
+    KDA_ERR_TIMEOUT = 5,      /* a kernel gave up waiting (device status only)    */
+    KDA_ERR_PRECONDITION = 6, /* debug library: an input outside its stated range
+                                 (device status only)                             */
+    KDA_ERR_DEVICE_CHECK = 7  /* debug library: a kernel found an index outside its
+                                 buffer and skipped the access (device status)    */
 } kda_status;
 
 typedef enum kda_dtype {
@@ -306,6 +310,27 @@ KDA_API kda_status kda_check_wait_timeout(long long limit_cycles, cudaStream_t s
  * kernel with CUDA events on the stream the kernel runs on.
  */
 KDA_API kda_status kda_set_trace_events(void* const* events, int n_events);
+
+/*
+ * Debug variant.  The library is also built as libkda_debug.so, compiled with
+ * KDA_DEBUG: the same entry points with the same results, plus checks that the
+ * release library leaves out for speed.
+ *   - Precondition: before each kda_prefill, kda_prefill_ckpt,
+ *     kda_prefill_noalloc, kda_decode and kda_decode_multi call, one pass over
+ *     log_alpha records KDA_ERR_PRECONDITION in the device status word when a
+ *     value lies outside [-5, 0] or is not a number.  That is the log-decay
+ *     bound of "LLM architecture at trillion scale", section "The KDA update,
+ *     in plain words", inside which the chunked form's staged decay factors
+ *     stay finite and the accuracy target is stated; the call still computes.
+ *     (The *_fused calls clamp the log-decay themselves and are not checked.)
+ *   - Device checks: the tensor-core kernels check the workspace slots and
+ *     segment indices they derive from the call's lengths against the sizes
+ *     they were given; an index outside records KDA_ERR_DEVICE_CHECK and the
+ *     access is skipped.  Nothing traps.
+ * kda_get_last_device_status of the same library reports either code.
+ * Returns 1 in the debug library, 0 in the release library.
+ */
+KDA_API int kda_debug_build(void);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 KDA_API const char* kda_status_string(kda_status status);

@@ -15,16 +15,20 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkda.so")
+LIB_DEBUG_PATH = os.path.join(_PKG, "libkda_debug.so")
 
-KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = range(6)
+(KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA, KDA_ERR_TIMEOUT,
+ KDA_ERR_PRECONDITION, KDA_ERR_DEVICE_CHECK) = range(8)
 KDA_FP32, KDA_BF16 = 0, 1
 SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_ckpt", "kda_prefill_fused",
            "kda_prefill_noalloc", "kda_decode", "kda_decode_fused", "kda_decode_multi",
-           "kda_get_last_device_status", "kda_check_wait_timeout", "kda_set_trace_events", "kda_status_string")
+           "kda_get_last_device_status", "kda_check_wait_timeout", "kda_set_trace_events", "kda_debug_build",
+           "kda_status_string")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lock = threading.Lock()
 _lib = None
+_lib_debug = None
 
 
 class KDAError(RuntimeError):
@@ -37,39 +41,56 @@ def load():
     """Load libkda.so (built by ``build.build()``); raises if it is not there."""
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        if not os.path.exists(LIB_PATH):
-            raise ImportError(f"KDA CUDA library not built: {LIB_PATH} is missing "
-                              "(run python -m kimi_delta_attention_chunked_gb300.build)")
-        lib = ctypes.CDLL(LIB_PATH)
-        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-        lib.kda_prefill_workspace_size.argtypes = [I, I, I, I, I, I, I]
-        lib.kda_prefill_workspace_size.restype = Z
-        lib.kda_prefill.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, Z, P]
-        lib.kda_prefill.restype = I
-        lib.kda_prefill_ckpt.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, I, P, I, P, Z, P]
-        lib.kda_prefill_ckpt.restype = I
-        lib.kda_prefill_fused.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, Z, P]
-        lib.kda_prefill_fused.restype = I
-        lib.kda_decode_fused.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P]
-        lib.kda_decode_fused.restype = I
-        lib.kda_prefill_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
-        lib.kda_prefill_noalloc.restype = I
-        lib.kda_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P]
-        lib.kda_decode.restype = I
-        lib.kda_decode_multi.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P]
-        lib.kda_decode_multi.restype = I
-        lib.kda_get_last_device_status.argtypes = [P]
-        lib.kda_get_last_device_status.restype = I
-        lib.kda_check_wait_timeout.argtypes = [ctypes.c_longlong, P]
-        lib.kda_check_wait_timeout.restype = I
-        lib.kda_set_trace_events.argtypes = [P, I]
-        lib.kda_set_trace_events.restype = I
-        lib.kda_status_string.argtypes = [I]
-        lib.kda_status_string.restype = ctypes.c_char_p
-        _lib = lib
-        return lib
+        if _lib is None:
+            _lib = _open(LIB_PATH)
+        return _lib
+
+
+def load_debug():
+    """Load libkda_debug.so, the variant with the input precondition and device
+    index checks (include/kda.h, kda_debug_build); raises if it is not there.
+    The functions of this module call the release library; the debug one is
+    called through the returned ctypes handle."""
+    global _lib_debug
+    with _lock:
+        if _lib_debug is None:
+            _lib_debug = _open(LIB_DEBUG_PATH)
+        return _lib_debug
+
+
+def _open(path):
+    if not os.path.exists(path):
+        raise ImportError(f"KDA CUDA library not built: {path} is missing "
+                          "(run python -m kimi_delta_attention_chunked_gb300.build)")
+    lib = ctypes.CDLL(path)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.kda_prefill_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.kda_prefill_workspace_size.restype = Z
+    lib.kda_prefill.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, Z, P]
+    lib.kda_prefill.restype = I
+    lib.kda_prefill_ckpt.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, I, P, I, P, Z, P]
+    lib.kda_prefill_ckpt.restype = I
+    lib.kda_prefill_fused.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, Z, P]
+    lib.kda_prefill_fused.restype = I
+    lib.kda_decode_fused.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P]
+    lib.kda_decode_fused.restype = I
+    lib.kda_prefill_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
+    lib.kda_prefill_noalloc.restype = I
+    lib.kda_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P]
+    lib.kda_decode.restype = I
+    lib.kda_decode_multi.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P]
+    lib.kda_decode_multi.restype = I
+    lib.kda_get_last_device_status.argtypes = [P]
+    lib.kda_get_last_device_status.restype = I
+    lib.kda_check_wait_timeout.argtypes = [ctypes.c_longlong, P]
+    lib.kda_check_wait_timeout.restype = I
+    lib.kda_set_trace_events.argtypes = [P, I]
+    lib.kda_set_trace_events.restype = I
+    lib.kda_debug_build.argtypes = []
+    lib.kda_debug_build.restype = I
+    lib.kda_status_string.argtypes = [I]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    return lib
 
 
 def kda_status_string(status: int) -> str:

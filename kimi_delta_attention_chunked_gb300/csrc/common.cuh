@@ -21,6 +21,16 @@ __device__ __forceinline__ void record_status(int* status, int code) {
     if (status) atomicCAS(status, kDevOk, code);
 }
 
+// Debug-build device checks (compiled with KDA_DEBUG): a condition that fails
+// records KDA_ERR_DEVICE_CHECK in the status word and evaluates to false, so
+// that the caller skips the access it guards.  In release builds the check is
+// not compiled and evaluates to true.
+#ifdef KDA_DEBUG
+#define KDA_DCHECK(status, cond) ((cond) ? true : (::kda::record_status((status), KDA_ERR_DEVICE_CHECK), false))
+#else
+#define KDA_DCHECK(status, cond) true
+#endif
+
 template <typename T> struct io;
 template <> struct io<float> {
     static __device__ __forceinline__ float ld(const float* p) { return *p; }

@@ -35,6 +35,35 @@ __global__ void kda_wait_check_kernel(int* status, long long limit) {
     }
 }
 
+#ifdef KDA_DEBUG
+// Debug-build precondition: every log-decay value inside [-5, 0] (the bound
+// of "LLM architecture at trillion scale", section "The KDA update, in plain
+// words"); the first one outside (or a NaN) records KDA_ERR_PRECONDITION.
+__global__ void kda_check_log_alpha_kernel(const float* __restrict__ la, long long n, int* status) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const float x = la[i];
+        if (!(x >= -5.f && x <= 0.f)) {
+            kda::record_status(status, KDA_ERR_PRECONDITION);
+            return;
+        }
+    }
+}
+#endif
+
+// Launches the precondition check of the debug library (nothing in release).
+cudaError_t check_log_alpha(const float* la, long long n, cudaStream_t stream, int* status) {
+#ifdef KDA_DEBUG
+    if (n <= 0 || !la) return cudaSuccess;
+    const long long blocks = std::min<long long>((n + 255) / 256, 1216);
+    kda_check_log_alpha_kernel<<<(unsigned)blocks, 256, 0, stream>>>(la, n, status);
+    return cudaGetLastError();
+#else
+    (void)la; (void)n; (void)stream; (void)status;
+    return cudaSuccess;
+#endif
+}
+
 bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 bool chunk_ok(int c) { return c == 16 || c == 32 || c == 64; }
 bool dtype_ok(kda_dtype t) { return t == KDA_FP32 || t == KDA_BF16; }
@@ -144,11 +173,19 @@ kda_status prefill_impl(const void* q, const void* k, const void* v, const float
         if (workspace_bytes < need || (need && !workspace)) return KDA_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return KDA_ERR_WORKSPACE;
         a.status = status_ptr();
+        if (!prologue) {
+            const cudaError_t e = check_log_alpha(log_alpha, (long long)T_total * H * dk, stream, a.status);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
         kda_host::trace_reset();
         kda_host::trace_mark(stream);
         return from_cuda(kda_host::launch_prefill_tc(a));
     }
     a.status = status_ptr();
+    if (!prologue) {
+        const cudaError_t e = check_log_alpha(log_alpha, (long long)T_total * H * dk, stream, a.status);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
     kda_host::trace_reset();
     kda_host::trace_mark(stream);
     using L = cudaError_t (*)(const kda_host::PrefillArgs&);
@@ -174,6 +211,10 @@ kda_status decode_impl(const void* q, const void* k, const void* v, const float*
     if (o == q || o == k || o == v || o == (void*)S) return KDA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(S) % 16 != 0) return KDA_ERR_INVALID_ARG;
     kda_host::DecodeArgs a{q, k, v, log_alpha, beta, S, N, H, dk, dv, dtype, o, stream, prologue};
+    if (!prologue) {
+        const cudaError_t e = check_log_alpha(log_alpha, (long long)N * H * dk, stream, status_ptr());
+        if (e != cudaSuccess) return from_cuda(e);
+    }
     kda_host::trace_reset();
     kda_host::trace_mark(stream);
     const cudaError_t e = kda_host::launch_decode(a);
@@ -251,6 +292,8 @@ kda_status kda_decode_multi(const void* q, const void* k, const void* v, const f
     if (o && (o == q || o == k || o == v || o == (void*)S)) return KDA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(S) % 16 != 0) return KDA_ERR_INVALID_ARG;
     kda_host::DecodeArgs a{q, k, v, log_alpha, beta, S, N, H, dk, dv, dtype, o, stream, 0};
+    const cudaError_t ec = check_log_alpha(log_alpha, (long long)N * K * H * dk, stream, status_ptr());
+    if (ec != cudaSuccess) return from_cuda(ec);
     kda_host::trace_reset();
     kda_host::trace_mark(stream);
     const cudaError_t e = kda_host::launch_decode_multi(a, K, commit_len);
@@ -273,6 +316,14 @@ kda_status kda_get_last_device_status(cudaStream_t stream) {
     return h == 0 ? KDA_OK : static_cast<kda_status>(h);
 }
 
+int kda_debug_build(void) {
+#ifdef KDA_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 const char* kda_status_string(kda_status s) {
     switch (s) {
         case KDA_OK: return "KDA_OK: success";
@@ -281,6 +332,9 @@ const char* kda_status_string(kda_status s) {
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing, too small or misaligned";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime or launch error";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a kernel gave up waiting; outputs incomplete";
+        case KDA_ERR_PRECONDITION: return "KDA_ERR_PRECONDITION: log_alpha outside [-5, 0] (debug library check)";
+        case KDA_ERR_DEVICE_CHECK:
+            return "KDA_ERR_DEVICE_CHECK: a kernel index left its buffer; access skipped (debug library check)";
     }
     return "KDA: unknown status";
 }

@@ -330,7 +330,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
             const float* __restrict__ beta, int H, int use_table,
             int fixed_len, int nch_per_seq, const int4* __restrict__ chunk_info,
-            const int4* __restrict__ seq_info, int j_begin, int j_count, int n_x,
+            const int4* __restrict__ seq_info, int j_begin, int j_count, int n_x, int n_slots,
             uint8_t* __restrict__ ws_blocks, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
@@ -356,6 +356,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             tok0 = ci.x;
             nrows = ci.y;
         }
+        if (!KDA_DCHECK(status, slot >= 0 && slot < n_slots)) return false;    // workspace block of the item
         return nrows > 0;
     };
     const long long n_items = (long long)n_x * H;
@@ -875,7 +876,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1)
 kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, int nch_per_seq,
              int c_begin, int c_end, const uint8_t* __restrict__ ws_blocks, const float* __restrict__ S0, int H,
              bf16* __restrict__ O, float* __restrict__ S_final, int ckpt_every, float* __restrict__ ckpt,
-             int ckpt_cap, int* status, int seg_pass1, float* __restrict__ S_final_map) {
+             int ckpt_cap, int* status, int seg_pass1, float* __restrict__ S_final_map, int n_slots) {
     // seg_pass1 (segment scan, first pass): blockIdx.z = 0 runs each segment
     // from a zero state (its affine offset, into S_final), blockIdx.z = 1 from
     // the identity with U0 taken as zero (its linear map, into S_final_map);
@@ -896,7 +897,9 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     // this launch runs chunks [c_begin, c_end) of the sequence; locally they are
     // numbered 0 .. nloc - 1 (stage and barrier parities use the local number)
     const int cb = min(c_begin, nch);
-    const int nloc = max(0, min(c_end, nch) - cb);
+    int nloc = max(0, min(c_end, nch) - cb);
+    // the chunks' workspace blocks must exist (debug builds check; none is read otherwise)
+    if (!KDA_DCHECK(status, nloc == 0 || (first + cb >= 0 && first + cb + nloc <= n_slots))) nloc = 0;
     // state checkpoints: index of this sequence's first one (block-wide sum)
     int ck_base = 0;
     if (ckpt_every > 0)
@@ -1252,7 +1255,8 @@ constexpr uint32_t SC_SMEM = (DK * SC_LDA + DK * SC_COLS) * 4;
 
 __global__ void __launch_bounds__(256)
 kda_tc_seg_scan(const int2* __restrict__ seq_seg, const float* __restrict__ A, const float* __restrict__ B,
-                const float* __restrict__ S0, float* __restrict__ S_start, float* __restrict__ S_final, int H) {
+                const float* __restrict__ S0, float* __restrict__ S_start, float* __restrict__ S_final, int H,
+                int s_max, int* status) {
     extern __shared__ float sc_smem[];
     float* As = sc_smem;                         // [DK][SC_LDA]
     float* Ss = sc_smem + DK * SC_LDA;           // [DK][SC_COLS]
@@ -1267,7 +1271,8 @@ kda_tc_seg_scan(const int2* __restrict__ seq_seg, const float* __restrict__ A, c
         for (int u = 0; u < 4; ++u) srow[u] = src ? src[u] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
-    const int2 ss = seq_seg[n];
+    int2 ss = seq_seg[n];
+    if (!KDA_DCHECK(status, ss.x >= 0 && ss.y >= 0 && ss.x + ss.y <= s_max)) ss.y = 0;
     for (int p = 0; p < ss.y; ++p) {
         const int sg = ss.x + p;
         // this segment's starting state; then its map A_p into shared memory
@@ -1503,13 +1508,14 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         const long long items = (long long)gx * a.H;
         const unsigned grid = (unsigned)std::min<long long>(items, 2LL * n_sm);   // two resident CTAs per SM
         prep_kernel<<<grid, 256, prep_smem, st>>>(tm_q, tm_k, tm_v, tm_g, a.beta, a.H, use_table, fixed_len,
-                                                  nch_per, chunk_info, seq_info, j0, jn, gx, blocks, a.status);
+                                                  nch_per, chunk_info, seq_info, j0, jn, gx, (int)ub, blocks,
+                                                  a.status);
         return cudaGetLastError();
     };
     auto chain = [&](int c0, int c1, const float* s_in, float* s_out, cudaStream_t st) {
         kda_tc_chain<<<dim3(NTILES * a.n_seq, a.H), K2_THREADS, chain_smem, st>>>(
             seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
-            a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr);
+            a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub);
         return cudaGetLastError();
     };
 
@@ -1522,16 +1528,17 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         // pass 1: every segment from zero (-> seg_B) and as a map from the identity (-> seg_A)
         kda_tc_chain<<<dim3(NTILES * sp.s_max, a.H, 2), K2_THREADS, chain_smem, a.stream>>>(
             seg_info, 1, 0, 0, 0, INT32_MAX, blocks, nullptr, a.H, static_cast<bf16*>(a.O), seg_B, 0, nullptr, 0,
-            a.status, 1, seg_A);
+            a.status, 1, seg_A, (int)ub);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // pass 2: starting state of every segment, and the final states
         kda_tc_seg_scan<<<dim3(a.n_seq, a.H, DV / SC_COLS), 256, SC_SMEM, a.stream>>>(seq_seg, seg_A, seg_B, a.S0,
-                                                                                       seg_S, a.S_final, a.H);
+                                                                                       seg_S, a.S_final, a.H,
+                                                                                       sp.s_max, a.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // pass 3: every segment from its starting state, writing O
         kda_tc_chain<<<dim3(NTILES * sp.s_max, a.H), K2_THREADS, chain_smem, a.stream>>>(
             seg_info, 1, 0, 0, 0, INT32_MAX, blocks, seg_S, a.H, static_cast<bf16*>(a.O), nullptr, 0, nullptr, 0,
-            a.status, 0, nullptr);
+            a.status, 0, nullptr, (int)ub);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         trace_mark(a.stream);
         return cudaSuccess;

@@ -39,6 +39,20 @@ def test_every_declared_symbol_is_exported(lib):
     assert exported == sorted(declared_functions())
 
 
+def test_debug_library_exports_the_same_api():
+    """libkda_debug.so (KDA_DEBUG: precondition and device index checks) has
+    exactly the release library's entry points, and says which build it is."""
+    import subprocess
+    build.build()
+    dbg = _lib.load_debug()
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_DEBUG_PATH], capture_output=True, text=True).stdout
+    assert sorted(set(re.findall(r"\s(kda_\w+)$", out, re.M))) == sorted(declared_functions())
+    assert dbg.kda_debug_build() == 1
+    assert _lib.load().kda_debug_build() == 0
+    # host-side argument checks are the same
+    assert dbg.kda_check_wait_timeout(-1, None) == _lib.KDA_ERR_INVALID_ARG
+
+
 def test_wait_check_rejects_bad_limits_before_launch(lib):
     # checked on the host: nothing is launched (no GPU is needed for this)
     assert lib.kda_check_wait_timeout(-1, None) == _lib.KDA_ERR_INVALID_ARG
@@ -46,7 +60,7 @@ def test_wait_check_rejects_bad_limits_before_launch(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(8):
         s = kda.kda_status_string(code)
         assert s.startswith("KDA"), s
     assert "unknown" in kda.kda_status_string(99)
