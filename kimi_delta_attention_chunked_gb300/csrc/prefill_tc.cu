@@ -418,6 +418,18 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             kda::tma_load_3d(sm + K1_BWU + 16384, &tm_v, 0, h, tok0, bar_ld);
             kda::tma_load_3d(sm + K1_BWU + 16384 + 8192, &tm_v, 64, h, tok0, bar_ld);
             ++n_loads;
+            // the next item's inputs into L2 while this one is worked on (the
+            // first valid one among the next four this CTA takes)
+            for (long long nx = it + gridDim.x; nx < n_items && nx <= it + 4LL * gridDim.x; nx += gridDim.x) {
+                int t1, r1, s1, h1;
+                if (!item(nx, t1, r1, s1, h1)) continue;
+                kda::tma_prefetch_3d(&tm_g, 0, h1, t1);
+                kda::tma_prefetch_3d(&tm_q, 0, h1, t1);
+                kda::tma_prefetch_3d(&tm_k, 0, h1, t1);
+                kda::tma_prefetch_3d(&tm_v, 0, h1, t1);
+                kda::tma_prefetch_3d(&tm_v, 64, h1, t1);
+                break;
+            }
         }
         // beta of row 16 b + (lane % 16): one value per lane
         float bt = beta[((size_t)tok0 + min(16 * b + (lane & 15), nrows - 1)) * H + h];
@@ -960,6 +972,10 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 kda::mbar_arrive_expect_tx(fullA + sa, K2_ASTAGE);
                 kda::bulk_g2s(sm + sa * K2_ASTAGE, block_of(k) + WS_A1, K2_ASTAGE, fullA + sa);
                 ++nA;
+                // the U0 / O0 tiles and a_last of this chunk, which the conversion
+                // warps load into registers when the chunk comes up, into L2
+                kda::bulk_prefetch_l2(block_of(k) + WS_UO + 2 * TILE_F32 * tile, 2 * TILE_F32);
+                kda::bulk_prefetch_l2(block_of(k) + WS_AL, DK * 4);
                 const int sb = k % K2_NB;
                 if (k >= K2_NB) wait(emptyB + sb, (uint32_t)(((k - K2_NB) / K2_NB) & 1));
                 if (*abort_f) break;

@@ -118,6 +118,19 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, 
         : "memory");
 }
 
+// Prefetch into L2 of the box at (x, y, z) of a tensor map (no shared memory,
+// no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(x), "r"(y),
+                 "r"(z)
+                 : "memory");
+}
+
+// Prefetch into L2 of `bytes` (multiple of 16) at a 16-byte aligned global address.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM
 // Allocation / deallocation are warp-collective.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
