@@ -383,8 +383,9 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     uint32_t n_done = 0;                          // items finished by this CTA (bar_q parity)
     uint32_t bar_phase = 0;                       // completed phases of bar (three per item)
     uint32_t n_loads = 0, n_qloads = 0;           // input / Q_decay copy phases issued (thread 0)
-    // Bounded wait; once it runs out (or another thread's did) the CTA stops
-    // taking items and drains what it has in flight before it exits.
+    // Bounded wait.  Once one runs out (or another thread's did) the CTA
+    // issues no further copy or MMA: the remaining items run through without
+    // waiting, and what is in flight is drained before the CTA exits.
     auto wait = [&](uint64_t* b, uint32_t parity) {
         if (!kda::mbar_wait_or_abort(b, parity, kda::kWaitCycles, abort_f)) {
             kda::record_status(status, kda::kDevTimeout);
@@ -402,14 +403,17 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         uint8_t* blk = ws_blocks + ((size_t)slot * H + h) * WS_BLOCK;
 
         // ---------------- a1: loads and per-block cumulative log-decay
-        const int p = w >> 2, b = w & 3;          // channel panel, row block
-        const int ch = 64 * p + 2 * lane;          // this thread's two channels
-        float G0[16], G1[16];
-        uint32_t qv[16], kv[16];
+        // Thread tile: rows r0 .. r0 + 3 of row block b (r0 = 16 b + 4 rq) and
+        // the eight channels c0 .. c0 + 7 (c0 = 64 p + 8 cg), so that every load
+        // and store of a row piece is one 16-byte vector; the four row quads of
+        // a block are lanes 8 apart, and the cumulative sum crosses them by
+        // shuffles.
+        const int b = w >> 1, p = w & 1, cg = lane & 7, rq = lane >> 3;
+        const int c0 = 64 * p + 8 * cg, r0 = 16 * b + 4 * rq;
         // inputs: one TMA copy per tensor (V straight into its operand slot, both
         // 64-channel panels) once the previous item's output images have left
         // shared memory; rows past the end of the tensor read as zero
-        if (tid == 0) {
+        if (tid == 0 && !*abort_f) {
             kda::bulk_wait_read_all();
             kda::mbar_arrive_expect_tx(bar_ld, K1_IN_BYTES);
             kda::tma_load_3d(sm + K1_SG, &tm_g, 0, h, tok0, bar_ld);
@@ -418,152 +422,233 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             kda::tma_load_3d(sm + K1_BWU + 16384, &tm_v, 0, h, tok0, bar_ld);
             kda::tma_load_3d(sm + K1_BWU + 16384 + 8192, &tm_v, 64, h, tok0, bar_ld);
             ++n_loads;
-            // the next item's inputs into L2 while this one is worked on (the
-            // first valid one among the next four this CTA takes)
-            for (long long nx = it + gridDim.x; nx < n_items && nx <= it + 4LL * gridDim.x; nx += gridDim.x) {
-                int t1, r1, s1, h1;
-                if (!item(nx, t1, r1, s1, h1)) continue;
-                kda::tma_prefetch_3d(&tm_g, 0, h1, t1);
-                kda::tma_prefetch_3d(&tm_q, 0, h1, t1);
-                kda::tma_prefetch_3d(&tm_k, 0, h1, t1);
-                kda::tma_prefetch_3d(&tm_v, 0, h1, t1);
-                kda::tma_prefetch_3d(&tm_v, 64, h1, t1);
-                break;
+        }
+        float bt[4];                               // beta of this thread's rows
+#pragma unroll
+        for (int i = 0; i < 4; ++i) bt[i] = beta[((size_t)tok0 + min(r0 + i, nrows - 1)) * H + h];
+        wait(bar_ld, n_done & 1);
+        float e[4][8];                             // log-decay, then its cumulative sum, then staged factors
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = r0 + i;
+            const float4 g0 = *reinterpret_cast<const float4*>(sm + K1_SG + r * 512 + c0 * 4);
+            const float4 g1 = *reinterpret_cast<const float4*>(sm + K1_SG + r * 512 + c0 * 4 + 16);
+            e[i][0] = g0.x; e[i][1] = g0.y; e[i][2] = g0.z; e[i][3] = g0.w;
+            e[i][4] = g1.x; e[i][5] = g1.y; e[i][6] = g1.z; e[i][7] = g1.w;
+            // rows past the chunk's end (another sequence's tokens, or zeros): zero
+            // inputs (log-decay 0, beta 0, and q = k = v = 0 below)
+            if (r >= nrows) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) e[i][j] = 0.f;
+                bt[i] = 0.f;
+            } else if (PROLOGUE) {
+                bt[i] = kda::prologue_beta(bt[i]);
             }
         }
-        // beta of row 16 b + (lane % 16): one value per lane
-        float bt = beta[((size_t)tok0 + min(16 * b + (lane & 15), nrows - 1)) * H + h];
-        wait(bar_ld, n_done & 1);
+        // this thread's q and k row pieces (zero past the chunk's end)
+        auto load_qk = [&](int i, float* q, float* k) {
+            const int r = r0 + i;
+            uint4 qv = *reinterpret_cast<const uint4*>(sm + K1_SQ + r * 256 + c0 * 2);
+            uint4 kv = *reinterpret_cast<const uint4*>(sm + K1_SK + r * 256 + c0 * 2);
+            if (r >= nrows) { qv = make_uint4(0u, 0u, 0u, 0u); kv = qv; }
+            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+            const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            const int r = 16 * b + rr;
-            const float2 gg = *reinterpret_cast<const float2*>(sm + K1_SG + r * 512 + ch * 4);
-            G0[rr] = gg.x;
-            G1[rr] = gg.y;
-            qv[rr] = *reinterpret_cast<const uint32_t*>(sm + K1_SQ + r * 256 + ch * 2);
-            kv[rr] = *reinterpret_cast<const uint32_t*>(sm + K1_SK + r * 256 + ch * 2);
-        }
-        // rows past the chunk's end (another sequence's tokens, or zeros): zero
-        // inputs (log-decay 0, beta 0, q = k = v = 0)
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            if (16 * b + rr >= nrows) { G0[rr] = 0.f; G1[rr] = 0.f; qv[rr] = 0u; kv[rr] = 0u; }
-        }
-        if (16 * b + (lane & 15) >= nrows) bt = 0.f;
-        else if (PROLOGUE) bt = kda::prologue_beta(bt);
-        for (int e = tid; e < (C - nrows) * (DV / 8); e += 256) {
-            const int t = nrows + (e >> 4), cc = e & 15;
+            for (int j = 0; j < 4; ++j) {
+                const float2 qf = kda::unpack_bf16x2(qw[j]), kf = kda::unpack_bf16x2(kw[j]);
+                q[2 * j] = qf.x; q[2 * j + 1] = qf.y; k[2 * j] = kf.x; k[2 * j + 1] = kf.y;
+            }
+        };
+        for (int el = tid; el < (C - nrows) * (DV / 8); el += 256) {
+            const int t = nrows + (el >> 4), cc = el & 15;
             *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) = make_uint4(0u, 0u, 0u, 0u);
         }
-        __syncthreads();                           // the input tiles are in registers
-        if (*abort_f) break;                       // read after the barrier: the same for every thread
+        __syncthreads();                           // the log-decay tile is in registers
         float* nrm = reinterpret_cast<float*>(sm + K1_NRM);
         if (PROLOGUE) {
             // fused prologue: gates from their pre-activations; squared norms of
-            // q and k rows over this warp's 64 channels
+            // the q and k rows over this panel's 64 channels
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                if (16 * b + rr < nrows) {
-                    G0[rr] = kda::prologue_log_alpha(G0[rr]);
-                    G1[rr] = kda::prologue_log_alpha(G1[rr]);
+            for (int i = 0; i < 4; ++i) {
+                float sq = 0.f, sk = 0.f;
+                {
+                    float q[8], k[8];
+                    load_qk(i, q, k);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        sq = fmaf(q[j], q[j], sq);
+                        sk = fmaf(k[j], k[j], sk);
+                    }
                 }
-                const float2 qf = kda::unpack_bf16x2(qv[rr]), kf = kda::unpack_bf16x2(kv[rr]);
-                float sq = fmaf(qf.x, qf.x, qf.y * qf.y), sk = fmaf(kf.x, kf.x, kf.y * kf.y);
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
+                for (int o = 1; o < 8; o <<= 1) {
                     sq += __shfl_xor_sync(0xffffffffu, sq, o);
                     sk += __shfl_xor_sync(0xffffffffu, sk, o);
                 }
-                if (lane == 0) {
-                    nrm[p * 64 + 16 * b + rr] = sq;
-                    nrm[128 + p * 64 + 16 * b + rr] = sk;
+                if (cg == 0) {
+                    nrm[p * 64 + r0 + i] = sq;
+                    nrm[128 + p * 64 + r0 + i] = sk;
+                }
+                if (r0 + i < nrows) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) e[i][j] = kda::prologue_log_alpha(e[i][j]);
                 }
             }
         }
+        // inclusive cumulative sum within the 16-row block: over this thread's
+        // four rows, then across the block's four row quads
 #pragma unroll
-        for (int rr = 1; rr < 16; ++rr) { G0[rr] += G0[rr - 1]; G1[rr] += G1[rr - 1]; }
+        for (int i = 1; i < 4; ++i) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) e[i][j] += e[i - 1][j];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float t = e[3][j];
+            float x = t;
+            float y = __shfl_up_sync(0xffffffffu, x, 8);
+            if (rq >= 1) x += y;
+            y = __shfl_up_sync(0xffffffffu, x, 16);
+            if (rq >= 2) x += y;
+            const float excl = x - t;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) e[i][j] += excl;
+        }
         float* tot = reinterpret_cast<float*>(sm + K1_TOT);
         float* first = reinterpret_cast<float*>(sm + K1_FIRST);
         float* beta_s = reinterpret_cast<float*>(sm + K1_BETA);
-        tot[b * 128 + ch] = G0[15];
-        tot[b * 128 + ch + 1] = G1[15];
-        first[b * 128 + ch] = G0[0];
-        first[b * 128 + ch + 1] = G1[0];
-        if (p == 0 && lane < 16) beta_s[16 * b + lane] = bt;
+        if (rq == 3) {
+            *reinterpret_cast<float4*>(tot + b * 128 + c0) = make_float4(e[3][0], e[3][1], e[3][2], e[3][3]);
+            *reinterpret_cast<float4*>(tot + b * 128 + c0 + 4) = make_float4(e[3][4], e[3][5], e[3][6], e[3][7]);
+        }
+        if (rq == 0) {
+            *reinterpret_cast<float4*>(first + b * 128 + c0) = make_float4(e[0][0], e[0][1], e[0][2], e[0][3]);
+            *reinterpret_cast<float4*>(first + b * 128 + c0 + 4) = make_float4(e[0][4], e[0][5], e[0][6], e[0][7]);
+        }
+        if (p == 0 && cg == 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) beta_s[r0 + i] = bt[i];
+        }
         __syncthreads();
 
-        // global cumulative log-decay at each block start (Gs) and at the chunk end
-        float Gs0[4], Gs1[4], acc0 = 0.f, acc1 = 0.f;
+        // chunk-wide cumulative log-decay at this block's first row (myG) and at
+        // the chunk's end (acc), per channel
+        float myG[8], acc[8], fb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { acc[j] = 0.f; myG[j] = 0.f; fb[j] = 0.f; }
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            Gs0[m] = acc0 + first[m * 128 + ch];
-            Gs1[m] = acc1 + first[m * 128 + ch + 1];
-            acc0 += tot[m * 128 + ch];
-            acc1 += tot[m * 128 + ch + 1];
-        }
-        float myG0 = Gs0[0], myG1 = Gs1[0];
+            const float4 f0 = *reinterpret_cast<const float4*>(first + m * 128 + c0);
+            const float4 f1 = *reinterpret_cast<const float4*>(first + m * 128 + c0 + 4);
+            const float4 t0 = *reinterpret_cast<const float4*>(tot + m * 128 + c0);
+            const float4 t1 = *reinterpret_cast<const float4*>(tot + m * 128 + c0 + 4);
+            const float fm[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+            const float tm[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
 #pragma unroll
-        for (int m = 1; m < 4; ++m)
-            if (m == b) { myG0 = Gs0[m]; myG1 = Gs1[m]; }
-        const float ap0 = __expf(myG0), ap1 = __expf(myG1);              // a at the block start
-        const float R0 = __expf(acc0 - myG0), R1 = __expf(acc1 - myG1);  // a_last / a(block start)
-        if (b == 0) {
-            *reinterpret_cast<float2*>(blk + WS_AL + 4 * ch) = make_float2(__expf(acc0), __expf(acc1));
+            for (int j = 0; j < 8; ++j) {
+                if (m == b) { myG[j] = acc[j] + fm[j]; fb[j] = fm[j]; }
+                acc[j] += tm[j];
+            }
+        }
+        float ap[8], R[8];                         // a at the block start; a_last / a(block start)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { ap[j] = __expf(myG[j]); R[j] = __expf(acc[j] - myG[j]); }
+        if (b == 0 && rq == 0) {
+            float al[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) al[j] = __expf(acc[j]);
+            *reinterpret_cast<float4*>(blk + WS_AL + 4 * c0) = make_float4(al[0], al[1], al[2], al[3]);
+            *reinterpret_cast<float4*>(blk + WS_AL + 4 * c0 + 16) = make_float4(al[4], al[5], al[6], al[7]);
         }
 
-        // ---------------- a1: operands, in two halves of 8 rows (fewer live registers)
+        // ---------------- a1: operands, row by row.  Row factors exp(G_r - G_pb) <= 1,
+        // column factors exp(G_pb - G_t) >= 1 (<= e^75), with p_b the block's first row
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            float kts[16];                             // column factors k exp(G_pb - G_t) of the 8 rows
+        for (int i = 0; i < 4; ++i) {
 #pragma unroll
-            for (int rr = 8 * hf; rr < 8 * hf + 8; ++rr) {
-                const int r = 16 * b + rr;
-                const float e0 = __expf(G0[rr] - G0[0]), e1 = __expf(G1[rr] - G1[0]);   // <= 1
-                const float c0 = __fdividef(1.f, e0), c1 = __fdividef(1.f, e1);         // >= 1, <= e^75
-                float2 qf = kda::unpack_bf16x2(qv[rr]);
-                float2 kf = kda::unpack_bf16x2(kv[rr]);
-                if (PROLOGUE) {                        // unit-length q and k rows
-                    const float iq = rsqrtf(nrm[r] + nrm[64 + r] + kda::kNormEps);
-                    const float ik = rsqrtf(nrm[128 + r] + nrm[192 + r] + kda::kNormEps);
-                    qf.x *= iq; qf.y *= iq; kf.x *= ik; kf.y *= ik;
-                }
-                const float be = beta_s[r];
-                const float qt0 = qf.x * e0, qt1 = qf.y * e1;            // q~ (row factor)
-                const float kh0 = be * kf.x * e0, kh1 = be * kf.y * e1;  // k^ = beta k (row factor)
-                const float kt0 = kf.x * c0, kt1 = kf.y * c1;            // k (column factor, own block)
-                st_shared_u32(sm + K1_AG + kda::sw128(32 * b + rr, ch, 128), kda::pack_bf16x2(qt0, qt1));
-                st_shared_u32(sm + K1_AG + kda::sw128(32 * b + 16 + rr, ch, 128), kda::pack_bf16x2(kh0, kh1));
-                // own block's column operand (block b of tile b); the later tiles below
-                st_shared_u32(sm + K1_BG + kda::sw128(8 * b * (b + 1) + r, ch, 160), kda::pack_bf16x2(kt0, kt1));
-                kts[2 * (rr - 8 * hf)] = kt0;
-                kts[2 * (rr - 8 * hf) + 1] = kt1;
-                // Q_decay -> rows 0..63 of the [Q_decay; W] image
-                *reinterpret_cast<uint32_t*>(blk + WS_A1 + kda::sw128(r, ch, 128)) = kda::pack_bf16x2(qt0 * ap0, qt1 * ap1);
-                // K_decay -> left half of the [K_decay | V] operand
-                st_shared_u32(sm + K1_BWU + kda::sw128(r, ch, 64),
-                              kda::pack_bf16x2(kf.x * e0 * ap0, kf.y * e1 * ap1));
-                // K_restore -> K_restore^T images, high and low bf16 parts (MN-major: row =
-                // token, contiguous = channel)
-                {
-                    uint32_t krh, krl;
-                    split_pack2(kt0 * R0, kt1 * R1, krh, krl);
-                    const uint32_t off = kda::sw128(r, ch, 64);
-                    *reinterpret_cast<uint32_t*>(blk + WS_KR + off) = krh;
-                    *reinterpret_cast<uint32_t*>(blk + WS_KRL + off) = krl;
-                }
+            for (int j = 0; j < 8; ++j) e[i][j] = __expf(e[i][j] - fb[j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = r0 + i;
+            float q[8], k[8];
+            load_qk(i, q, k);
+            if (PROLOGUE) {                        // unit-length q and k rows
+                const float iq = rsqrtf(nrm[r] + nrm[64 + r] + kda::kNormEps);
+                const float ik = rsqrtf(nrm[128 + r] + nrm[192 + r] + kda::kNormEps);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) { q[j] *= iq; k[j] *= ik; }
             }
-            // tiles m > b hold this block's column factors times a(p_m) / a(p_b) <= 1
-            // (a rolled loop keeps this replicated part of the code small)
-#pragma unroll 1
-            for (int m = b + 1; m < 4; ++m) {
-                const float gs0 = m == 1 ? Gs0[1] : (m == 2 ? Gs0[2] : Gs0[3]);
-                const float gs1 = m == 1 ? Gs1[1] : (m == 2 ? Gs1[2] : Gs1[3]);
-                const float s0 = __expf(gs0 - myG0), s1 = __expf(gs1 - myG1);
-                uint8_t* tile = sm + K1_BG + 1024 * m * (m + 1);        // row 8 m (m + 1), an 8-row atom boundary
+            // each operand row is formed and stored before the next one is formed
+            // (few values live at a time)
+            {
+                float t[8];
 #pragma unroll
-                for (int rr = 0; rr < 8; ++rr)
-                    st_shared_u32(tile + kda::sw128(16 * b + 8 * hf + rr, ch, 160),
-                                  kda::pack_bf16x2(kts[2 * rr] * s0, kts[2 * rr + 1] * s1));
+                for (int j = 0; j < 8; ++j) t[j] = q[j] * e[i][j];            // q~ (row factor)
+                *reinterpret_cast<uint4*>(sm + K1_AG + kda::sw128(32 * b + 4 * rq + i, c0, 128)) = pack8(t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) t[j] *= ap[j];                    // Q_decay
+                // -> rows 0..63 of the [Q_decay; W] image (read back for Q')
+                *reinterpret_cast<uint4*>(blk + WS_A1 + kda::sw128(r, c0, 128)) = pack8(t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) t[j] = bt[i] * k[j] * e[i][j];    // k^ = beta k (row factor)
+                *reinterpret_cast<uint4*>(sm + K1_AG + kda::sw128(32 * b + 16 + 4 * rq + i, c0, 128)) = pack8(t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) t[j] = k[j] * e[i][j] * ap[j];    // K_decay
+                *reinterpret_cast<uint4*>(sm + K1_BWU + kda::sw128(r, c0, 64)) = pack8(t);
+            }
+            float kt[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) kt[j] = k[j] * __fdividef(1.f, e[i][j]);   // k (column factor, own block)
+            // K_restore -> K_restore^T images, high and low bf16 parts (MN-major:
+            // row = token, contiguous = channel)
+            {
+                float kr[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) kr[j] = kt[j] * R[j];
+                uint4 hi, lo;
+                split_pack8(kr, hi, lo);
+                const uint32_t off = kda::sw128(r, c0, 64);
+                *reinterpret_cast<uint4*>(blk + WS_KR + off) = hi;
+                *reinterpret_cast<uint4*>(blk + WS_KRL + off) = lo;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) e[i][j] = kt[j];           // kept for the later tiles
+        }
+        // the column operands overlay the q / k input tiles: every thread has read its rows
+        __syncthreads();
+        // own block's column operand (block b of tile b)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(sm + K1_BG + kda::sw128(8 * b * (b + 1) + r0 + i, c0, 160)) = pack8(e[i]);
+        // tiles m > b hold this block's column factors times a(p_m) / a(p_b) <= 1
+        // (a rolled loop keeps this replicated part of the code small)
+#pragma unroll 1
+        for (int m = b + 1; m < 4; ++m) {
+            float sc[8], gm[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) gm[j] = 0.f;
+            for (int mm = 0; mm < m; ++mm) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) gm[j] += tot[mm * 128 + c0 + j];
+            }
+            float gb[8];                           // this block's reference G_pb
+#pragma unroll
+            for (int j = 0; j < 8; ++j) gb[j] = 0.f;
+            for (int mm = 0; mm < b; ++mm) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) gb[j] += tot[mm * 128 + c0 + j];
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                sc[j] = __expf((gm[j] + first[m * 128 + c0 + j]) - (gb[j] + first[b * 128 + c0 + j]));
+            uint8_t* tile = sm + K1_BG + 1024 * m * (m + 1);        // row 8 m (m + 1), an 8-row atom boundary
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) f[j] = e[i][j] * sc[j];
+                *reinterpret_cast<uint4*>(tile + kda::sw128(16 * b + 4 * rq + i, c0, 160)) = pack8(f);
             }
         }
         kda::fence_proxy_async_all();              // shared operands and the Q_decay rows read back later
@@ -572,7 +657,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
         // ---------------- a2: Gram MMAs: all 128 rows against the 160 stacked B rows
         // (row block b's products sit in columns [8b(b+1), 8b(b+1) + 16(b+1)))
-        if (tid == 0) {
+        if (tid == 0 && !*abort_f) {
             kda::tc_fence_after();
             const uint32_t sAG = kda::smem_u32(sm + K1_AG), sBG = kda::smem_u32(sm + K1_BG);
             const uint32_t idesc = kda::idesc_bf16(128, 160, 0, 0);
@@ -673,7 +758,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         kda::fence_proxy_async_smem();
         kda::tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0 && !*abort_f) {
             kda::tc_fence_after();
             const uint32_t idesc = kda::idesc_bf16(128, 64, 0, 1);
             const uint32_t sA[3] = {kda::smem_u32(sm + K1_MH), kda::smem_u32(sm + K1_MH), kda::smem_u32(sm + K1_ML)};
@@ -727,7 +812,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         __syncthreads();
 
         // ---------------- a3: [W | U0] = INV Diag(beta) [K_decay | V]  (INV in two bf16 parts)
-        if (tid == 0) {
+        if (tid == 0 && !*abort_f) {
             kda::tc_fence_after();
             const uint32_t sB = kda::smem_u32(sm + K1_BWU);
             const uint32_t idesc = kda::idesc_bf16(128, 256, 0, 1);
@@ -805,7 +890,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         kda::tc_fence_before();
         __syncthreads();                           // shared memory and TMEM are reused by the next item
         kda::tc_fence_after();
-        if (tid == 0) {
+        if (tid == 0 && !*abort_f) {
             kda::bulk_s2g(blk + WS_A1, sm + K1_OUT_A1, 32768);
             kda::bulk_s2g(blk + WS_UO, sm + K1_OUT_UO, NTILES * 2 * TILE_F32);
             kda::bulk_commit();

@@ -64,10 +64,10 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
                                                    const volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort || clock64() - t0 > limit) return false;
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15) == 0 && (*abort || clock64() - t0 > limit)) return false;
     }
-    return true;
 }
 
 // ---------------------------------------------------------------- fences
