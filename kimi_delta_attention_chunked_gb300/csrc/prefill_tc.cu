@@ -71,7 +71,7 @@ constexpr int NT = 64;                       // d_v columns per chain CTA
 constexpr int NTILES = DV / NT;
 
 // ---- per (chunk, head) workspace block: images of shared-memory operands
-constexpr uint32_t WS_A1 = 0;                // [Q'; W]       bf16, in the order the chain stores it into TMEM (ap_off)
+constexpr uint32_t WS_A1 = 0;                // [Q'; W]       K-major SW128, 128 rows, K = 128 (2 panels)
 constexpr uint32_t WS_KR = 32768;            // K_restore^T high part, MN-major SW128, K = 64 rows, M = 128 (2 panels)
 constexpr uint32_t WS_KRL = 49152;           //   ... low part, same layout, right after it
 constexpr uint32_t TILE_F32 = C * NT * 4;    // one d_v slice of U0 or O0, fp32, in the order the chain loads it
@@ -84,15 +84,6 @@ constexpr uint32_t WS_BLOCK = 132096;        // 129 KiB
 // together, so that the 32 lanes of a warp load 512 contiguous bytes.
 __host__ __device__ constexpr uint32_t uo_off(uint32_t r, uint32_t c) {
     return ((((c >> 4) * 4u + ((c >> 2) & 3u)) * 64u + r) * 4u + (c & 3u)) * 4u;
-}
-// Byte offset of 32-bit word w (w < 64: the bf16 pair of channels 2 w, 2 w + 1)
-// of row r (r < 128) of the [Q'; W] image.  The chain keeps [Q'; W] in TMEM
-// as an MMA A operand (lane = row, word w in column w); the 16 words a
-// thread stores there are four 16-byte pieces, piece j of 64 rows stored
-// together, so that a warp loads 512 contiguous bytes; Q' (rows 0..63) is the
-// first 16 KiB.
-__host__ __device__ constexpr uint32_t ap_off(uint32_t r, uint32_t w) {
-    return ((((r >> 6) * 16u + (w >> 2)) * 64u + (r & 63u)) * 4u + (w & 3u)) * 4u;
 }
 
 // ---- prep kernel shared memory
@@ -129,39 +120,48 @@ constexpr uint32_t K1_SK = 49152;            // k bf16 [64][128]
 constexpr uint32_t K1_IN_BYTES = 32768 + 2 * 16384 + 16384;
 // output images, assembled once the last MMA has completed (everything below
 // K1_TOT is free then) and written to the workspace by two bulk copies
-constexpr uint32_t K1_OUT_A1 = 0;            // [Q'; W] image, ap_off order (rows 0..63 arrive as Q_decay from the workspace)
+constexpr uint32_t K1_OUT_A1 = 0;            // [Q'; W] image (rows 0..63 arrive as Q_decay from the workspace)
 constexpr uint32_t K1_OUT_UO = 32768;        // [U0 | O0] of both d_v slices, the workspace's WS_UO layout
 
 // ---- chain kernel shared memory
+constexpr int K2_NA = 2;                     // [Q'; W] stages (released as soon as the P product is done)
 constexpr int K2_NB = 2;                     // K_restore^T stages, high and low part (released after the state update)
+constexpr uint32_t K2_ASTAGE = 32768;
 constexpr uint32_t K2_BSTAGE = 32768;
-constexpr uint32_t K2_B0 = 0;                            // B ring: high part at +0, low part at +16384
+constexpr uint32_t K2_B0 = K2_NA * K2_ASTAGE;            // B ring: high part at +0, low part at +16384
 constexpr uint32_t K2_SB = K2_B0 + K2_NB * K2_BSTAGE;    // [S_hi | S_lo] bf16, MN-major SW128, K = 128 rows, N = 2 x 64
 constexpr uint32_t K2_UB = K2_SB + 32768;                // [U_hi | U_lo] bf16, MN-major SW128, K = 64 rows, N = 2 x 64
 constexpr uint32_t K2_OS = K2_UB + 16384;                // one chunk's bf16 output rows [64][64] (16-byte pieces swizzled)
-constexpr uint32_t K2_BAR = K2_OS + 8192;                // full / empty B; p; s; drain; TMEM address; abort flag
+constexpr uint32_t K2_BAR = K2_OS + 8192;                // full / empty A, B; p; s; drain; TMEM address; abort flag
 constexpr uint32_t K2_BYTES = K2_BAR + 128;
-// TMEM: S [0, 64), X [64, 128), P of even chunks [128, 256), of odd [256, 384),
-// [Q'; W] as the P product's A operand [384, 448)
-constexpr uint32_t K2_TMEM_COLS = 512;
-constexpr uint32_t K2_TA = 384;
+constexpr uint32_t K2_TMEM_COLS = 512;       // S [0, 64), X [64, 128), P of even chunks [128, 256), of odd [256, 384)
 
 static_assert(K2_B0 % 1024 == 0 && K2_SB % 1024 == 0 && K2_UB % 1024 == 0, "SW128 operands are 1024-byte aligned");
-static_assert(2 * (K2_BYTES + 1024 + 1024) > 233472, "one state-pass CTA per SM (it takes all of TMEM)");
 static_assert(WS_KRL == WS_KR + 16384, "both parts of K_restore^T are one contiguous copy");
 static_assert(K1_AIL + 16384 <= K1_BWU, "[INV; X] must stay inside the alias region");
 static_assert(K1_ML + 16384 <= K1_BWU && K1_IL + 8192 <= K1_IS, "X operands stay inside the alias region");
 static_assert(K1_OUT_UO + NTILES * 2 * TILE_F32 <= K1_TOT && K1_OUT_A1 + 32768 <= K1_OUT_UO, "output images");
 static_assert(K1_BAR + 48 <= K1_NRM, "prep barriers and flags");
 static_assert(K1_SK + 16384 <= K1_BWU && (K1_BWU + 16384) % 1024 == 0, "input tiles");
-static_assert(K1_OUT_A1 + 16384 <= K1_XS, "Q_decay rows land in the free L / INV region while the last MMA runs");
+static_assert(K1_IS + 64 * LDS_ * 4 <= K1_XS && K1_XS + 4096 <= K1_MH && 16384 + 8192 <= K1_XS,
+              "Q_decay rows land in the free L / INV region while the last MMA runs");
 static_assert(WS_BLOCK % 1024 == 0 && WS_AL + DK * 4 <= WS_BLOCK, "workspace block");
 static_assert(K2_BYTES + 1024 + 256 <= 232448, "chain smem");
-static_assert(K2_BAR + 7 * 8 + 8 <= K2_BYTES, "chain barriers and flags");
+static_assert(K2_BAR + 11 * 8 + 8 <= K2_BYTES, "chain barriers and flags");
 static_assert(2 * (K1_BYTES + 1024 + 1024) <= 233472, "prep must fit two CTAs per SM");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void st_shared_u32(uint8_t* p, uint32_t x) { *reinterpret_cast<uint32_t*>(p) = x; }
+
+// (a, b) as a high / low pair of packed bf16x2 words: high = a, b truncated to
+// bf16, low = bf16 of the remainders (see split_pack8).
+__device__ __forceinline__ void split_pack2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+    hi = __byte_perm(ua, ub, 0x7632);
+    lo = kda::pack_bf16x2(a - __uint_as_float(ua & 0xFFFF0000u), b - __uint_as_float(ub & 0xFFFF0000u));
 }
 
 // x = hi + lo with hi = x truncated to bf16 and lo = bf16(x - hi): the pair
@@ -589,7 +589,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
                 for (int j = 0; j < 8; ++j) t[j] *= ap[j];                    // Q_decay
                 // -> rows 0..63 of the [Q_decay; W] image (read back for Q')
-                *reinterpret_cast<uint4*>(blk + WS_A1 + ap_off(r, c0 >> 1)) = pack8(t);
+                *reinterpret_cast<uint4*>(blk + WS_A1 + kda::sw128(r, c0, 128)) = pack8(t);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) t[j] = bt[i] * k[j] * e[i][j];    // k^ = beta k (row factor)
                 *reinterpret_cast<uint4*>(sm + K1_AG + kda::sw128(32 * b + 16 + 4 * rq + i, c0, 128)) = pack8(t);
@@ -827,9 +827,10 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
             }
             kda::umma_commit(bar);
-            // meanwhile, the Q_decay rows back into the [Q'; W] image (its first 16 KiB)
+            // meanwhile, the Q_decay rows (both 64-channel panels) back into the [Q'; W] image
             kda::mbar_arrive_expect_tx(bar_q, 16384);
-            kda::bulk_g2s(sm + K1_OUT_A1, blk + WS_A1, 16384, bar_q);
+            kda::bulk_g2s(sm + K1_OUT_A1, blk + WS_A1, 8192, bar_q);
+            kda::bulk_g2s(sm + K1_OUT_A1 + 16384, blk + WS_A1 + 16384, 8192, bar_q);
             ++n_qloads;
         }
         wait(bar, bar_phase & 1);
@@ -847,7 +848,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 kda::tmem_wait_ld();
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    *reinterpret_cast<uint4*>(sm + K1_OUT_A1 + ap_off(64 + r, 16 * cb + 4 * u)) = pack8(x + 8 * u);
+                    *reinterpret_cast<uint4*>(sm + K1_OUT_A1 + kda::sw128(64 + r, 32 * cb + 8 * u, 128)) = pack8(x + 8 * u);
             }
         } else if (w == 2 || w == 3) {             // Q' = Q_decay - M_qk W -> rows 0..63 of [Q'; W]
             wait(bar_q, n_done & 1);
@@ -858,7 +859,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 kda::tmem_wait_ld();
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    uint4* qp = reinterpret_cast<uint4*>(sm + K1_OUT_A1 + ap_off(r, 16 * cb + 4 * u));
+                    uint4* qp = reinterpret_cast<uint4*>(sm + K1_OUT_A1 + kda::sw128(r, 32 * cb + 8 * u, 128));
                     const uint4 qd = *qp;
                     const uint32_t qs[4] = {qd.x, qd.y, qd.z, qd.w};
 #pragma unroll
@@ -916,13 +917,12 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // ============================================================== chain (a4, a5)
 // Per CTA: one (sequence, head) pair and NT = 64 columns of d_v.  TMEM columns:
 //   [0, 64)      S, the fp32 state slice (TMEM lane = key channel)
-//   [64, 128)    X, the low-part share of the state update, folded into S
-//                when the state is next read
+//   [64, 128)    X, the low-part share K_restore^T U_lo of the state update,
+//                folded into S when the state is next read
 //   [128, 256)   P of even chunks, [256, 384) P of odd chunks:
 //                P = [Q'; W] [S_hi | S_lo]: columns 0..63 against the high
 //                part of S_in, 64..127 against its low part; lanes 0..63
 //                Q' S_in, lanes 64..127 W S_in
-//   [384, 448)   [Q'; W] of the current chunk, bf16, the A operand of P
 // MMAs per chunk (16 instructions):
 //   P        = [Q'; W] [S_hi | S_lo]                        K = 128, N = 128 -> commit(p)
 //   [S | X] += K_hi^T [U_hi | U_lo] + K_lo^T [U_hi | U_lo]  K = 64,  N = 128 -> commit(s)
@@ -933,28 +933,24 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // gate range it would otherwise add up over the sequence.  Q' = Q_decay -
 // M_qk W and O0 = M_qk U0 come from the prep kernel, so O = Q_decay S_in +
 // M_qk U needs no product of its own here.
-// K_restore^T streams through a two-stage ring filled by bulk copies.  [Q'; W]
-// goes global -> registers -> TMEM: the conversion warps load the next chunk's
-// rows while this one runs and store them once this chunk's P product is done,
-// which keeps 32 KiB per chunk of copies off the shared-memory path the MMAs
-// read.  U0, O0 and a_last are loaded straight into the registers of the
-// threads that use them; the bulk-copy warp prefetches each chunk's blocks
-// into L2 ahead of them.  P alternates between two TMEM buffers, so the output
-// rows of chunk c are formed while chunk c + 1 runs, off the sequential path.
+// [Q'; W] and K_restore^T stream through two rings filled by bulk copies;
+// U0, O0 and a_last are loaded straight into the registers of the threads
+// that use them, a chunk ahead.  P alternates between two TMEM buffers, so the
+// output rows of chunk c are formed while chunk c + 1 runs, off the sequential
+// path.
 // Warp roles:
 //   warps 0-15 conversion warps; warp w reads TMEM lanes 32 (w % 4) .. +31 and
 //              columns 16 (w / 4) .. +15 of each 64-wide block (four warps per
 //              sub-partition, so that their latencies overlap).
 //              - all 16: S_in = S + X -> high/low bf16 operand; then
-//                S <- Diag(a_last) S_in, X <- 0; [Q'; W] rows of the next chunk
+//                S <- Diag(a_last) S_in, X <- 0
 //              - lanes 64..127 (w % 4 = 2, 3): U = U0 - W S_in -> high/low bf16 operand
 //              - lanes 0..63 (w % 4 = 0, 1): O rows of the previous chunk =
 //                Q' S_in + O0, staged in shared memory and stored row by row
 //   warp 16    lane 0 issues the MMAs
-//   warp 17    lane 0 issues the bulk copies and the L2 prefetches
-// Named barriers (warps 0-16): 1 = S_in and [Q'; W] ready; 2 = conversion
-// warps arrive, the issuer waits (U ready, state rescaled); 3 = the eight O
-// warps (output staging).
+//   warp 17    lane 0 issues the bulk copies
+// Named barriers (warps 0-16): 1 = S_in ready; 2 = conversion warps arrive, the
+// issuer waits (U ready, state rescaled); 3 = the eight O warps (output staging).
 // A wait that runs out sets the CTA's abort flag: from then on no copy or MMA
 // is issued, every other wait returns at once, and before the CTA exits the
 // copies and MMAs already in flight are waited for (bounded again).
@@ -1016,7 +1012,9 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     };
     auto block_of = [&](int c) { return ws_blocks + ((size_t)(first + cb + c) * H + h) * WS_BLOCK; };
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    uint64_t* fullB = reinterpret_cast<uint64_t*>(sm + K2_BAR);
+    uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + K2_BAR);
+    uint64_t* emptyA = fullA + K2_NA;
+    uint64_t* fullB = emptyA + K2_NA;
     uint64_t* emptyB = fullB + K2_NB;
     uint64_t* bar_p = emptyB + K2_NB;
     uint64_t* bar_s = bar_p + 1;
@@ -1028,7 +1026,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         kda::tmem_relinquish();
     }
     if (tid == 0) {
-        // a stage is free once the MMAs that read it are done (one commit)
+        // a stage is free once the MMAs that read it are done (one commit each)
+        for (int s = 0; s < K2_NA; ++s) { kda::mbar_init(fullA + s, 1); kda::mbar_init(emptyA + s, 1); }
         for (int s = 0; s < K2_NB; ++s) { kda::mbar_init(fullB + s, 1); kda::mbar_init(emptyB + s, 1); }
         kda::mbar_init(bar_p, 1);
         kda::mbar_init(bar_s, 1);
@@ -1048,30 +1047,31 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     };
 
     if (w == K2_PRODUCER_WARP) {
-        // ---------------- bulk copies of K_restore^T, in chunk order; L2 prefetches
+        // ---------------- bulk copies, in the order the chunks need them
         if (lane == 0) {
-            // chunk c's [Q'; W] image, U0 / O0 tiles and a_last, which the
-            // conversion warps load into registers a chunk ahead, into L2
-            auto prefetch = [&](int c) {
-                if (c >= nloc) return;
-                kda::bulk_prefetch_l2(block_of(c) + WS_A1, 32768);
-                kda::bulk_prefetch_l2(block_of(c) + WS_UO + 2 * TILE_F32 * tile, 2 * TILE_F32);
-                kda::bulk_prefetch_l2(block_of(c) + WS_AL, DK * 4);
-            };
-            prefetch(0);
-            prefetch(1);
-            int nB = 0;                                     // copies issued
+            int nA = 0, nB = 0;                             // copies issued into each ring
             for (int k = 0; k < nloc && !*abort_f; ++k) {
+                const int sa = k % K2_NA;
+                if (k >= K2_NA) wait(emptyA + sa, (uint32_t)(((k - K2_NA) / K2_NA) & 1));
+                if (*abort_f) break;
+                kda::mbar_arrive_expect_tx(fullA + sa, K2_ASTAGE);
+                kda::bulk_g2s(sm + sa * K2_ASTAGE, block_of(k) + WS_A1, K2_ASTAGE, fullA + sa);
+                ++nA;
+                // the U0 / O0 tiles and a_last of this chunk, which the conversion
+                // warps load into registers when the chunk comes up, into L2
+                kda::bulk_prefetch_l2(block_of(k) + WS_UO + 2 * TILE_F32 * tile, 2 * TILE_F32);
+                kda::bulk_prefetch_l2(block_of(k) + WS_AL, DK * 4);
                 const int sb = k % K2_NB;
                 if (k >= K2_NB) wait(emptyB + sb, (uint32_t)(((k - K2_NB) / K2_NB) & 1));
                 if (*abort_f) break;
                 kda::mbar_arrive_expect_tx(fullB + sb, K2_BSTAGE);
                 kda::bulk_g2s(sm + K2_B0 + sb * K2_BSTAGE, block_of(k) + WS_KR, K2_BSTAGE, fullB + sb);
                 ++nB;
-                prefetch(k + 2);
             }
             if (*abort_f) {
                 // the last copy into each stage completes that stage's newest phase
+                for (int k = max(0, nA - K2_NA); k < nA; ++k)
+                    (void)kda::mbar_wait(fullA + k % K2_NA, (uint32_t)((k / K2_NA) & 1), kda::kWaitCycles);
                 for (int k = max(0, nB - K2_NB); k < nB; ++k)
                     (void)kda::mbar_wait(fullB + k % K2_NB, (uint32_t)((k / K2_NB) & 1), kda::kWaitCycles);
             }
@@ -1081,18 +1081,22 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         const uint32_t sSB = kda::smem_u32(sm + K2_SB), sUB = kda::smem_u32(sm + K2_UB);
         named_bar_sync(1, K2_SYNC);                        // initial state in TMEM
         for (int c = 0; c < nloc; ++c) {
-            const int sb = c % K2_NB;
+            const int sa = c % K2_NA, sb = c % K2_NB;
+            if (lane == 0) wait(fullA + sa, (uint32_t)((c / K2_NA) & 1));
             __syncwarp();
-            named_bar_sync(1, K2_SYNC);                    // S_in (shared memory) and [Q'; W] (TMEM) ready
+            named_bar_sync(1, K2_SYNC);
             if (lane == 0 && !*abort_f) {                   // P = [Q'; W] [S_hi | S_lo]
                 kda::tc_fence_after();
+                const uint32_t sA1 = kda::smem_u32(sm + sa * K2_ASTAGE);
                 const uint32_t idesc = kda::idesc_bf16(128, 2 * NT, 0, 1);
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
+                    const uint64_t ad = kda::sw128_desc(sA1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
                     const uint64_t bd = kda::sw128_desc(sSB + s * 2048, 16384, 1024);
-                    kda::umma_bf16_tmem_a(tmem + 128 + 128 * (c & 1), tmem + K2_TA + 8 * s, bd, idesc, s > 0 ? 1u : 0u);
+                    kda::umma_bf16(tmem + 128 + 128 * (c & 1), ad, bd, idesc, s > 0 ? 1u : 0u);
                 }
                 kda::umma_commit(bar_p);
+                kda::umma_commit(emptyA + sa);
             }
             if (lane == 0) wait(fullB + sb, (uint32_t)((c / K2_NB) & 1));
             __syncwarp();
@@ -1125,7 +1129,6 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
         const uint32_t tS = tmem + lane_off + col0;             // this warp's state columns (X at +64)
         const uint32_t tP = tmem + lane_off + 128 + col0;       // ... of P (buffer of chunk parity at +128)
-        const uint32_t tA = tmem + lane_off + K2_TA + col0;     // ... of [Q'; W] (16 of its 64 columns)
         const bool u_rows = quad >= 2;                          // lanes 64..127: U; lanes 0..63: O
         // this thread's 16 values of U0 (U rows) or O0 (O rows) of local chunk c
         auto load_uo = [&](int c, float* dst) {
@@ -1136,19 +1139,6 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 const float4 x = *reinterpret_cast<const float4*>(base + uo_off(r, col0 + 4 * j));
                 dst[4 * j] = x.x; dst[4 * j + 1] = x.y; dst[4 * j + 2] = x.z; dst[4 * j + 3] = x.w;
             }
-        };
-        // this thread's 16 words of row `row` of chunk c's [Q'; W]
-        auto load_ap = [&](int c, uint32_t* dst) {
-            const uint8_t* base = block_of(c) + WS_A1;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint4 x = *reinterpret_cast<const uint4*>(base + ap_off(row, col0 + 4 * j));
-                dst[4 * j] = x.x; dst[4 * j + 1] = x.y; dst[4 * j + 2] = x.z; dst[4 * j + 3] = x.w;
-            }
-        };
-        auto store_ap = [&](const uint32_t* a) {
-            kda::tmem_st16(tA, reinterpret_cast<const float*>(a));
-            kda::tmem_wait_st();
         };
         // O rows of chunk co (lanes 0..63 warps): P of that chunk is complete (the
         // state update issued after it is); staged in shared memory and stored
@@ -1189,7 +1179,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             kda::tc_fence_before();
         };
         {
-            // initial state slice -> TMEM (X = 0); the first chunk's [Q'; W]
+            // initial state slice -> TMEM (X = 0)
             float s[K2_CW];
             if (run_map) {
 #pragma unroll
@@ -1210,11 +1200,6 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
 #pragma unroll
             for (int u = 0; u < K2_CW; ++u) s[u] = 0.f;
             kda::tmem_st16(tS + 64, s);
-            if (nloc > 0) {
-                uint32_t a0[K2_CW];
-                load_ap(0, a0);
-                kda::tmem_st16(tA, reinterpret_cast<const float*>(a0));
-            }
             kda::tmem_wait_st();
             kda::tc_fence_before();
             named_bar_sync(1, K2_SYNC);
@@ -1228,9 +1213,6 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             if (c + 1 < nloc) al_next = reinterpret_cast<const float*>(block_of(c + 1) + WS_AL)[row];
             float uo[K2_CW];                                    // U0 (U rows) or O0 (O rows) of this chunk
             load_uo(c, uo);
-            uint32_t an[K2_CW];                                 // next chunk's [Q'; W] words of this row
-            const bool has_next = c + 1 < nloc;
-            if (has_next) load_ap(c + 1, an);
             // ---- S_in = S + X -> high/low bf16 operand
             if (c > 0) wait(bar_s, (uint32_t)((c - 1) & 1));
             kda::tc_fence_after();
@@ -1262,7 +1244,6 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 // ---- U = U0 - W S_in -> high/low bf16 operand
                 wait(bar_p, (uint32_t)(c & 1));
                 kda::tc_fence_after();
-                if (has_next) store_ap(an);                     // P is done with this chunk's [Q'; W]
                 const int r = row - 64;
                 float ph[K2_CW], pl[K2_CW];
                 kda::tmem_ld16(tP + 128 * (c & 1), ph);
@@ -1286,13 +1267,9 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             } else {
                 kda::tc_fence_before();
                 named_bar_arrive(2, K2_SYNC);
-                wait(bar_p, (uint32_t)(c & 1));
-                kda::tc_fence_after();
-                if (has_next) store_ap(an);                     // P is done with this chunk's [Q'; W]
                 if (c > 0) out_rows(c - 1, uo_prev);            // the previous chunk's output
 #pragma unroll
                 for (int u = 0; u < K2_CW; ++u) uo_prev[u] = uo[u];
-                kda::tc_fence_before();
             }
         }
         if (nloc > 0) wait(bar_s, (uint32_t)((nloc - 1) & 1));
