@@ -87,16 +87,16 @@ __host__ __device__ constexpr uint32_t uo_off(uint32_t r, uint32_t c) {
 }
 
 // ---- prep kernel shared memory
-constexpr uint32_t K1_AG = 0;                // Gram A: 128 rows [q~ b0 | k^ b0 | q~ b1 | ...], K = 128
-constexpr uint32_t K1_BG = 32768;            // Gram B: tiles b = 0..3 (16(b+1) rows each) stacked along N
+constexpr uint32_t K1_BG = 0;                // Gram B: tiles b = 0..3 (16(b+1) rows each) stacked along N
                                              // at row 8b(b+1): one 160-row K-major tile, K = 128
+constexpr uint32_t K1_AG = 40960;            // Gram A: 128 rows [q~ b0 | k^ b0 | q~ b1 | ...], K = 128
 constexpr uint32_t K1_BWU = 73728;           // [K_decay | V]: MN-major, K = 64 rows, N = 256 (4 panels)
 constexpr uint32_t K1_TOT = 106496;          // float [4][128] block totals of log-decay
 constexpr uint32_t K1_FIRST = 108544;        // float [4][128] first-row log-decay of each block
 constexpr uint32_t K1_BETA = 110592;         // float [64]
 constexpr uint32_t K1_BAR = 110848;          // MMA mbarrier (8 B), TMEM address (4 B), Q_decay copy mbarrier at +16,
-                                             // input copy mbarrier at +24, abort flag (4 B) at +32, drain
-                                             // mbarrier at +40
+                                             // log-decay and V copy mbarrier at +24, abort flag (4 B) at +32,
+                                             // drain mbarrier at +40, q and k copy mbarrier at +48
 constexpr uint32_t K1_NRM = 110912;          // fused prologue: float [q, k][channel half][64 rows] sums of squares
 constexpr uint32_t K1_BYTES = 111936;
 // aliases, valid once the Gram MMAs have completed
@@ -112,16 +112,20 @@ constexpr uint32_t K1_AI = 38912;            // [INV; X] Diag(beta), high bf16 p
 constexpr uint32_t K1_AIL = 55296;           // ... low bf16 part (both written once the X product is done)
 constexpr uint32_t K1_TMEM_COLS = 256;
 constexpr uint32_t K1_TX = 160;              // TMEM columns of X = M_qk INV (lanes 0..63)
-// input tiles of an item, copied by TMA over the Gram operands' space (read into
-// registers before the operands are written); V lands in its operand slot
-constexpr uint32_t K1_SG = 0;                // log-decay fp32 [64 tokens][128]
-constexpr uint32_t K1_SQ = 32768;            // q bf16 [64][128]
-constexpr uint32_t K1_SK = 49152;            // k bf16 [64][128]
-constexpr uint32_t K1_IN_BYTES = 32768 + 2 * 16384 + 16384;
-// output images, assembled once the last MMA has completed (everything below
-// K1_TOT is free then) and written to the workspace by two bulk copies
+// input tiles of an item, copied by TMA over the Gram operands' space.  The
+// log-decay tile (under the Gram A operand, read into registers before that is
+// written) and V (straight into its operand slot) of the next item are copied
+// while this item's epilogue runs; q and k (under the Gram B operand, which is
+// written after every thread has read its rows) once this item's [Q'; W] image
+// has been read out, behind the cumulative sum of the next item.
+constexpr uint32_t K1_SG = 40960;            // log-decay fp32 [64 tokens][128]
+constexpr uint32_t K1_SQ = 0;                // q bf16 [64][128]
+constexpr uint32_t K1_SK = 16384;            // k bf16 [64][128]
+constexpr uint32_t K1_GV_BYTES = 32768 + 16384;   // log-decay and V
+constexpr uint32_t K1_QK_BYTES = 2 * 16384;       // q and k
+// output image, assembled once the last MMA has completed and written to the
+// workspace by one bulk copy (U0 and O0 go from registers straight to the workspace)
 constexpr uint32_t K1_OUT_A1 = 0;            // [Q'; W] image (rows 0..63 arrive as Q_decay from the workspace)
-constexpr uint32_t K1_OUT_UO = 32768;        // [U0 | O0] of both d_v slices, the workspace's WS_UO layout
 
 // ---- chain kernel shared memory
 constexpr int K2_NA = 2;                     // [Q'; W] stages (released as soon as the P product is done)
@@ -140,9 +144,12 @@ static_assert(K2_B0 % 1024 == 0 && K2_SB % 1024 == 0 && K2_UB % 1024 == 0, "SW12
 static_assert(WS_KRL == WS_KR + 16384, "both parts of K_restore^T are one contiguous copy");
 static_assert(K1_AIL + 16384 <= K1_BWU, "[INV; X] must stay inside the alias region");
 static_assert(K1_ML + 16384 <= K1_BWU && K1_IL + 8192 <= K1_IS, "X operands stay inside the alias region");
-static_assert(K1_OUT_UO + NTILES * 2 * TILE_F32 <= K1_TOT && K1_OUT_A1 + 32768 <= K1_OUT_UO, "output images");
-static_assert(K1_BAR + 48 <= K1_NRM, "prep barriers and flags");
-static_assert(K1_SK + 16384 <= K1_BWU && (K1_BWU + 16384) % 1024 == 0, "input tiles");
+static_assert(K1_OUT_A1 + 32768 <= K1_SG, "the next log-decay tile does not touch the [Q'; W] image");
+static_assert(K1_BAR + 56 <= K1_NRM, "prep barriers and flags");
+static_assert(K1_BG + 160 * 256 <= K1_AG && K1_AG + 32768 == K1_BWU && K1_AG % 1024 == 0, "Gram operands");
+static_assert(K1_SK + 16384 <= K1_AG && K1_SG + 32768 <= K1_BWU && (K1_BWU + 16384) % 1024 == 0, "input tiles");
+static_assert(K1_AIL + 16384 <= K1_SG + 32768 && K1_ML + 16384 <= K1_SG + 32768,
+              "the next log-decay tile lands where only the last MMA's A operand was");
 static_assert(K1_IS + 64 * LDS_ * 4 <= K1_XS && K1_XS + 4096 <= K1_MH && 16384 + 8192 <= K1_XS,
               "Q_decay rows land in the free L / INV region while the last MMA runs");
 static_assert(WS_BLOCK % 1024 == 0 && WS_AL + DK * 4 <= WS_BLOCK, "workspace block");
@@ -365,9 +372,10 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + K1_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + K1_BAR + 8);
     uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + K1_BAR + 16);
-    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + K1_BAR + 24);
+    uint64_t* bar_gv = reinterpret_cast<uint64_t*>(sm + K1_BAR + 24);
     volatile int* abort_f = reinterpret_cast<volatile int*>(sm + K1_BAR + 32);
     uint64_t* bar_drain = reinterpret_cast<uint64_t*>(sm + K1_BAR + 40);
+    uint64_t* bar_qk = reinterpret_cast<uint64_t*>(sm + K1_BAR + 48);
     if (w == 0) {
         kda::tmem_alloc(tmem_slot, K1_TMEM_COLS);
         kda::tmem_relinquish();
@@ -375,14 +383,24 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     if (tid == 0) {
         kda::mbar_init(bar, 1);
         kda::mbar_init(bar_q, 1);
-        kda::mbar_init(bar_ld, 1);
+        kda::mbar_init(bar_gv, 1);
+        kda::mbar_init(bar_qk, 1);
         kda::mbar_init(bar_drain, 1);
         kda::fence_barrier_init();
         *abort_f = 0;
     }
     uint32_t n_done = 0;                          // items finished by this CTA (bar_q parity)
     uint32_t bar_phase = 0;                       // completed phases of bar (three per item)
-    uint32_t n_loads = 0, n_qloads = 0;           // input / Q_decay copy phases issued (thread 0)
+    uint32_t n_gv = 0, n_qk = 0, n_qloads = 0;    // copy phases issued (thread 0): log-decay and V, q and k, Q_decay
+    // log-decay tile and V of item `it` into shared memory (thread 0)
+    auto load_gv = [&](int t0, int hh) {
+        kda::mbar_arrive_expect_tx(bar_gv, K1_GV_BYTES);
+        kda::tma_load_3d(sm + K1_SG, &tm_g, 0, hh, t0, bar_gv);
+        kda::tma_load_3d(sm + K1_BWU + 16384, &tm_v, 0, hh, t0, bar_gv);
+        kda::tma_load_3d(sm + K1_BWU + 16384 + 8192, &tm_v, 64, hh, t0, bar_gv);
+        ++n_gv;
+    };
+    bool gv_ready = false;                        // thread 0: this item's log-decay and V already issued
     // Bounded wait.  Once one runs out (or another thread's did) the CTA
     // issues no further copy or MMA: the remaining items run through without
     // waiting, and what is in flight is drained before the CTA exits.
@@ -410,23 +428,23 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         // shuffles.
         const int b = w >> 1, p = w & 1, cg = lane & 7, rq = lane >> 3;
         const int c0 = 64 * p + 8 * cg, r0 = 16 * b + 4 * rq;
-        // inputs: one TMA copy per tensor (V straight into its operand slot, both
-        // 64-channel panels) once the previous item's output images have left
-        // shared memory; rows past the end of the tensor read as zero
+        // inputs: one TMA copy per tensor, rows past the end of the tensor read
+        // as zero.  The log-decay tile and V were copied during the previous
+        // item's epilogue (the first item's are copied here); q and k once the
+        // previous item's [Q'; W] image has left shared memory.
         if (tid == 0 && !*abort_f) {
+            if (!gv_ready) load_gv(tok0, h);
             kda::bulk_wait_read_all();
-            kda::mbar_arrive_expect_tx(bar_ld, K1_IN_BYTES);
-            kda::tma_load_3d(sm + K1_SG, &tm_g, 0, h, tok0, bar_ld);
-            kda::tma_load_3d(sm + K1_SQ, &tm_q, 0, h, tok0, bar_ld);
-            kda::tma_load_3d(sm + K1_SK, &tm_k, 0, h, tok0, bar_ld);
-            kda::tma_load_3d(sm + K1_BWU + 16384, &tm_v, 0, h, tok0, bar_ld);
-            kda::tma_load_3d(sm + K1_BWU + 16384 + 8192, &tm_v, 64, h, tok0, bar_ld);
-            ++n_loads;
+            kda::mbar_arrive_expect_tx(bar_qk, K1_QK_BYTES);
+            kda::tma_load_3d(sm + K1_SQ, &tm_q, 0, h, tok0, bar_qk);
+            kda::tma_load_3d(sm + K1_SK, &tm_k, 0, h, tok0, bar_qk);
+            ++n_qk;
         }
+        gv_ready = false;
         float bt[4];                               // beta of this thread's rows
 #pragma unroll
         for (int i = 0; i < 4; ++i) bt[i] = beta[((size_t)tok0 + min(r0 + i, nrows - 1)) * H + h];
-        wait(bar_ld, n_done & 1);
+        wait(bar_gv, n_done & 1);
         float e[4][8];                             // log-decay, then its cumulative sum, then staged factors
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -466,6 +484,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         __syncthreads();                           // the log-decay tile is in registers
         float* nrm = reinterpret_cast<float*>(sm + K1_NRM);
         if (PROLOGUE) {
+            wait(bar_qk, n_done & 1);
             // fused prologue: gates from their pre-activations; squared norms of
             // the q and k rows over this panel's 64 channels
 #pragma unroll
@@ -561,6 +580,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             *reinterpret_cast<float4*>(blk + WS_AL + 4 * c0 + 16) = make_float4(al[4], al[5], al[6], al[7]);
         }
 
+        if (!PROLOGUE) wait(bar_qk, n_done & 1);   // q and k (copied behind the cumulative sum)
         // ---------------- a1: operands, row by row.  Row factors exp(G_r - G_pb) <= 1,
         // column factors exp(G_pb - G_t) >= 1 (<= e^75), with p_b the block's first row
 #pragma unroll
@@ -837,6 +857,17 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         ++bar_phase;
         kda::tc_fence_after();
 
+        // the last MMA is done with its operands: the next item's log-decay tile
+        // (over the [INV; X] operand) and V (over this item's V) can come in
+        if (tid == 0 && !*abort_f) {
+            for (long long nx = it + gridDim.x; nx < n_items; nx += gridDim.x) {
+                int t1, r1, s1, h1;
+                if (!item(nx, t1, r1, s1, h1)) continue;
+                load_gv(t1, h1);
+                gv_ready = true;
+                break;
+            }
+        }
         // TMEM lanes 0..63 hold [W | U0], lanes 64..127 hold [M_qk W | O0] (columns 0..127 | 128..255)
         const int quad = w & 3, r = 32 * (quad & 1) + lane;
         const uint32_t t_row = tmem + ((uint32_t)(32 * quad) << 16) + (w >= 4 ? 128u : 0u);
@@ -871,15 +902,15 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     *qp = pack8(x + 8 * u);
                 }
             }
-        } else {                                   // U0 (warps 4, 5) or O0 (warps 6, 7) rows, fp32, per d_v slice
-            const uint32_t part = w < 6 ? 0u : TILE_F32;
+        } else {                                   // U0 (warps 4, 5) or O0 (warps 6, 7) rows, fp32, per d_v slice,
+            const uint32_t part = w < 6 ? 0u : TILE_F32;   // straight to the workspace (512 contiguous bytes a warp)
 #pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
                 float x[32];
                 kda::tmem_ld32(t_row + 32 * cb, x);
                 kda::tmem_wait_ld();
                 const int tile = (32 * cb) / NT, c0 = (32 * cb) % NT;
-                uint8_t* dst = sm + K1_OUT_UO + 2 * TILE_F32 * tile + part;
+                uint8_t* dst = blk + WS_UO + 2 * TILE_F32 * tile + part;
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     *reinterpret_cast<float4*>(dst + uo_off(r, c0 + 4 * u)) =
@@ -892,7 +923,6 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         kda::tc_fence_after();
         if (tid == 0 && !*abort_f) {
             kda::bulk_s2g(blk + WS_A1, sm + K1_OUT_A1, 32768);
-            kda::bulk_s2g(blk + WS_UO, sm + K1_OUT_UO, NTILES * 2 * TILE_F32);
             kda::bulk_commit();
         }
         ++n_done;
@@ -901,7 +931,8 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (*abort_f) {
             // a wait ran out: let the copies and MMAs already issued finish
             // (bounded again) before the shared memory and TMEM are released
-            if (n_loads) (void)kda::mbar_wait(bar_ld, (n_loads - 1) & 1, kda::kWaitCycles);
+            if (n_gv) (void)kda::mbar_wait(bar_gv, (n_gv - 1) & 1, kda::kWaitCycles);
+            if (n_qk) (void)kda::mbar_wait(bar_qk, (n_qk - 1) & 1, kda::kWaitCycles);
             if (n_qloads) (void)kda::mbar_wait(bar_q, (n_qloads - 1) & 1, kda::kWaitCycles);
             kda::umma_commit(bar_drain);           // arrives once every MMA issued so far is done
             (void)kda::mbar_wait(bar_drain, 0, kda::kWaitCycles);
