@@ -57,6 +57,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -136,8 +137,11 @@ constexpr uint32_t K2_B0 = K2_NA * K2_ASTAGE;            // B ring: high part at
 constexpr uint32_t K2_SB = K2_B0 + K2_NB * K2_BSTAGE;    // [S_hi | S_lo] bf16, MN-major SW128, K = 128 rows, N = 2 x 64
 constexpr uint32_t K2_UB = K2_SB + 32768;                // [U_hi | U_lo] bf16, MN-major SW128, K = 64 rows, N = 2 x 64
 constexpr uint32_t K2_OS = K2_UB + 16384;                // one chunk's bf16 output rows [64][64] (16-byte pieces swizzled)
-constexpr uint32_t K2_BAR = K2_OS + 8192;                // full / empty A, B; p; s; drain; TMEM address; abort flag
-constexpr uint32_t K2_BYTES = K2_BAR + 128;
+constexpr uint32_t K2_U0 = K2_OS + 8192;                 // U0 tile of this slice (fp32, workspace order), one chunk
+constexpr uint32_t K2_O0 = K2_U0 + TILE_F32;             // O0 tile of this slice, one chunk
+constexpr uint32_t K2_BAR = K2_O0 + TILE_F32;            // full / empty A, B; p; s; drain; full / empty U0, O0;
+                                                         // TMEM address; abort flag
+constexpr uint32_t K2_BYTES = K2_BAR + 192;
 constexpr uint32_t K2_TMEM_COLS = 512;       // S [0, 64), X [64, 128), P of even chunks [128, 256), of odd [256, 384)
 
 static_assert(K2_B0 % 1024 == 0 && K2_SB % 1024 == 0 && K2_UB % 1024 == 0, "SW128 operands are 1024-byte aligned");
@@ -154,7 +158,8 @@ static_assert(K1_IS + 64 * LDS_ * 4 <= K1_XS && K1_XS + 4096 <= K1_MH && 16384 +
               "Q_decay rows land in the free L / INV region while the last MMA runs");
 static_assert(WS_BLOCK % 1024 == 0 && WS_AL + DK * 4 <= WS_BLOCK, "workspace block");
 static_assert(K2_BYTES + 1024 + 256 <= 232448, "chain smem");
-static_assert(K2_BAR + 11 * 8 + 8 <= K2_BYTES, "chain barriers and flags");
+static_assert(K2_BAR + 15 * 8 + 8 <= K2_BYTES, "chain barriers and flags");
+static_assert(K2_OS % 1024 == 0, "the output tile is stored by a 128-byte-swizzled tensor copy");
 static_assert(2 * (K1_BYTES + 1024 + 1024) <= 233472, "prep must fit two CTAs per SM");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -965,10 +970,11 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // M_qk W and O0 = M_qk U0 come from the prep kernel, so O = Q_decay S_in +
 // M_qk U needs no product of its own here.
 // [Q'; W] and K_restore^T stream through two rings filled by bulk copies;
-// U0, O0 and a_last are loaded straight into the registers of the threads
-// that use them, a chunk ahead.  P alternates between two TMEM buffers, so the
-// output rows of chunk c are formed while chunk c + 1 runs, off the sequential
-// path.
+// the U0 and O0 tiles of the slice arrive by bulk copy too (one chunk each),
+// and the output rows leave by a tensor store, so that the conversion warps
+// have no global loads or stores in flight at their proxy fences.  P
+// alternates between two TMEM buffers, so the output rows of chunk c are
+// formed while chunk c + 1 runs, off the sequential path.
 // Warp roles:
 //   warps 0-15 conversion warps; warp w reads TMEM lanes 32 (w % 4) .. +31 and
 //              columns 16 (w / 4) .. +15 of each 64-wide block (four warps per
@@ -979,7 +985,8 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 //              - lanes 0..63 (w % 4 = 0, 1): O rows of the previous chunk =
 //                Q' S_in + O0, staged in shared memory and stored row by row
 //   warp 16    lane 0 issues the MMAs
-//   warp 17    lane 0 issues the bulk copies
+//   warp 17    lane 0 issues the bulk copies of the two rings
+//   warp 18    lane 0 issues the bulk copies of the U0 and O0 tiles
 // Named barriers (warps 0-16): 1 = S_in ready; 2 = conversion warps arrive, the
 // issuer waits (U ready, state rescaled); 3 = the eight O warps (output staging).
 // A wait that runs out sets the CTA's abort flag: from then on no copy or MMA
@@ -987,10 +994,11 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // copies and MMAs already in flight are waited for (bounded again).
 constexpr int K2_CONV_WARPS = 16;
 constexpr int K2_CW = NT / (K2_CONV_WARPS / 4);   // state columns per conversion warp
-constexpr int K2_THREADS = 32 * (K2_CONV_WARPS + 2);
+constexpr int K2_THREADS = 32 * (K2_CONV_WARPS + 3);
 constexpr int K2_SYNC = 32 * (K2_CONV_WARPS + 1);  // conversion warps + the MMA issuer
 constexpr int K2_ISSUER_WARP = K2_CONV_WARPS;
 constexpr int K2_PRODUCER_WARP = K2_CONV_WARPS + 1;
+constexpr int K2_TILE_WARP = K2_CONV_WARPS + 2;
 static_assert(K2_CW == 16, "conversion code below moves 16 columns per thread");
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
@@ -1004,7 +1012,8 @@ __global__ void __launch_bounds__(K2_THREADS, 1)
 kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, int nch_per_seq,
              int c_begin, int c_end, const uint8_t* __restrict__ ws_blocks, const float* __restrict__ S0, int H,
              bf16* __restrict__ O, float* __restrict__ S_final, int ckpt_every, float* __restrict__ ckpt,
-             int ckpt_cap, int* status, int seg_pass1, float* __restrict__ S_final_map, int n_slots) {
+             int ckpt_cap, int* status, int seg_pass1, float* __restrict__ S_final_map, int n_slots,
+             const __grid_constant__ CUtensorMap tm_o, int o_tma) {
     // seg_pass1 (segment scan, first pass): blockIdx.z = 0 runs each segment
     // from a zero state (its affine offset, into S_final), blockIdx.z = 1 from
     // the identity with U0 taken as zero (its linear map, into S_final_map);
@@ -1050,7 +1059,11 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     uint64_t* bar_p = emptyB + K2_NB;
     uint64_t* bar_s = bar_p + 1;
     uint64_t* bar_drain = bar_s + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + 1);
+    uint64_t* fullU = bar_drain + 1;                // U0 tile: landed / read by the eight U warps
+    uint64_t* emptyU = fullU + 1;
+    uint64_t* fullO = emptyU + 1;                   // O0 tile: landed / read by the eight O warps
+    uint64_t* emptyO = fullO + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(emptyO + 1);
     volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
     if (w == 0) {
         kda::tmem_alloc(tmem_slot, K2_TMEM_COLS);
@@ -1063,6 +1076,10 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         kda::mbar_init(bar_p, 1);
         kda::mbar_init(bar_s, 1);
         kda::mbar_init(bar_drain, 1);
+        kda::mbar_init(fullU, 1);
+        kda::mbar_init(emptyU, K2_CONV_WARPS / 2);
+        kda::mbar_init(fullO, 1);
+        kda::mbar_init(emptyO, K2_CONV_WARPS / 2);
         kda::fence_barrier_init();
         *abort_f = 0;
     }
@@ -1088,8 +1105,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 kda::mbar_arrive_expect_tx(fullA + sa, K2_ASTAGE);
                 kda::bulk_g2s(sm + sa * K2_ASTAGE, block_of(k) + WS_A1, K2_ASTAGE, fullA + sa);
                 ++nA;
-                // the U0 / O0 tiles and a_last of this chunk, which the conversion
-                // warps load into registers when the chunk comes up, into L2
+                // this chunk's U0 / O0 tiles (copied by the tile warp when their
+                // buffers come free) and a_last (loaded by every conversion thread) into L2
                 kda::bulk_prefetch_l2(block_of(k) + WS_UO + 2 * TILE_F32 * tile, 2 * TILE_F32);
                 kda::bulk_prefetch_l2(block_of(k) + WS_AL, DK * 4);
                 const int sb = k % K2_NB;
@@ -1107,9 +1124,34 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                     (void)kda::mbar_wait(fullB + k % K2_NB, (uint32_t)((k / K2_NB) & 1), kda::kWaitCycles);
             }
         }
+    } else if (w == K2_TILE_WARP) {
+        // ---------------- U0 / O0 tiles of this slice, one chunk of each at a time
+        if (lane == 0) {
+            int nU = 0, nO = 0;                             // copies issued into each tile
+            for (int k = 0; k < nloc && !*abort_f; ++k) {
+                const uint8_t* uo = block_of(k) + WS_UO + 2 * TILE_F32 * tile;
+                if (k > 0) wait(emptyU, (uint32_t)((k - 1) & 1));
+                if (*abort_f) break;
+                kda::mbar_arrive_expect_tx(fullU, TILE_F32);
+                kda::bulk_g2s(sm + K2_U0, uo, TILE_F32, fullU);
+                ++nU;
+                if (!write_o) continue;                     // no output rows: O0 is not needed
+                if (k > 0) wait(emptyO, (uint32_t)((k - 1) & 1));
+                if (*abort_f) break;
+                kda::mbar_arrive_expect_tx(fullO, TILE_F32);
+                kda::bulk_g2s(sm + K2_O0, uo + TILE_F32, TILE_F32, fullO);
+                ++nO;
+            }
+            if (*abort_f) {                                 // the newest copy into each tile
+                if (nU > 0) (void)kda::mbar_wait(fullU, (uint32_t)((nU - 1) & 1), kda::kWaitCycles);
+                if (nO > 0) (void)kda::mbar_wait(fullO, (uint32_t)((nO - 1) & 1), kda::kWaitCycles);
+            }
+        }
     } else if (w == K2_ISSUER_WARP) {
         // ---------------- MMAs
-        const uint32_t sSB = kda::smem_u32(sm + K2_SB), sUB = kda::smem_u32(sm + K2_UB);
+        // operand descriptors: one per operand base; each MMA's start is a constant step from it
+        const uint64_t sb0 = kda::sw128_desc(kda::smem_u32(sm + K2_SB), 16384, 1024);
+        const uint64_t ub0 = kda::sw128_desc(kda::smem_u32(sm + K2_UB), 8192, 1024);
         named_bar_sync(1, K2_SYNC);                        // initial state in TMEM
         for (int c = 0; c < nloc; ++c) {
             const int sa = c % K2_NA, sb = c % K2_NB;
@@ -1118,14 +1160,13 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             named_bar_sync(1, K2_SYNC);
             if (lane == 0 && !*abort_f) {                   // P = [Q'; W] [S_hi | S_lo]
                 kda::tc_fence_after();
-                const uint32_t sA1 = kda::smem_u32(sm + sa * K2_ASTAGE);
+                const uint64_t ad0 = kda::sw128_desc(kda::smem_u32(sm + sa * K2_ASTAGE), 16, 1024);
                 const uint32_t idesc = kda::idesc_bf16(128, 2 * NT, 0, 1);
+                const uint32_t tP = tmem + 128 + 128 * (c & 1);
 #pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint64_t ad = kda::sw128_desc(sA1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
-                    const uint64_t bd = kda::sw128_desc(sSB + s * 2048, 16384, 1024);
-                    kda::umma_bf16(tmem + 128 + 128 * (c & 1), ad, bd, idesc, s > 0 ? 1u : 0u);
-                }
+                for (int s = 0; s < 8; ++s)
+                    kda::umma_bf16(tP, ad0 + kda::desc_step((s >> 2) * 16384 + (s & 3) * 32),
+                                   sb0 + kda::desc_step(s * 2048), idesc, s > 0 ? 1u : 0u);
                 kda::umma_commit(bar_p);
                 kda::umma_commit(emptyA + sa);
             }
@@ -1134,14 +1175,12 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             named_bar_sync(2, K2_SYNC);
             if (lane == 0 && !*abort_f) {                   // [S | X] += K_hi^T [U_hi | U_lo] + K_lo^T [U_hi | U_lo]
                 kda::tc_fence_after();
-                const uint32_t sKR = kda::smem_u32(sm + K2_B0 + sb * K2_BSTAGE);
+                const uint64_t ad0 = kda::sw128_desc(kda::smem_u32(sm + K2_B0 + sb * K2_BSTAGE), 8192, 1024);
                 const uint32_t id_s = kda::idesc_bf16(128, 2 * NT, 1, 1);
 #pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint64_t ad = kda::sw128_desc(sKR + (s >> 2) * 16384 + (s & 3) * 2048, 8192, 1024);
-                    const uint64_t bd = kda::sw128_desc(sUB + (s & 3) * 2048, 8192, 1024);
-                    kda::umma_bf16(tmem, ad, bd, id_s, 1u);
-                }
+                for (int s = 0; s < 8; ++s)
+                    kda::umma_bf16(tmem, ad0 + kda::desc_step((s >> 2) * 16384 + (s & 3) * 2048),
+                                   ub0 + kda::desc_step((s & 3) * 2048), id_s, 1u);
                 kda::umma_commit(bar_s);
                 kda::umma_commit(emptyB + sb);
             }
@@ -1161,19 +1200,23 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         const uint32_t tS = tmem + lane_off + col0;             // this warp's state columns (X at +64)
         const uint32_t tP = tmem + lane_off + 128 + col0;       // ... of P (buffer of chunk parity at +128)
         const bool u_rows = quad >= 2;                          // lanes 64..127: U; lanes 0..63: O
-        // this thread's 16 values of U0 (U rows) or O0 (O rows) of local chunk c
-        auto load_uo = [&](int c, float* dst) {
-            const uint8_t* base = block_of(c) + WS_UO + 2 * TILE_F32 * tile + (u_rows ? 0u : TILE_F32);
-            const int r = u_rows ? row - 64 : row;
+        // this thread's 16 values of a U0 or O0 tile in shared memory (row r of the chunk)
+        auto read_tile = [&](uint32_t off, int r, float* dst) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float4 x = *reinterpret_cast<const float4*>(base + uo_off(r, col0 + 4 * j));
+                const float4 x = *reinterpret_cast<const float4*>(sm + off + uo_off(r, col0 + 4 * j));
                 dst[4 * j] = x.x; dst[4 * j + 1] = x.y; dst[4 * j + 2] = x.z; dst[4 * j + 3] = x.w;
             }
         };
+        const bool o_issuer = w == 0 && lane == 0;           // issues the output tensor stores
         // O rows of chunk co (lanes 0..63 warps): P of that chunk is complete (the
         // state update issued after it is); staged in shared memory and stored
-        auto out_rows = [&](int co, const float* o0) {
+        auto out_rows = [&](int co) {
+            float o0[K2_CW];
+            wait(fullO, (uint32_t)(co & 1));
+            read_tile(K2_O0, row, o0);
+            __syncwarp();
+            if (lane == 0) kda::mbar_arrive(emptyO);
             kda::tc_fence_after();
             float ph[K2_CW], pl[K2_CW];
             kda::tmem_ld16(tP + 128 * (co & 1), ph);
@@ -1188,23 +1231,36 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 ov[cc] = pack8(f);
             }
             uint8_t* ost = sm + K2_OS;
+            if (o_issuer) kda::bulk_wait_read_all();             // the previous tile has left shared memory
             named_bar_sync(3, K2_CONV_WARPS * 16);             // every O warp is done with the last staged rows
 #pragma unroll
             for (int cc = 0; cc < K2_CW / 8; ++cc) {
                 const int k = (col0 + 8 * cc) / 8;               // 16-byte piece of the 128-byte row
                 *reinterpret_cast<uint4*>(ost + row * 128 + ((k ^ (row & 7)) << 4)) = ov[cc];
             }
-            named_bar_sync(3, K2_CONV_WARPS * 16);             // the staged tile is complete
-            const int wo = (grp << 1) | quad;                    // 0..7: rows 8 wo .. 8 wo + 7
             const int valid = len - (cb + co) * C;
+            // a full chunk leaves by one tensor store (the staging order is the
+            // store's 128-byte swizzle); the last rows of a sequence row by row,
+            // since the rows past them belong to the next sequence
+            const bool whole = o_tma && valid >= C;
+            if (whole) kda::fence_proxy_async_smem();
+            named_bar_sync(3, K2_CONV_WARPS * 16);             // the staged tile is complete
+            if (whole) {
+                if (o_issuer && !*abort_f) {
+                    kda::tma_store_3d(&tm_o, tile * NT, h, bos + (cb + co) * C, ost);
+                    kda::bulk_commit();
+                }
+            } else {
+                const int wo = (grp << 1) | quad;                // 0..7: rows 8 wo .. 8 wo + 7
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int rr = 8 * wo + i;
-                if (write_o && rr < valid) {
-                    const uint32_t x = *reinterpret_cast<const uint32_t*>(
-                        ost + rr * 128 + (((lane >> 2) ^ (rr & 7)) << 4) + 4 * (lane & 3));
-                    *reinterpret_cast<uint32_t*>(O + ((size_t)(bos + (cb + co) * C + rr) * H + h) * DV + tile * NT +
-                                                 2 * lane) = x;
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = 8 * wo + i;
+                    if (rr < valid) {
+                        const uint32_t x = *reinterpret_cast<const uint32_t*>(
+                            ost + rr * 128 + (((lane >> 2) ^ (rr & 7)) << 4) + 4 * (lane & 3));
+                        *reinterpret_cast<uint32_t*>(O + ((size_t)(bos + (cb + co) * C + rr) * H + h) * DV +
+                                                     tile * NT + 2 * lane) = x;
+                    }
                 }
             }
             kda::tc_fence_before();
@@ -1236,14 +1292,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             named_bar_sync(1, K2_SYNC);
         }
         float al_next = nloc > 0 ? reinterpret_cast<const float*>(block_of(0) + WS_AL)[row] : 1.f;
-        float uo_prev[K2_CW];                                   // O rows: O0 of the previous chunk
-#pragma unroll
-        for (int u = 0; u < K2_CW; ++u) uo_prev[u] = 0.f;
         for (int c = 0; c < nloc; ++c) {
             const float al = al_next;
-            if (c + 1 < nloc) al_next = reinterpret_cast<const float*>(block_of(c + 1) + WS_AL)[row];
-            float uo[K2_CW];                                    // U0 (U rows) or O0 (O rows) of this chunk
-            load_uo(c, uo);
             // ---- S_in = S + X -> high/low bf16 operand
             if (c > 0) wait(bar_s, (uint32_t)((c - 1) & 1));
             kda::tc_fence_after();
@@ -1263,6 +1313,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             kda::fence_proxy_async_smem();
             kda::tc_fence_before();
             named_bar_sync(1, K2_SYNC);
+            // the next chunk's a_last, loaded after the proxy fence (which would wait for it)
+            if (c + 1 < nloc) al_next = reinterpret_cast<const float*>(block_of(c + 1) + WS_AL)[row];
             if (ckpt_every > 0 && cb + c > 0 && ((cb + c) * C) % ckpt_every == 0)   // state after (cb + c) chunks
                 put_ckpt(ck_base + (cb + c) * C / ckpt_every - 1, s, row, col0);
             // ---- S <- Diag(a_last) S_in, X <- 0 while the P product runs
@@ -1273,6 +1325,11 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             kda::tmem_wait_st();
             if (u_rows) {
                 // ---- U = U0 - W S_in -> high/low bf16 operand
+                float uo[K2_CW];                                // U0 of this chunk
+                wait(fullU, (uint32_t)(c & 1));
+                read_tile(K2_U0, row - 64, uo);
+                __syncwarp();
+                if (lane == 0) kda::mbar_arrive(emptyU);
                 wait(bar_p, (uint32_t)(c & 1));
                 kda::tc_fence_after();
                 const int r = row - 64;
@@ -1298,14 +1355,13 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             } else {
                 kda::tc_fence_before();
                 named_bar_arrive(2, K2_SYNC);
-                if (c > 0) out_rows(c - 1, uo_prev);            // the previous chunk's output
-#pragma unroll
-                for (int u = 0; u < K2_CW; ++u) uo_prev[u] = uo[u];
+                if (write_o && c > 0) out_rows(c - 1);          // the previous chunk's output
             }
         }
         if (nloc > 0) wait(bar_s, (uint32_t)((nloc - 1) & 1));
         kda::tc_fence_after();
-        if (!u_rows && nloc > 0) out_rows(nloc - 1, uo_prev);
+        if (write_o && !u_rows && nloc > 0) out_rows(nloc - 1);
+        if (o_issuer) kda::bulk_wait_all();                     // the output stores are complete
         const bool end_ckpt = ckpt_every > 0 && nloc > 0 && cb + nloc == nch && len % ckpt_every == 0;
         if (S_final || end_ckpt) {
             float s[K2_CW], x[K2_CW];
@@ -1520,11 +1576,31 @@ cudaError_t make_input_map(CUtensorMap* m, const void* base, int esize, int H, i
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tensor map of the output O [T][H][d_v] bf16 for the state pass's stores: one
+// box = 64 tokens x one head x NT channels, 128-byte swizzled in shared memory.
+cudaError_t make_output_map(CUtensorMap* m, void* base, int H, int T) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)DV, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)H * DV * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)NT, 1, (cuuint32_t)C};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // ---- stream overlap: the prep of a later slice of chunks runs while the
-// state pass works through the previous slice.  Per device: one
+// state pass works through the previous slice.  It pays when the state pass
+// leaves most SMs to the prep (few chains), and for long sequences whenever
+// the state pass leaves at least half of them (one CTA per SM): there the
+// prep of each slice runs on the SMs the state pass does not hold, with a
+// grid sized to them, so that the state pass's CTAs always find free SMs.  Per device: one
 // high-priority stream for the state pass and a pool of events, created on
 // first use and kept for the life of the process.
 constexpr int kMaxSlices = 8;
+constexpr int kOverlapMinChunks = 1024;          // "long": chunks of the longest sequence
 constexpr int kMaxDevices = 64;
 struct OverlapRes {
     cudaStream_t chain = nullptr;
@@ -1607,7 +1683,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     float* seg_B = reinterpret_cast<float*>(seg_base + seg_table_bytes(sp, a.n_seq));
     float* seg_A = seg_B + (size_t)sp.s_max * a.H * DK * DV;
     float* seg_S = seg_A + (size_t)sp.s_max * a.H * DK * DV;
-    const bool overlap = !use_seg && chain_ctas * 4 <= n_sm && !(use_table && a.max_chunks <= 0);
+    const bool long_seq = max_chunks >= kOverlapMinChunks && chain_ctas * 2 <= n_sm;
+    const bool overlap = !use_seg && (chain_ctas * 4 <= n_sm || long_seq) && !(use_table && a.max_chunks <= 0);
+    // prep CTAs that fit beside a running state pass (two per free SM)
+    const long long side_ctas = std::max<long long>(2, 2LL * (n_sm - std::min<long long>(chain_ctas, n_sm)));
     const int n_slices = overlap ? std::max(1, std::min(kMaxSlices, max_chunks / 16)) : 1;
     const int slice = n_slices > 1 ? (max_chunks + n_slices - 1) / n_slices : max_chunks;
 
@@ -1627,18 +1706,23 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     e = cudaFuncSetAttribute(kda_tc_seg_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM);
     if (e != cudaSuccess) return e;
 
-    CUtensorMap tm_q, tm_k, tm_v, tm_g;
+    CUtensorMap tm_q, tm_k, tm_v, tm_g, tm_o;
+    std::memset(&tm_o, 0, sizeof(tm_o));
+    // full output chunks leave the state pass by tensor stores when O is 16-byte aligned
+    const int o_tma = a.T_total > 0 && a.O != nullptr && (reinterpret_cast<uintptr_t>(a.O) & 15) == 0;
+    if (o_tma && (e = make_output_map(&tm_o, a.O, a.H, a.T_total)) != cudaSuccess) return e;
     if (a.T_total > 0) {
         if ((e = make_input_map(&tm_q, a.q, 2, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
         if ((e = make_input_map(&tm_k, a.k, 2, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
         if ((e = make_input_map(&tm_v, a.v, 2, a.H, a.T_total, 64, true)) != cudaSuccess) return e;
         if ((e = make_input_map(&tm_g, a.log_alpha, 4, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
     }
-    auto prep = [&](int j0, int jn, cudaStream_t st) {
+    auto prep = [&](int j0, int jn, cudaStream_t st, bool beside_chain) {
         if (jn <= 0 || a.total_chunks <= 0 || a.T_total <= 0) return cudaSuccess;
         const int gx = use_table ? a.total_chunks : a.n_seq * jn;
         const long long items = (long long)gx * a.H;
-        const unsigned grid = (unsigned)std::min<long long>(items, 2LL * n_sm);   // two resident CTAs per SM
+        // two resident CTAs per SM; beside a running state pass, only on its free SMs
+        const unsigned grid = (unsigned)std::min<long long>(items, beside_chain ? side_ctas : 2LL * n_sm);
         prep_kernel<<<grid, 256, prep_smem, st>>>(tm_q, tm_k, tm_v, tm_g, a.beta, a.H, use_table, fixed_len,
                                                   nch_per, chunk_info, seq_info, j0, jn, gx, (int)ub, blocks,
                                                   a.status);
@@ -1647,12 +1731,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     auto chain = [&](int c0, int c1, const float* s_in, float* s_out, cudaStream_t st) {
         kda_tc_chain<<<dim3(NTILES * a.n_seq, a.H), K2_THREADS, chain_smem, st>>>(
             seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
-            a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub);
+            a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub, tm_o, o_tma);
         return cudaGetLastError();
     };
 
     if (use_seg) {
-        if ((e = prep(0, max_chunks, a.stream)) != cudaSuccess) return e;
+        if ((e = prep(0, max_chunks, a.stream, false)) != cudaSuccess) return e;
         trace_mark(a.stream);
         kda_tc_segments<<<1, 1024, 0, a.stream>>>(seq_info, use_table, fixed_len, nch_per, a.n_seq, seg_L, sp.s_max,
                                                   seg_info, seq_seg, a.status);
@@ -1660,7 +1744,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         // pass 1: every segment from zero (-> seg_B) and as a map from the identity (-> seg_A)
         kda_tc_chain<<<dim3(NTILES * sp.s_max, a.H, 2), K2_THREADS, chain_smem, a.stream>>>(
             seg_info, 1, 0, 0, 0, INT32_MAX, blocks, nullptr, a.H, static_cast<bf16*>(a.O), seg_B, 0, nullptr, 0,
-            a.status, 1, seg_A, (int)ub);
+            a.status, 1, seg_A, (int)ub, tm_o, o_tma);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // pass 2: starting state of every segment, and the final states
         kda_tc_seg_scan<<<dim3(a.n_seq, a.H, DV / SC_COLS), 256, SC_SMEM, a.stream>>>(seq_seg, seg_A, seg_B, a.S0,
@@ -1670,14 +1754,14 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         // pass 3: every segment from its starting state, writing O
         kda_tc_chain<<<dim3(NTILES * sp.s_max, a.H), K2_THREADS, chain_smem, a.stream>>>(
             seg_info, 1, 0, 0, 0, INT32_MAX, blocks, seg_S, a.H, static_cast<bf16*>(a.O), nullptr, 0, nullptr, 0,
-            a.status, 0, nullptr, (int)ub);
+            a.status, 0, nullptr, (int)ub, tm_o, o_tma);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         trace_mark(a.stream);
         return cudaSuccess;
     }
 
     if (n_slices == 1) {
-        if ((e = prep(0, max_chunks, a.stream)) != cudaSuccess) return e;
+        if ((e = prep(0, max_chunks, a.stream, false)) != cudaSuccess) return e;
         trace_mark(a.stream);
         if ((e = chain(0, max_chunks, a.S0, a.S_final, a.stream)) != cudaSuccess) return e;
         trace_mark(a.stream);
@@ -1693,7 +1777,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     if ((e = cudaStreamWaitEvent(r->chain, r->ev[n_slices], 0)) != cudaSuccess) return e;
     for (int k = 0; k < n_slices; ++k) {
         const int c0 = k * slice, c1 = std::min(max_chunks, (k + 1) * slice);
-        if ((e = prep(c0, c1 - c0, a.stream)) != cudaSuccess) return e;
+        if ((e = prep(c0, c1 - c0, a.stream, k > 0 && long_seq && chain_ctas * 4 > n_sm)) != cudaSuccess) return e;
         if ((e = cudaEventRecord(r->ev[k], a.stream)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(r->chain, r->ev[k], 0)) != cudaSuccess) return e;
         const bool last = (k == n_slices - 1);

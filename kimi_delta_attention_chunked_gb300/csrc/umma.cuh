@@ -32,6 +32,10 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// One arrival (release: this thread's earlier shared-memory accesses happen before it).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
@@ -118,6 +122,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, 
         : "memory");
 }
 
+// Tiled 3-D tensor store (TMA) of a box from shared memory to the tensor
+// described by `tmap` at element coordinates (x, y, z), tracked by the issuing
+// thread's bulk-async group; elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, int x, int y, int z, const void* src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
+                 "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
+                 : "memory");
+}
+
 // Prefetch into L2 of the box at (x, y, z) of a tensor map (no shared memory,
 // no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int x, int y, int z) {
@@ -198,6 +211,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     d |= (uint64_t)2 << 61;          // 128-byte swizzle
     return d;
 }
+
+// Advance a descriptor's start address by `bytes` (a multiple of 16): the
+// start field holds the address in 16-byte units in its low 14 bits, and
+// shared-memory addresses stay below 256 KB, so the sum cannot carry out of it.
+__host__ __device__ constexpr uint64_t desc_step(uint32_t bytes) { return (uint64_t)(bytes >> 4); }
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulation.
 // a_mn / b_mn: 0 = K-major, 1 = MN-major.

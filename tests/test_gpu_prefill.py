@@ -139,6 +139,16 @@ def test_tc_overlapped_slices_few_heads():
         assert eo <= 5e-3 and es <= 5e-3, (lengths, eo, es)
 
 
+def test_tc_overlapped_slices_long_sequence_32_heads():
+    """A long sequence at 32 heads (64 state-pass CTAs, a third of the SMs free
+    at most): the prep of later chunk slices runs beside the state pass of
+    earlier ones on the SMs it leaves free; a ragged tail and a random S0."""
+    dev = need_gpu()
+    w = inputs.Workload("tc", "prefill", H=32, dk=128, dv=128, dtype=torch.bfloat16, chunk=64, s0_std=0.02)
+    _, _, _, eo, es = run_case(w, dev, lengths=[64 * 1024 + 37], seed=18, heads=(29, 31))
+    assert eo <= 5e-3 and es <= 5e-3, (eo, es)
+
+
 @pytest.mark.parametrize("host_cu", [True, False])
 def test_tc_segment_scan_few_heads(host_cu):
     """Two heads and long sequences: each sequence is cut into segments of 16
