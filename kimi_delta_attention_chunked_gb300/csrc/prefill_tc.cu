@@ -149,7 +149,7 @@ static_assert(WS_KRL == WS_KR + 16384, "both parts of K_restore^T are one contig
 static_assert(K1_AIL + 16384 <= K1_BWU, "[INV; X] must stay inside the alias region");
 static_assert(K1_ML + 16384 <= K1_BWU && K1_IL + 8192 <= K1_IS, "X operands stay inside the alias region");
 static_assert(K1_OUT_A1 + 32768 <= K1_SG, "the next log-decay tile does not touch the [Q'; W] image");
-static_assert(K1_BAR + 56 <= K1_NRM, "prep barriers and flags");
+static_assert(K1_BAR + 64 <= K1_NRM, "prep barriers and flags");
 static_assert(K1_BG + 160 * 256 <= K1_AG && K1_AG + 32768 == K1_BWU && K1_AG % 1024 == 0, "Gram operands");
 static_assert(K1_SK + 16384 <= K1_AG && K1_SG + 32768 <= K1_BWU && (K1_BWU + 16384) % 1024 == 0, "input tiles");
 static_assert(K1_AIL + 16384 <= K1_SG + 32768 && K1_ML + 16384 <= K1_SG + 32768,
@@ -343,13 +343,22 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             const float* __restrict__ beta, int H, int use_table,
             int fixed_len, int nch_per_seq, const int4* __restrict__ chunk_info,
             const int4* __restrict__ seq_info, int j_begin, int j_count, int n_x, int n_slots,
-            uint8_t* __restrict__ ws_blocks, int* status) {
+            uint8_t* __restrict__ ws_blocks, int* status, unsigned long long* item_ctr, int reserve_sm) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
-    // Persistent: this CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ... of
-    // the n_x * H (chunk, head) items, head fastest.  The launch covers chunks
-    // j_begin .. j_begin + j_count - 1 of every sequence: equal lengths ->
-    // n_x = n_seq * j_count; chunk table -> n_x = chunk slots.
+    // Persistent over the n_x * H (chunk, head) items, head fastest.  The launch
+    // covers chunks j_begin .. j_begin + j_count - 1 of every sequence: equal
+    // lengths -> n_x = n_seq * j_count; chunk table -> n_x = chunk slots.
+    // Static schedule (item_ctr null): this CTA takes items blockIdx.x,
+    // blockIdx.x + gridDim.x, ...  Dynamic schedule: the CTAs draw items from
+    // the counter *item_ctr (zero at launch), and a CTA that finds itself on an
+    // SM whose id is below reserve_sm leaves at once, so that a state pass
+    // launched beside this kernel finds those SMs free.
+    if (item_ctr != nullptr && reserve_sm > 0) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        if ((int)smid < reserve_sm) return;        // nothing allocated or initialised yet
+    }
     auto item = [&](long long it, int& tok0, int& nrows, int& slot, int& h) -> bool {
         const int x = (int)(it / H);
         h = (int)(it % H);
@@ -372,6 +381,15 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         return nrows > 0;
     };
     const long long n_items = (long long)n_x * H;
+    // dynamic schedule (thread 0): the next item that exists, or n_items
+    auto draw = [&]() -> long long {
+        for (;;) {
+            const long long x = (long long)atomicAdd(item_ctr, 1ull);
+            if (x >= n_items) return n_items;
+            int t_, r_, s_, h_;
+            if (item(x, t_, r_, s_, h_)) return x;
+        }
+    };
 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + K1_BAR);
@@ -381,6 +399,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     volatile int* abort_f = reinterpret_cast<volatile int*>(sm + K1_BAR + 32);
     uint64_t* bar_drain = reinterpret_cast<uint64_t*>(sm + K1_BAR + 40);
     uint64_t* bar_qk = reinterpret_cast<uint64_t*>(sm + K1_BAR + 48);
+    volatile long long* next_it = reinterpret_cast<volatile long long*>(sm + K1_BAR + 56);   // dynamic schedule
     if (w == 0) {
         kda::tmem_alloc(tmem_slot, K1_TMEM_COLS);
         kda::tmem_relinquish();
@@ -393,6 +412,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         kda::mbar_init(bar_drain, 1);
         kda::fence_barrier_init();
         *abort_f = 0;
+        if (item_ctr != nullptr) *next_it = draw();
     }
     uint32_t n_done = 0;                          // items finished by this CTA (bar_q parity)
     uint32_t bar_phase = 0;                       // completed phases of bar (three per item)
@@ -420,9 +440,13 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     kda::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const bool dyn = item_ctr != nullptr;
+    for (long long it = dyn ? *next_it : blockIdx.x; it < n_items; it = dyn ? *next_it : it + gridDim.x) {
         int tok0, nrows, slot, h;
-        if (!item(it, tok0, nrows, slot, h)) continue;
+        if (!item(it, tok0, nrows, slot, h)) {
+            if (dyn) break;                        // (drawn items exist: not reached)
+            continue;
+        }
         uint8_t* blk = ws_blocks + ((size_t)slot * H + h) * WS_BLOCK;
 
         // ---------------- a1: loads and per-block cumulative log-decay
@@ -864,13 +888,24 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
         // the last MMA is done with its operands: the next item's log-decay tile
         // (over the [INV; X] operand) and V (over this item's V) can come in
-        if (tid == 0 && !*abort_f) {
-            for (long long nx = it + gridDim.x; nx < n_items; nx += gridDim.x) {
+        if (tid == 0) {
+            if (dyn) {
+                // the next item is drawn even after an abort (the loop runs out the items)
+                const long long nx = draw();
+                *next_it = nx;                     // read by every thread after the item's last barrier
                 int t1, r1, s1, h1;
-                if (!item(nx, t1, r1, s1, h1)) continue;
-                load_gv(t1, h1);
-                gv_ready = true;
-                break;
+                if (!*abort_f && nx < n_items && item(nx, t1, r1, s1, h1)) {
+                    load_gv(t1, h1);
+                    gv_ready = true;
+                }
+            } else if (!*abort_f) {
+                for (long long nx = it + gridDim.x; nx < n_items; nx += gridDim.x) {
+                    int t1, r1, s1, h1;
+                    if (!item(nx, t1, r1, s1, h1)) continue;
+                    load_gv(t1, h1);
+                    gv_ready = true;
+                    break;
+                }
             }
         }
         // TMEM lanes 0..63 hold [W | U0], lanes 64..127 hold [M_qk W | O0] (columns 0..127 | 128..255)
@@ -1508,8 +1543,12 @@ kda_tc_seg_scan(const int2* __restrict__ seq_seg, const float* __restrict__ A, c
     }
 }
 
+// Workspace header: chunk table (16 B a slot), sequence table (16 B a
+// sequence), then kSliceWords 8-byte words: the item counters of the chunk-prep
+// slices that run beside the state pass (and, once per device, the SM-id mask).
+constexpr int kSliceWords = 8;
 size_t header_bytes(int n_seq, long long slots) {
-    const size_t raw = 16u * (size_t)slots + 16u * (size_t)n_seq;
+    const size_t raw = 16u * (size_t)slots + 16u * (size_t)n_seq + 8u * kSliceWords;
     return (raw + 1023) & ~size_t(1023);
 }
 
@@ -1592,21 +1631,71 @@ cudaError_t make_output_map(CUtensorMap* m, void* base, int H, int T) {
 }
 
 // ---- stream overlap: the prep of a later slice of chunks runs while the
-// state pass works through the previous slice.  It pays when the state pass
-// leaves most SMs to the prep (few chains), and for long sequences whenever
-// the state pass leaves at least half of them (one CTA per SM): there the
-// prep of each slice runs on the SMs the state pass does not hold, with a
-// grid sized to them, so that the state pass's CTAs always find free SMs.  Per device: one
-// high-priority stream for the state pass and a pool of events, created on
-// first use and kept for the life of the process.
+// state pass works through the previous slice, for long sequences whose state
+// pass (one CTA per SM) leaves at least half of the SMs free.  (At a few
+// thousand tokens the prep on the remaining SMs takes longer than the state
+// pass saves: 0.56 against 0.49 ms at 8192 tokens and 32 heads.)  The state pass is
+// launched on a high-priority stream, but a prep slice launched first would
+// still take every SM; so the preps that run beside it draw their items from
+// a counter, and their CTAs that land on the SMs kept for the state pass (the
+// ones with the lowest ids) leave at once.  Per device: the state-pass
+// stream, a pool of events and the sorted SM ids, found on first use and kept
+// for the life of the process.
 constexpr int kMaxSlices = 8;
+static_assert(kMaxSlices <= kSliceWords, "one item counter per prep slice");
+constexpr int kSliceChunks = 16;                 // fewest chunks in a slice
 constexpr int kOverlapMinChunks = 1024;          // "long": chunks of the longest sequence
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSmIds = 256;
 struct OverlapRes {
     cudaStream_t chain = nullptr;
     cudaEvent_t ev[kMaxSlices + 2] = {};
+    int n_ids = 0;                               // SM ids seen (0: not known)
+    int ids[kMaxSmIds] = {};                     // ... sorted
     bool ok = false;
 };
+
+// One bit per SM id that a CTA ran on; the CTAs stay resident for ~10 us so
+// that they spread over every SM.
+__global__ void kda_sm_ids(unsigned int* mask) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    if (threadIdx.x == 0 && smid < kMaxSmIds) atomicOr(mask + (smid >> 5), 1u << (smid & 31));
+    const long long t0 = clock64();
+    while (clock64() - t0 < 20000) {
+    }
+}
+
+// SM-id bound below which `count` SMs lie (the ids need not be contiguous);
+// with the ids not known, `count` itself.
+int reserve_bound(const OverlapRes& r, long long count) {
+    if (count <= 0) return 0;
+    if (r.n_ids < count) return (int)count;
+    return r.ids[count - 1] + 1;
+}
+
+// Finds the device's SM ids once (not while the stream is being captured),
+// using 32 bytes of the caller's workspace.
+cudaError_t probe_sm_ids(OverlapRes& r, int n_sm, void* scratch, cudaStream_t st) {
+    if (r.n_ids > 0) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess || cs != cudaStreamCaptureStatusNone) return e;
+    unsigned int* mask = static_cast<unsigned int*>(scratch);
+    if ((e = cudaMemsetAsync(mask, 0, kMaxSmIds / 8, st)) != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kda_sm_ids, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
+    if (e != cudaSuccess) return e;
+    kda_sm_ids<<<4 * n_sm, 32, 100 * 1024, st>>>(mask);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    unsigned int h[kMaxSmIds / 32];
+    if ((e = cudaMemcpyAsync(h, mask, sizeof(h), cudaMemcpyDeviceToHost, st)) != cudaSuccess) return e;
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return e;
+    int n = 0;
+    for (int i = 0; i < kMaxSmIds; ++i)
+        if (h[i >> 5] >> (i & 31) & 1u) r.ids[n++] = i;
+    r.n_ids = n;
+    return cudaSuccess;
+}
 std::mutex g_overlap_mutex;
 OverlapRes g_overlap[kMaxDevices];
 
@@ -1654,6 +1743,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     int4* chunk_info = reinterpret_cast<int4*>(ws);
     int4* seq_info = reinterpret_cast<int4*>(ws + 16 * (size_t)ub);
+    // item counters of the prep slices that run beside the state pass
+    unsigned long long* slice_ctr = reinterpret_cast<unsigned long long*>(ws + 16 * (size_t)ub + 16 * (size_t)a.n_seq);
     float* S_mid = reinterpret_cast<float*>(ws + header_bytes(a.n_seq, ub));
     uint8_t* blocks = ws + header_bytes(a.n_seq, ub) + state_bytes(a.n_seq, a.H);
 
@@ -1683,11 +1774,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     float* seg_B = reinterpret_cast<float*>(seg_base + seg_table_bytes(sp, a.n_seq));
     float* seg_A = seg_B + (size_t)sp.s_max * a.H * DK * DV;
     float* seg_S = seg_A + (size_t)sp.s_max * a.H * DK * DV;
-    const bool long_seq = max_chunks >= kOverlapMinChunks && chain_ctas * 2 <= n_sm;
-    const bool overlap = !use_seg && (chain_ctas * 4 <= n_sm || long_seq) && !(use_table && a.max_chunks <= 0);
-    // prep CTAs that fit beside a running state pass (two per free SM)
-    const long long side_ctas = std::max<long long>(2, 2LL * (n_sm - std::min<long long>(chain_ctas, n_sm)));
-    const int n_slices = overlap ? std::max(1, std::min(kMaxSlices, max_chunks / 16)) : 1;
+    const bool overlap = !use_seg && chain_ctas * 2 <= n_sm && max_chunks >= kOverlapMinChunks &&
+                         !(use_table && a.max_chunks <= 0);
+    const int n_slices = overlap ? std::min(kMaxSlices, max_chunks / kSliceChunks) : 1;
     const int slice = n_slices > 1 ? (max_chunks + n_slices - 1) / n_slices : max_chunks;
 
     if (use_table) {
@@ -1717,15 +1806,16 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         if ((e = make_input_map(&tm_v, a.v, 2, a.H, a.T_total, 64, true)) != cudaSuccess) return e;
         if ((e = make_input_map(&tm_g, a.log_alpha, 4, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
     }
-    auto prep = [&](int j0, int jn, cudaStream_t st, bool beside_chain) {
+    // chunks [j0, j0 + jn) of every sequence; beside a running state pass
+    // (reserve > 0) the CTAs draw items from `ctr` and leave the SMs below `reserve`
+    auto prep = [&](int j0, int jn, cudaStream_t st, unsigned long long* ctr, int reserve) {
         if (jn <= 0 || a.total_chunks <= 0 || a.T_total <= 0) return cudaSuccess;
         const int gx = use_table ? a.total_chunks : a.n_seq * jn;
         const long long items = (long long)gx * a.H;
-        // two resident CTAs per SM; beside a running state pass, only on its free SMs
-        const unsigned grid = (unsigned)std::min<long long>(items, beside_chain ? side_ctas : 2LL * n_sm);
+        const unsigned grid = (unsigned)std::min<long long>(items + (ctr ? 2LL * n_sm : 0), 2LL * n_sm);
         prep_kernel<<<grid, 256, prep_smem, st>>>(tm_q, tm_k, tm_v, tm_g, a.beta, a.H, use_table, fixed_len,
                                                   nch_per, chunk_info, seq_info, j0, jn, gx, (int)ub, blocks,
-                                                  a.status);
+                                                  a.status, ctr, reserve);
         return cudaGetLastError();
     };
     auto chain = [&](int c0, int c1, const float* s_in, float* s_out, cudaStream_t st) {
@@ -1736,7 +1826,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     };
 
     if (use_seg) {
-        if ((e = prep(0, max_chunks, a.stream, false)) != cudaSuccess) return e;
+        if ((e = prep(0, max_chunks, a.stream, nullptr, 0)) != cudaSuccess) return e;
         trace_mark(a.stream);
         kda_tc_segments<<<1, 1024, 0, a.stream>>>(seq_info, use_table, fixed_len, nch_per, a.n_seq, seg_L, sp.s_max,
                                                   seg_info, seq_seg, a.status);
@@ -1761,7 +1851,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     }
 
     if (n_slices == 1) {
-        if ((e = prep(0, max_chunks, a.stream, false)) != cudaSuccess) return e;
+        if ((e = prep(0, max_chunks, a.stream, nullptr, 0)) != cudaSuccess) return e;
         trace_mark(a.stream);
         if ((e = chain(0, max_chunks, a.S0, a.S_final, a.stream)) != cudaSuccess) return e;
         trace_mark(a.stream);
@@ -1773,11 +1863,16 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     std::lock_guard<std::mutex> lock(g_overlap_mutex);
     OverlapRes* r = nullptr;
     if ((e = overlap_resources(&r)) != cudaSuccess) return e;
+    if ((e = probe_sm_ids(*r, n_sm, slice_ctr, a.stream)) != cudaSuccess) return e;
+    const int reserve = reserve_bound(*r, chain_ctas);
+    if ((e = cudaMemsetAsync(slice_ctr, 0, 8u * kMaxSlices, a.stream)) != cudaSuccess) return e;
     if ((e = cudaEventRecord(r->ev[n_slices], a.stream)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(r->chain, r->ev[n_slices], 0)) != cudaSuccess) return e;
     for (int k = 0; k < n_slices; ++k) {
         const int c0 = k * slice, c1 = std::min(max_chunks, (k + 1) * slice);
-        if ((e = prep(c0, c1 - c0, a.stream, k > 0 && long_seq && chain_ctas * 4 > n_sm)) != cudaSuccess) return e;
+        // the first slice has the GPU to itself; the others run beside the state pass
+        if ((e = prep(c0, c1 - c0, a.stream, k > 0 ? slice_ctr + k : nullptr, k > 0 ? reserve : 0)) != cudaSuccess)
+            return e;
         if ((e = cudaEventRecord(r->ev[k], a.stream)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(r->chain, r->ev[k], 0)) != cudaSuccess) return e;
         const bool last = (k == n_slices - 1);
