@@ -56,9 +56,9 @@ PARTS = ("prefill", "decode", "verify", "few", "varlen", "long", "e2e")
 # them the traffic reads null until a new capture replaces the entry.
 PROFILED_TRAFFIC = {
     "kda_tc_prep": {
-        "read_mb": 336.688128, "write_mb": 479.177728, "profile": "profiles/prefill_tc_T8192_H32_D128.md",
-        "sources": {"csrc/prefill_tc.cu": "ce2a20be72a45dd8", "csrc/umma.cuh": "f70da77c79c8c26e",
-                    "csrc/common.cuh": "10fad8ef65a72b1e"}},
+        "read_mb": 337.512448, "write_mb": 482.086400, "profile": "profiles/prefill_tc_T8192_H32_D128.md",
+        "sources": {"csrc/prefill_tc.cu": "6bda46d6a61fa522", "csrc/umma.cuh": "284f4428858e7949",
+                    "csrc/common.cuh": "9b104993be79c2d2"}},
     "kda_decode_kernel": {
         "read_mb": 547.525376, "write_mb": 478.725120, "profile": "profiles/decode_N256_H32_D128.md",
         "sources": {"csrc/decode.cu": "ca2b6a97d7eeaad3", "csrc/common.cuh": "10fad8ef65a72b1e"}},

@@ -155,3 +155,32 @@ def test_verify_outputs_only_then_commit():
             assert rel_err(S[n], Sf[0]) <= 1e-4
         else:
             assert torch.equal(S[n], d["S0"][n])
+
+
+def test_verify_unaligned_inputs_take_the_scalar_staging():
+    """Inputs at an odd element offset (2 bytes past an aligned start): the
+    results are the same bits as from aligned copies of the same inputs, and
+    match the oracle."""
+    dev = need_gpu()
+    N, K, H, D = 8, 8, 4, 128
+    w = inputs.Workload("verify3", "prefill", H=H, dk=D, dv=D, dtype=torch.bfloat16, chunk=64, T=K, B=N, s0_std=0.02)
+    d = inputs.make_prefill(w, device=dev, seed=5, lengths=[K] * N)
+    rs = lambda x: x.view(N, K, H, D).contiguous()
+
+    def shifted(x):                                   # same values, one element past an aligned start
+        buf = torch.empty(x.numel() + 1, dtype=x.dtype, device=dev)
+        buf[1:].copy_(x.reshape(-1))
+        return buf[1:].view(x.shape)
+
+    b = d["beta"].view(N, K, H).contiguous()
+    args = [rs(d[n]) for n in ("q", "k", "v", "log_alpha")]
+    S1, S2 = d["S0"].clone(), d["S0"].clone()
+    o1 = kda.kda_decode_multi(*args, b, S1)
+    o2 = kda.kda_decode_multi(*[shifted(a) for a in args], b, S2)
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
+    O_ref, S_ref = oracle.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], cu_seqlens=d["cu_seqlens_host"],
+                                  S0=d["S0"])
+    assert rel_err(o2.view(N * K, H, D), O_ref) <= tol_for(torch.bfloat16)
+    assert rel_err(S2, S_ref) <= tol_for(torch.bfloat16)
