@@ -134,17 +134,29 @@ constexpr int K2_NB = 2;                     // K_restore^T stages, high and low
 constexpr uint32_t K2_ASTAGE = 32768;
 constexpr uint32_t K2_BSTAGE = 32768;
 constexpr uint32_t K2_B0 = K2_NA * K2_ASTAGE;            // B ring: high part at +0, low part at +16384
-constexpr uint32_t K2_SB = K2_B0 + K2_NB * K2_BSTAGE;    // [S_hi | S_lo] bf16, MN-major SW128, K = 128 rows, N = 2 x 64
-constexpr uint32_t K2_UB = K2_SB + 32768;                // [U_hi | U_lo] bf16, MN-major SW128, K = 64 rows, N = 2 x 64
-constexpr uint32_t K2_OS = K2_UB + 16384;                // one chunk's bf16 output rows [64][64] (16-byte pieces swizzled)
-constexpr uint32_t K2_U0 = K2_OS + 8192;                 // U0 tile of this slice (fp32, workspace order), one chunk
-constexpr uint32_t K2_O0 = K2_U0 + TILE_F32;             // O0 tile of this slice, one chunk
-constexpr uint32_t K2_BAR = K2_O0 + TILE_F32;            // full / empty A, B; p; s; drain; full / empty U0, O0;
-                                                         // TMEM address; abort flag
-constexpr uint32_t K2_BYTES = K2_BAR + 192;
-constexpr uint32_t K2_TMEM_COLS = 512;       // S [0, 64), X [64, 128), P of even chunks [128, 256), of odd [256, 384)
-
-static_assert(K2_B0 % 1024 == 0 && K2_SB % 1024 == 0 && K2_UB % 1024 == 0, "SW128 operands are 1024-byte aligned");
+// The rest depends on NTC, the d_v columns of one state-pass CTA (64, or 32
+// when the whole pass fits one wave of CTAs):
+template <int NTC>
+struct ChainCfg {
+    static constexpr int NTL = DV / NTC;                   // CTAs (slices) per (sequence, head)
+    static constexpr int CW = NTC / 4;                     // state columns per conversion thread
+    static constexpr uint32_t TILE = C * NTC * 4;          // one slice's U0 or O0 tile, fp32
+    static constexpr uint32_t SB = K2_B0 + K2_NB * K2_BSTAGE;   // [S_hi | S_lo] bf16, MN-major SW128, K = 128 rows, N = 2 NTC
+    static constexpr uint32_t UB = SB + 128 * 4 * NTC;     // [U_hi | U_lo] bf16, MN-major SW128, K = 64 rows, N = 2 NTC
+    static constexpr uint32_t OS = UB + 64 * 4 * NTC;      // one chunk's bf16 output rows [64][NTC], 16-byte pieces swizzled
+    static constexpr uint32_t U0 = OS + 64 * 2 * NTC;      // U0 tile of this slice (workspace order), one chunk
+    static constexpr uint32_t O0 = U0 + TILE;              // O0 tile of this slice, one chunk
+    static constexpr uint32_t BAR = O0 + TILE;             // full / empty A, B; p; s; drain; full / empty U0, O0;
+                                                           // TMEM address; abort flag
+    static constexpr uint32_t BYTES = BAR + 192;
+    // TMEM: S [0, NTC), X [NTC, 2 NTC), P of even chunks [2 NTC, 4 NTC), of odd [4 NTC, 6 NTC)
+    static constexpr uint32_t TMEM_COLS = NTC == 64 ? 512 : 256;
+    static_assert(NTC == 64 || NTC == 32, "state-pass slice width");
+    static_assert(SB % 1024 == 0 && UB % 1024 == 0 && OS % 1024 == 0, "SW128 operands / swizzled output tile");
+    static_assert(BYTES + 1024 + 256 <= 232448, "chain smem");
+    static_assert(BAR + 15 * 8 + 8 <= BYTES, "chain barriers and flags");
+};
+static_assert(K2_B0 % 1024 == 0, "SW128 operands are 1024-byte aligned");
 static_assert(WS_KRL == WS_KR + 16384, "both parts of K_restore^T are one contiguous copy");
 static_assert(K1_AIL + 16384 <= K1_BWU, "[INV; X] must stay inside the alias region");
 static_assert(K1_ML + 16384 <= K1_BWU && K1_IL + 8192 <= K1_IS, "X operands stay inside the alias region");
@@ -157,9 +169,6 @@ static_assert(K1_AIL + 16384 <= K1_SG + 32768 && K1_ML + 16384 <= K1_SG + 32768,
 static_assert(K1_IS + 64 * LDS_ * 4 <= K1_XS && K1_XS + 4096 <= K1_MH && 16384 + 8192 <= K1_XS,
               "Q_decay rows land in the free L / INV region while the last MMA runs");
 static_assert(WS_BLOCK % 1024 == 0 && WS_AL + DK * 4 <= WS_BLOCK, "workspace block");
-static_assert(K2_BYTES + 1024 + 256 <= 232448, "chain smem");
-static_assert(K2_BAR + 15 * 8 + 8 <= K2_BYTES, "chain barriers and flags");
-static_assert(K2_OS % 1024 == 0, "the output tile is stored by a 128-byte-swizzled tensor copy");
 static_assert(2 * (K1_BYTES + 1024 + 1024) <= 233472, "prep must fit two CTAs per SM");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -986,17 +995,20 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 }
 
 // ============================================================== chain (a4, a5)
-// Per CTA: one (sequence, head) pair and NT = 64 columns of d_v.  TMEM columns:
-//   [0, 64)      S, the fp32 state slice (TMEM lane = key channel)
-//   [64, 128)    X, the low-part share K_restore^T U_lo of the state update,
-//                folded into S when the state is next read
-//   [128, 256)   P of even chunks, [256, 384) P of odd chunks:
-//                P = [Q'; W] [S_hi | S_lo]: columns 0..63 against the high
-//                part of S_in, 64..127 against its low part; lanes 0..63
-//                Q' S_in, lanes 64..127 W S_in
+// Per CTA: one (sequence, head) pair and NTC columns of d_v (64; or 32, with
+// four CTAs per pair, when the whole pass fits one wave: each conversion
+// thread then moves half as many values on the sequential path, while the
+// MMAs, issue-bound at this size, take as long).  TMEM columns:
+//   [0, NTC)          S, the fp32 state slice (TMEM lane = key channel)
+//   [NTC, 2 NTC)      X, the low-part share K_restore^T U_lo of the state
+//                     update, folded into S when the state is next read
+//   [2 NTC, 4 NTC)    P of even chunks, [4 NTC, 6 NTC) P of odd chunks:
+//                     P = [Q'; W] [S_hi | S_lo]: columns 0..NTC-1 against the
+//                     high part of S_in, the next NTC against its low part;
+//                     lanes 0..63 Q' S_in, lanes 64..127 W S_in
 // MMAs per chunk (16 instructions):
-//   P        = [Q'; W] [S_hi | S_lo]                        K = 128, N = 128 -> commit(p)
-//   [S | X] += K_hi^T [U_hi | U_lo] + K_lo^T [U_hi | U_lo]  K = 64,  N = 128 -> commit(s)
+//   P        = [Q'; W] [S_hi | S_lo]                        K = 128, N = 2 NTC -> commit(p)
+//   [S | X] += K_hi^T [U_hi | U_lo] + K_lo^T [U_hi | U_lo]  K = 64,  N = 2 NTC -> commit(s)
 // with U = U0 - W S_in, O = Q' S_in + O0, and S_in, K_restore and U each
 // carried as a high and a low bf16 part (x = hi + lo, |lo| <= 2^-8 |x|), so
 // that no operand of the sequential pass is rounded to a single bf16: the
@@ -1012,8 +1024,9 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // formed while chunk c + 1 runs, off the sequential path.
 // Warp roles:
 //   warps 0-15 conversion warps; warp w reads TMEM lanes 32 (w % 4) .. +31 and
-//              columns 16 (w / 4) .. +15 of each 64-wide block (four warps per
-//              sub-partition, so that their latencies overlap).
+//              columns CW (w / 4) .. +CW-1 (CW = NTC / 4) of each NTC-wide
+//              block (four warps per sub-partition, so that their latencies
+//              overlap).
 //              - all 16: S_in = S + X -> high/low bf16 operand; then
 //                S <- Diag(a_last) S_in, X <- 0
 //              - lanes 64..127 (w % 4 = 2, 3): U = U0 - W S_in -> high/low bf16 operand
@@ -1028,13 +1041,11 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 // is issued, every other wait returns at once, and before the CTA exits the
 // copies and MMAs already in flight are waited for (bounded again).
 constexpr int K2_CONV_WARPS = 16;
-constexpr int K2_CW = NT / (K2_CONV_WARPS / 4);   // state columns per conversion warp
 constexpr int K2_THREADS = 32 * (K2_CONV_WARPS + 3);
 constexpr int K2_SYNC = 32 * (K2_CONV_WARPS + 1);  // conversion warps + the MMA issuer
 constexpr int K2_ISSUER_WARP = K2_CONV_WARPS;
 constexpr int K2_PRODUCER_WARP = K2_CONV_WARPS + 1;
 constexpr int K2_TILE_WARP = K2_CONV_WARPS + 2;
-static_assert(K2_CW == 16, "conversion code below moves 16 columns per thread");
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -1043,6 +1054,7 @@ __device__ __forceinline__ void named_bar_arrive(int id, int count) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+template <int NTC>
 __global__ void __launch_bounds__(K2_THREADS, 1)
 kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, int nch_per_seq,
              int c_begin, int c_end, const uint8_t* __restrict__ ws_blocks, const float* __restrict__ S0, int H,
@@ -1053,12 +1065,18 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     // from a zero state (its affine offset, into S_final), blockIdx.z = 1 from
     // the identity with U0 taken as zero (its linear map, into S_final_map);
     // neither writes O.
+    using Cfg = ChainCfg<NTC>;
+    constexpr int K2_CW = Cfg::CW;
+    constexpr uint32_t K2_SB = Cfg::SB, K2_UB = Cfg::UB, K2_OS = Cfg::OS, K2_U0 = Cfg::U0, K2_O0 = Cfg::O0;
     const bool run_map = seg_pass1 && blockIdx.z == 1;
     const bool write_o = !seg_pass1;
     if (run_map) S_final = S_final_map;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
-    const int tile = blockIdx.x % NTILES, n = blockIdx.x / NTILES, h = blockIdx.y;
+    const int tile = blockIdx.x % Cfg::NTL, n = blockIdx.x / Cfg::NTL, h = blockIdx.y;
+    // this slice's U0 / O0 tiles in a workspace block: the prep stores them per
+    // 64-column slice, and a 32-column slice is one half of such a tile
+    const uint32_t ws_u0 = WS_UO + 2 * TILE_F32 * (uint32_t)((tile * NTC) / 64) + (uint32_t)((tile * NTC) % 64) * C * 4;
     int bos, len, first, nch;
     if (!use_table) {
         bos = n * fixed_len; len = fixed_len; first = n * nch_per_seq; nch = nch_per_seq;
@@ -1080,14 +1098,14 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     // store this thread's K2_CW state values as checkpoint `idx` (if it fits)
     auto put_ckpt = [&](int idx, const float* vals, int row_, int col0) {
         if (idx < 0 || idx >= ckpt_cap) return;
-        float4* dst = reinterpret_cast<float4*>(ckpt + (((size_t)idx * H + h) * DK + row_) * DV + tile * NT + col0);
+        float4* dst = reinterpret_cast<float4*>(ckpt + (((size_t)idx * H + h) * DK + row_) * DV + tile * NTC + col0);
 #pragma unroll
         for (int u = 0; u < K2_CW / 4; ++u)
             dst[u] = make_float4(vals[4 * u], vals[4 * u + 1], vals[4 * u + 2], vals[4 * u + 3]);
     };
     auto block_of = [&](int c) { return ws_blocks + ((size_t)(first + cb + c) * H + h) * WS_BLOCK; };
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + K2_BAR);
+    uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + Cfg::BAR);
     uint64_t* emptyA = fullA + K2_NA;
     uint64_t* fullB = emptyA + K2_NA;
     uint64_t* emptyB = fullB + K2_NB;
@@ -1101,7 +1119,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(emptyO + 1);
     volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
     if (w == 0) {
-        kda::tmem_alloc(tmem_slot, K2_TMEM_COLS);
+        kda::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
         kda::tmem_relinquish();
     }
     if (tid == 0) {
@@ -1142,7 +1160,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 ++nA;
                 // this chunk's U0 / O0 tiles (copied by the tile warp when their
                 // buffers come free) and a_last (loaded by every conversion thread) into L2
-                kda::bulk_prefetch_l2(block_of(k) + WS_UO + 2 * TILE_F32 * tile, 2 * TILE_F32);
+                kda::bulk_prefetch_l2(block_of(k) + ws_u0, Cfg::TILE);
+                kda::bulk_prefetch_l2(block_of(k) + ws_u0 + TILE_F32, Cfg::TILE);
                 kda::bulk_prefetch_l2(block_of(k) + WS_AL, DK * 4);
                 const int sb = k % K2_NB;
                 if (k >= K2_NB) wait(emptyB + sb, (uint32_t)(((k - K2_NB) / K2_NB) & 1));
@@ -1164,17 +1183,17 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         if (lane == 0) {
             int nU = 0, nO = 0;                             // copies issued into each tile
             for (int k = 0; k < nloc && !*abort_f; ++k) {
-                const uint8_t* uo = block_of(k) + WS_UO + 2 * TILE_F32 * tile;
+                const uint8_t* uo = block_of(k) + ws_u0;
                 if (k > 0) wait(emptyU, (uint32_t)((k - 1) & 1));
                 if (*abort_f) break;
-                kda::mbar_arrive_expect_tx(fullU, TILE_F32);
-                kda::bulk_g2s(sm + K2_U0, uo, TILE_F32, fullU);
+                kda::mbar_arrive_expect_tx(fullU, Cfg::TILE);
+                kda::bulk_g2s(sm + K2_U0, uo, Cfg::TILE, fullU);
                 ++nU;
                 if (!write_o) continue;                     // no output rows: O0 is not needed
                 if (k > 0) wait(emptyO, (uint32_t)((k - 1) & 1));
                 if (*abort_f) break;
-                kda::mbar_arrive_expect_tx(fullO, TILE_F32);
-                kda::bulk_g2s(sm + K2_O0, uo + TILE_F32, TILE_F32, fullO);
+                kda::mbar_arrive_expect_tx(fullO, Cfg::TILE);
+                kda::bulk_g2s(sm + K2_O0, uo + TILE_F32, Cfg::TILE, fullO);
                 ++nO;
             }
             if (*abort_f) {                                 // the newest copy into each tile
@@ -1196,8 +1215,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             if (lane == 0 && !*abort_f) {                   // P = [Q'; W] [S_hi | S_lo]
                 kda::tc_fence_after();
                 const uint64_t ad0 = kda::sw128_desc(kda::smem_u32(sm + sa * K2_ASTAGE), 16, 1024);
-                const uint32_t idesc = kda::idesc_bf16(128, 2 * NT, 0, 1);
-                const uint32_t tP = tmem + 128 + 128 * (c & 1);
+                const uint32_t idesc = kda::idesc_bf16(128, 2 * NTC, 0, 1);
+                const uint32_t tP = tmem + 2 * NTC + 2 * NTC * (c & 1);
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
                     kda::umma_bf16(tP, ad0 + kda::desc_step((s >> 2) * 16384 + (s & 3) * 32),
@@ -1211,7 +1230,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             if (lane == 0 && !*abort_f) {                   // [S | X] += K_hi^T [U_hi | U_lo] + K_lo^T [U_hi | U_lo]
                 kda::tc_fence_after();
                 const uint64_t ad0 = kda::sw128_desc(kda::smem_u32(sm + K2_B0 + sb * K2_BSTAGE), 8192, 1024);
-                const uint32_t id_s = kda::idesc_bf16(128, 2 * NT, 1, 1);
+                const uint32_t id_s = kda::idesc_bf16(128, 2 * NTC, 1, 1);
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
                     kda::umma_bf16(tmem, ad0 + kda::desc_step((s >> 2) * 16384 + (s & 3) * 2048),
@@ -1232,18 +1251,27 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         const int row = 32 * quad + lane;                       // TMEM lane = state row / P row
         const int col0 = K2_CW * grp;                           // this warp's first column of the slice
         const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-        const uint32_t tS = tmem + lane_off + col0;             // this warp's state columns (X at +64)
-        const uint32_t tP = tmem + lane_off + 128 + col0;       // ... of P (buffer of chunk parity at +128)
+        const uint32_t tS = tmem + lane_off + col0;             // this warp's state columns (X at +NTC)
+        const uint32_t tP = tmem + lane_off + 2 * NTC + col0;   // ... of P (buffer of chunk parity at +2 NTC)
+        auto tld = [&](uint32_t ta, float* r) {
+            if constexpr (K2_CW == 16) kda::tmem_ld16(ta, r); else kda::tmem_ld8(ta, r);
+        };
+        auto tst = [&](uint32_t ta, const float* r) {
+            if constexpr (K2_CW == 16) kda::tmem_st16(ta, r); else kda::tmem_st8(ta, r);
+        };
         const bool u_rows = quad >= 2;                          // lanes 64..127: U; lanes 0..63: O
         // this thread's 16 values of a U0 or O0 tile in shared memory (row r of the chunk)
         auto read_tile = [&](uint32_t off, int r, float* dst) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < K2_CW / 4; ++j) {
                 const float4 x = *reinterpret_cast<const float4*>(sm + off + uo_off(r, col0 + 4 * j));
                 dst[4 * j] = x.x; dst[4 * j + 1] = x.y; dst[4 * j + 2] = x.z; dst[4 * j + 3] = x.w;
             }
         };
         const bool o_issuer = w == 0 && lane == 0;           // issues the output tensor stores
+        // 16-byte piece k of output row r in the staging tile: the 128-byte
+        // (NTC = 64) or 64-byte (NTC = 32) swizzle of the tensor store
+        auto o_swz = [](int r, int k) -> int { return NTC == 64 ? (k ^ (r & 7)) : (k ^ ((r >> 1) & 3)); };
         // O rows of chunk co (lanes 0..63 warps): P of that chunk is complete (the
         // state update issued after it is); staged in shared memory and stored
         auto out_rows = [&](int co) {
@@ -1254,8 +1282,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             if (lane == 0) kda::mbar_arrive(emptyO);
             kda::tc_fence_after();
             float ph[K2_CW], pl[K2_CW];
-            kda::tmem_ld16(tP + 128 * (co & 1), ph);
-            kda::tmem_ld16(tP + 128 * (co & 1) + 64, pl);
+            tld(tP + 2 * NTC * (co & 1), ph);
+            tld(tP + 2 * NTC * (co & 1) + NTC, pl);
             kda::tmem_wait_ld();
             uint4 ov[K2_CW / 8];
 #pragma unroll
@@ -1270,8 +1298,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             named_bar_sync(3, K2_CONV_WARPS * 16);             // every O warp is done with the last staged rows
 #pragma unroll
             for (int cc = 0; cc < K2_CW / 8; ++cc) {
-                const int k = (col0 + 8 * cc) / 8;               // 16-byte piece of the 128-byte row
-                *reinterpret_cast<uint4*>(ost + row * 128 + ((k ^ (row & 7)) << 4)) = ov[cc];
+                const int k = (col0 + 8 * cc) / 8;               // 16-byte piece of the row
+                *reinterpret_cast<uint4*>(ost + row * (2 * NTC) + (o_swz(row, k) << 4)) = ov[cc];
             }
             const int valid = len - (cb + co) * C;
             // a full chunk leaves by one tensor store (the staging order is the
@@ -1282,19 +1310,20 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             named_bar_sync(3, K2_CONV_WARPS * 16);             // the staged tile is complete
             if (whole) {
                 if (o_issuer && !*abort_f) {
-                    kda::tma_store_3d(&tm_o, tile * NT, h, bos + (cb + co) * C, ost);
+                    kda::tma_store_3d(&tm_o, tile * NTC, h, bos + (cb + co) * C, ost);
                     kda::bulk_commit();
                 }
             } else {
                 const int wo = (grp << 1) | quad;                // 0..7: rows 8 wo .. 8 wo + 7
+                constexpr int LR = NTC / 2;                      // lanes per row (4 bytes each)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int rr = 8 * wo + i;
+                for (int i = 0; i < 8 * LR / 32; ++i) {
+                    const int rr = 8 * wo + (32 / LR) * i + lane / LR, pc = lane % LR;
                     if (rr < valid) {
                         const uint32_t x = *reinterpret_cast<const uint32_t*>(
-                            ost + rr * 128 + (((lane >> 2) ^ (rr & 7)) << 4) + 4 * (lane & 3));
+                            ost + rr * (2 * NTC) + (o_swz(rr, pc >> 2) << 4) + 4 * (pc & 3));
                         *reinterpret_cast<uint32_t*>(O + ((size_t)(bos + (cb + co) * C + rr) * H + h) * DV +
-                                                     tile * NT + 2 * lane) = x;
+                                                     tile * NTC + 2 * pc) = x;
                     }
                 }
             }
@@ -1305,10 +1334,10 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             float s[K2_CW];
             if (run_map) {
 #pragma unroll
-                for (int u = 0; u < K2_CW; ++u) s[u] = (row == tile * NT + col0 + u) ? 1.f : 0.f;
+                for (int u = 0; u < K2_CW; ++u) s[u] = (row == tile * NTC + col0 + u) ? 1.f : 0.f;
             } else if (S0 && !seg_pass1) {
                 const float4* src = reinterpret_cast<const float4*>(S0 + (((size_t)n * H + h) * DK + row) * DV +
-                                                                    tile * NT + col0);
+                                                                    tile * NTC + col0);
 #pragma unroll
                 for (int u = 0; u < K2_CW / 4; ++u) {
                     const float4 x = src[u];
@@ -1318,10 +1347,10 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
 #pragma unroll
                 for (int u = 0; u < K2_CW; ++u) s[u] = 0.f;
             }
-            kda::tmem_st16(tS, s);
+            tst(tS, s);
 #pragma unroll
             for (int u = 0; u < K2_CW; ++u) s[u] = 0.f;
-            kda::tmem_st16(tS + 64, s);
+            tst(tS + NTC, s);
             kda::tmem_wait_st();
             kda::tc_fence_before();
             named_bar_sync(1, K2_SYNC);
@@ -1333,8 +1362,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             if (c > 0) wait(bar_s, (uint32_t)((c - 1) & 1));
             kda::tc_fence_after();
             float s[K2_CW], x[K2_CW];
-            kda::tmem_ld16(tS, s);
-            kda::tmem_ld16(tS + 64, x);
+            tld(tS, s);
+            tld(tS + NTC, x);
             kda::tmem_wait_ld();
 #pragma unroll
             for (int u = 0; u < K2_CW; ++u) s[u] += x[u];
@@ -1343,7 +1372,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 uint4 hi, lo;
                 split_pack8(s + 8 * cc, hi, lo);
                 *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(row, col0 + 8 * cc, 128)) = hi;
-                *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(row, NT + col0 + 8 * cc, 128)) = lo;
+                *reinterpret_cast<uint4*>(sm + K2_SB + kda::sw128(row, NTC + col0 + 8 * cc, 128)) = lo;
             }
             kda::fence_proxy_async_smem();
             kda::tc_fence_before();
@@ -1355,8 +1384,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
             // ---- S <- Diag(a_last) S_in, X <- 0 while the P product runs
 #pragma unroll
             for (int u = 0; u < K2_CW; ++u) { s[u] *= al; x[u] = 0.f; }
-            kda::tmem_st16(tS, s);
-            kda::tmem_st16(tS + 64, x);
+            tst(tS, s);
+            tst(tS + NTC, x);
             kda::tmem_wait_st();
             if (u_rows) {
                 // ---- U = U0 - W S_in -> high/low bf16 operand
@@ -1369,8 +1398,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                 kda::tc_fence_after();
                 const int r = row - 64;
                 float ph[K2_CW], pl[K2_CW];
-                kda::tmem_ld16(tP + 128 * (c & 1), ph);
-                kda::tmem_ld16(tP + 128 * (c & 1) + 64, pl);
+                tld(tP + 2 * NTC * (c & 1), ph);
+                tld(tP + 2 * NTC * (c & 1) + NTC, pl);
                 kda::tmem_wait_ld();
 #pragma unroll
                 for (int cc = 0; cc < K2_CW / 8; ++cc) {
@@ -1380,9 +1409,8 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
                         f[u] = (run_map ? 0.f : uo[8 * cc + u]) - (ph[8 * cc + u] + pl[8 * cc + u]);
                     uint4 hi, lo;
                     split_pack8(f, hi, lo);
-                    const uint32_t off = kda::sw128(r, col0 + 8 * cc, 64);
-                    *reinterpret_cast<uint4*>(sm + K2_UB + off) = hi;
-                    *reinterpret_cast<uint4*>(sm + K2_UB + 8192 + off) = lo;
+                    *reinterpret_cast<uint4*>(sm + K2_UB + kda::sw128(r, col0 + 8 * cc, 64)) = hi;
+                    *reinterpret_cast<uint4*>(sm + K2_UB + kda::sw128(r, NTC + col0 + 8 * cc, 64)) = lo;
                 }
                 kda::fence_proxy_async_smem();
                 kda::tc_fence_before();
@@ -1400,15 +1428,15 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
         const bool end_ckpt = ckpt_every > 0 && nloc > 0 && cb + nloc == nch && len % ckpt_every == 0;
         if (S_final || end_ckpt) {
             float s[K2_CW], x[K2_CW];
-            kda::tmem_ld16(tS, s);
-            kda::tmem_ld16(tS + 64, x);
+            tld(tS, s);
+            tld(tS + NTC, x);
             kda::tmem_wait_ld();
 #pragma unroll
             for (int u = 0; u < K2_CW; ++u) s[u] += x[u];
             if (end_ckpt) put_ckpt(ck_base + len / ckpt_every - 1, s, row, col0);
             if (S_final) {
                 float4* dst = reinterpret_cast<float4*>(S_final + (((size_t)n * H + h) * DK + row) * DV +
-                                                        tile * NT + col0);
+                                                        tile * NTC + col0);
 #pragma unroll
                 for (int u = 0; u < K2_CW / 4; ++u)
                     dst[u] = make_float4(s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]);
@@ -1417,7 +1445,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     }
     kda::tc_fence_before();
     __syncthreads();
-    if (w == 0) kda::tmem_dealloc(tmem, K2_TMEM_COLS);
+    if (w == 0) kda::tmem_dealloc(tmem, Cfg::TMEM_COLS);
 }
 
 // ============================================================== segment scan
@@ -1616,16 +1644,18 @@ cudaError_t make_input_map(CUtensorMap* m, const void* base, int esize, int H, i
 }
 
 // Tensor map of the output O [T][H][d_v] bf16 for the state pass's stores: one
-// box = 64 tokens x one head x NT channels, 128-byte swizzled in shared memory.
-cudaError_t make_output_map(CUtensorMap* m, void* base, int H, int T) {
+// box = 64 tokens x one head x ntc channels, swizzled in shared memory by the
+// row's byte width (128 bytes for ntc = 64, 64 for ntc = 32).
+cudaError_t make_output_map(CUtensorMap* m, void* base, int H, int T, int ntc) {
     auto enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     const cuuint64_t dims[3] = {(cuuint64_t)DV, (cuuint64_t)H, (cuuint64_t)T};
     const cuuint64_t strides[2] = {(cuuint64_t)DV * 2, (cuuint64_t)H * DV * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)NT, 1, (cuuint32_t)C};
+    const cuuint32_t box[3] = {(cuuint32_t)ntc, 1, (cuuint32_t)C};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           ntc == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -1786,20 +1816,26 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         if (e != cudaSuccess) return e;
     }
     const int prep_smem = (int)(K1_BYTES + 1024);
-    const int chain_smem = (int)(K2_BYTES + 1024);
+    const int chain_smem = (int)(ChainCfg<64>::BYTES + 1024);
+    const int narrow_smem = (int)(ChainCfg<32>::BYTES + 1024);
     auto prep_kernel = a.prologue ? kda_tc_prep<true> : kda_tc_prep<false>;
     cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kda_tc_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
+    e = cudaFuncSetAttribute(kda_tc_chain<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kda_tc_chain<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, narrow_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kda_tc_seg_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM);
     if (e != cudaSuccess) return e;
 
+    // the state pass over 32-column slices when that still fits one wave of CTAs
+    // (one per SM) and runs alone (no segment scan, no prep beside it)
+    const bool narrow = !use_seg && n_slices == 1 && 4LL * a.n_seq * a.H <= n_sm;
     CUtensorMap tm_q, tm_k, tm_v, tm_g, tm_o;
     std::memset(&tm_o, 0, sizeof(tm_o));
     // full output chunks leave the state pass by tensor stores when O is 16-byte aligned
     const int o_tma = a.T_total > 0 && a.O != nullptr && (reinterpret_cast<uintptr_t>(a.O) & 15) == 0;
-    if (o_tma && (e = make_output_map(&tm_o, a.O, a.H, a.T_total)) != cudaSuccess) return e;
+    if (o_tma && (e = make_output_map(&tm_o, a.O, a.H, a.T_total, narrow ? 32 : 64)) != cudaSuccess) return e;
     if (a.T_total > 0) {
         if ((e = make_input_map(&tm_q, a.q, 2, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
         if ((e = make_input_map(&tm_k, a.k, 2, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
@@ -1819,9 +1855,14 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         return cudaGetLastError();
     };
     auto chain = [&](int c0, int c1, const float* s_in, float* s_out, cudaStream_t st) {
-        kda_tc_chain<<<dim3(NTILES * a.n_seq, a.H), K2_THREADS, chain_smem, st>>>(
-            seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
-            a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub, tm_o, o_tma);
+        if (narrow)
+            kda_tc_chain<32><<<dim3(ChainCfg<32>::NTL * a.n_seq, a.H), K2_THREADS, narrow_smem, st>>>(
+                seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
+                a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub, tm_o, o_tma);
+        else
+            kda_tc_chain<64><<<dim3(NTILES * a.n_seq, a.H), K2_THREADS, chain_smem, st>>>(
+                seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
+                a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub, tm_o, o_tma);
         return cudaGetLastError();
     };
 
@@ -1832,7 +1873,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
                                                   seg_info, seq_seg, a.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // pass 1: every segment from zero (-> seg_B) and as a map from the identity (-> seg_A)
-        kda_tc_chain<<<dim3(NTILES * sp.s_max, a.H, 2), K2_THREADS, chain_smem, a.stream>>>(
+        kda_tc_chain<64><<<dim3(NTILES * sp.s_max, a.H, 2), K2_THREADS, chain_smem, a.stream>>>(
             seg_info, 1, 0, 0, 0, INT32_MAX, blocks, nullptr, a.H, static_cast<bf16*>(a.O), seg_B, 0, nullptr, 0,
             a.status, 1, seg_A, (int)ub, tm_o, o_tma);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1842,7 +1883,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
                                                                                        sp.s_max, a.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // pass 3: every segment from its starting state, writing O
-        kda_tc_chain<<<dim3(NTILES * sp.s_max, a.H), K2_THREADS, chain_smem, a.stream>>>(
+        kda_tc_chain<64><<<dim3(NTILES * sp.s_max, a.H), K2_THREADS, chain_smem, a.stream>>>(
             seg_info, 1, 0, 0, 0, INT32_MAX, blocks, seg_S, a.H, static_cast<bf16*>(a.O), nullptr, 0, nullptr, 0,
             a.status, 0, nullptr, (int)ub, tm_o, o_tma);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -185,6 +185,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* r) {
           "=r"(u[30]), "=r"(u[31])
         : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float* r) {
+    const uint32_t* u = reinterpret_cast<const uint32_t*>(r);
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(u[0]),
+                 "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* r) {
     const uint32_t* u = reinterpret_cast<const uint32_t*>(r);
     asm volatile(
