@@ -469,17 +469,22 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         // inputs: one TMA copy per tensor, rows past the end of the tensor read
         // as zero.  The log-decay tile and V were copied during the previous
         // item's epilogue (the first item's are copied here); q and k once the
-        // previous item's [Q'; W] image has left shared memory.
-        if (tid == 0 && !*abort_f) {
-            if (!gv_ready) load_gv(tok0, h);
+        // previous item's [Q'; W] image has left shared memory (they land where
+        // it was staged): thread 0 waits for that after the first barrier, not
+        // before it, unless the fused prologue needs q and k right away.
+        auto issue_qk = [&]() {
             kda::bulk_wait_read_all();
             kda::mbar_arrive_expect_tx(bar_qk, K1_QK_BYTES);
             kda::tma_load_3d(sm + K1_SQ, &tm_q, 0, h, tok0, bar_qk);
             kda::tma_load_3d(sm + K1_SK, &tm_k, 0, h, tok0, bar_qk);
             ++n_qk;
+        };
+        if (tid == 0 && !*abort_f) {
+            if (!gv_ready) load_gv(tok0, h);
+            if (PROLOGUE) issue_qk();
         }
         gv_ready = false;
-        float bt[4];                               // beta of this thread's rows
+        float bt[4];                               // beta of this thread's rows (used after the cumulative sum)
 #pragma unroll
         for (int i = 0; i < 4; ++i) bt[i] = beta[((size_t)tok0 + min(r0 + i, nrows - 1)) * H + h];
         wait(bar_gv, n_done & 1);
@@ -496,9 +501,6 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             if (r >= nrows) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) e[i][j] = 0.f;
-                bt[i] = 0.f;
-            } else if (PROLOGUE) {
-                bt[i] = kda::prologue_beta(bt[i]);
             }
         }
         // this thread's q and k row pieces (zero past the chunk's end)
@@ -520,6 +522,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             *reinterpret_cast<uint4*>(sm + K1_BWU + 16384 + kda::sw128(t, 8 * cc, 64)) = make_uint4(0u, 0u, 0u, 0u);
         }
         __syncthreads();                           // the log-decay tile is in registers
+        if (!PROLOGUE && tid == 0 && !*abort_f) issue_qk();
         float* nrm = reinterpret_cast<float*>(sm + K1_NRM);
         if (PROLOGUE) {
             wait(bar_qk, n_done & 1);
@@ -582,6 +585,9 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             *reinterpret_cast<float4*>(first + b * 128 + c0) = make_float4(e[0][0], e[0][1], e[0][2], e[0][3]);
             *reinterpret_cast<float4*>(first + b * 128 + c0 + 4) = make_float4(e[0][4], e[0][5], e[0][6], e[0][7]);
         }
+        // beta: zero past the chunk's end (the loads were issued at the item's start)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) bt[i] = r0 + i >= nrows ? 0.f : (PROLOGUE ? kda::prologue_beta(bt[i]) : bt[i]);
         if (p == 0 && cg == 0) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) beta_s[r0 + i] = bt[i];
