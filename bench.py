@@ -60,11 +60,11 @@ PROFILED_TRAFFIC = {
         "sources": {"csrc/prefill_tc.cu": "6bda46d6a61fa522", "csrc/umma.cuh": "284f4428858e7949",
                     "csrc/common.cuh": "9b104993be79c2d2"}},
     "kda_decode_kernel": {
-        "read_mb": 547.525376, "write_mb": 478.725120, "profile": "profiles/decode_N256_H32_D128.md",
-        "sources": {"csrc/decode.cu": "ca2b6a97d7eeaad3", "csrc/common.cuh": "10fad8ef65a72b1e"}},
+        "read_mb": 547.414016, "write_mb": 477.989376, "profile": "profiles/decode_N256_H32_D128.md",
+        "sources": {"csrc/decode.cu": "ca2b6a97d7eeaad3", "csrc/common.cuh": "9b104993be79c2d2"}},
     "kda_decode_multi_kernel": {
-        "read_mb": 621.046784, "write_mb": 492.997888, "profile": "profiles/decode_N256_H32_D128.md",
-        "sources": {"csrc/decode.cu": "ca2b6a97d7eeaad3", "csrc/common.cuh": "10fad8ef65a72b1e"}},
+        "read_mb": 621.050880, "write_mb": 491.888128, "profile": "profiles/decode_N256_H32_D128.md",
+        "sources": {"csrc/decode.cu": "ca2b6a97d7eeaad3", "csrc/common.cuh": "9b104993be79c2d2"}},
 }
 
 
