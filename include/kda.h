@@ -33,12 +33,18 @@
  *   - All tensor arguments are caller-owned, contiguous, row-major DEVICE
  *     pointers (cu_seqlens_host is the one host pointer).  The library never
  *     allocates device memory and never synchronises the stream, except in
- *     kda_get_last_device_status.
+ *     kda_get_last_device_status and once per device in the first long
+ *     tensor-core prefill (below).
  *   - Work is enqueued on `stream` (0 = the legacy default stream).  A call
- *     returns once the work is enqueued.  A long tensor-core prefill forks
- *     part of its work onto an internal high-priority stream of the library
- *     (created once per device, kept until exit) and joins it back into
- *     `stream` with events before returning, so ordering on `stream` holds.
+ *     returns once the work is enqueued.  A long tensor-core prefill (the
+ *     longest sequence at least 1024 chunks, its state pass on at most half
+ *     of the SMs) forks part of its work onto an internal high-priority
+ *     stream of the library (created once per device, kept until exit) and
+ *     joins it back into `stream` with events before returning, so ordering
+ *     on `stream` holds.  The first such call on a device, unless `stream`
+ *     is being captured into a graph, also runs a ~10 us kernel that finds
+ *     which SM ids the device has (32 bytes of the workspace) and waits for
+ *     it on `stream`; later calls reuse the result.
  *   - Arguments are checked before anything is launched; a failed check
  *     returns an error and launches nothing.  A launch failure returns
  *     KDA_ERR_CUDA.  Faults detected inside a kernel (a wait that ran out of
