@@ -274,7 +274,8 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 // later access leaves the arrays even for an inconsistent device cu_seqlens.
 __global__ void __launch_bounds__(1024)
 kda_tc_schedule(const int32_t* __restrict__ cu, int n_seq, int T_total, int slots,
-                int4* __restrict__ chunk_info, int4* __restrict__ seq_info, int* status) {
+                int4* __restrict__ chunk_info, int4* __restrict__ seq_info, int* __restrict__ seq_order,
+                int* status) {
     __shared__ int part[1024];
     __shared__ int total;
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -307,6 +308,20 @@ kda_tc_schedule(const int32_t* __restrict__ cu, int n_seq, int T_total, int slot
         first += nch;
     }
     for (int s = total + tid; s < slots; s += nt) chunk_info[s] = make_int4(0, 0, -1, 0);
+    // the sequences by chunk count, longest first (ties by index), for the
+    // order of the state pass's CTAs (few sequences only: one rank a thread)
+    if (seq_order != nullptr && n_seq <= nt) {
+        __syncthreads();                          // seq_info of every sequence is written
+        if (tid < n_seq) {
+            const int mine = seq_info[tid].w;
+            int rank = 0;
+            for (int m = 0; m < n_seq; ++m) {
+                const int other = seq_info[m].w;
+                rank += (other > mine || (other == mine && m < tid)) ? 1 : 0;
+            }
+            seq_order[rank] = tid;
+        }
+    }
 }
 
 // ============================================================== prep (a1-a3)
@@ -1066,7 +1081,7 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
              int c_begin, int c_end, const uint8_t* __restrict__ ws_blocks, const float* __restrict__ S0, int H,
              bf16* __restrict__ O, float* __restrict__ S_final, int ckpt_every, float* __restrict__ ckpt,
              int ckpt_cap, int* status, int seg_pass1, float* __restrict__ S_final_map, int n_slots,
-             const __grid_constant__ CUtensorMap tm_o, int o_tma) {
+             const __grid_constant__ CUtensorMap tm_o, int o_tma, const int* __restrict__ seq_order) {
     // seg_pass1 (segment scan, first pass): blockIdx.z = 0 runs each segment
     // from a zero state (its affine offset, into S_final), blockIdx.z = 1 from
     // the identity with U0 taken as zero (its linear map, into S_final_map);
@@ -1079,7 +1094,11 @@ kda_tc_chain(const int4* __restrict__ seq_info, int use_table, int fixed_len, in
     if (run_map) S_final = S_final_map;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
-    const int tile = blockIdx.x % Cfg::NTL, n = blockIdx.x / Cfg::NTL, h = blockIdx.y;
+    // CTA -> (slice, sequence, head): grid (slices x sequences, heads), or with
+    // seq_order grid (slices x heads, sequences) with y the sequence's rank by length
+    const int tile = blockIdx.x % Cfg::NTL;
+    const int n = seq_order ? seq_order[blockIdx.y] : (int)(blockIdx.x / Cfg::NTL);
+    const int h = seq_order ? (int)(blockIdx.x / Cfg::NTL) : (int)blockIdx.y;
     // this slice's U0 / O0 tiles in a workspace block: the prep stores them per
     // 64-column slice, and a 32-column slice is one half of such a tile
     const uint32_t ws_u0 = WS_UO + 2 * TILE_F32 * (uint32_t)((tile * NTC) / 64) + (uint32_t)((tile * NTC) % 64) * C * 4;
@@ -1579,10 +1598,13 @@ kda_tc_seg_scan(const int2* __restrict__ seq_seg, const float* __restrict__ A, c
 
 // Workspace header: chunk table (16 B a slot), sequence table (16 B a
 // sequence), then kSliceWords 8-byte words: the item counters of the chunk-prep
-// slices that run beside the state pass (and, once per device, the SM-id mask).
+// slices that run beside the state pass (and, once per device, the SM-id mask),
+// then the sequences' order by length (4 B a sequence, up to kMaxOrdered).
 constexpr int kSliceWords = 8;
+constexpr int kMaxOrdered = 1024;            // the schedule kernel's block size
 size_t header_bytes(int n_seq, long long slots) {
-    const size_t raw = 16u * (size_t)slots + 16u * (size_t)n_seq + 8u * kSliceWords;
+    const size_t raw = 16u * (size_t)slots + 16u * (size_t)n_seq + 8u * kSliceWords +
+                       4u * (size_t)std::min(n_seq, kMaxOrdered);
     return (raw + 1023) & ~size_t(1023);
 }
 
@@ -1781,6 +1803,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     int4* seq_info = reinterpret_cast<int4*>(ws + 16 * (size_t)ub);
     // item counters of the prep slices that run beside the state pass
     unsigned long long* slice_ctr = reinterpret_cast<unsigned long long*>(ws + 16 * (size_t)ub + 16 * (size_t)a.n_seq);
+    int* seq_order = reinterpret_cast<int*>(ws + 16 * (size_t)ub + 16 * (size_t)a.n_seq + 8 * kSliceWords);
     float* S_mid = reinterpret_cast<float*>(ws + header_bytes(a.n_seq, ub));
     uint8_t* blocks = ws + header_bytes(a.n_seq, ub) + state_bytes(a.n_seq, a.H);
 
@@ -1814,10 +1837,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
                          !(use_table && a.max_chunks <= 0);
     const int n_slices = overlap ? std::min(kMaxSlices, max_chunks / kSliceChunks) : 1;
     const int slice = n_slices > 1 ? (max_chunks + n_slices - 1) / n_slices : max_chunks;
+    // the state pass over 32-column slices when that still fits one wave of CTAs
+    // (one per SM) and runs alone (no segment scan, no prep beside it)
+    const bool narrow = !use_seg && n_slices == 1 && 4LL * a.n_seq * a.H <= n_sm;
+    // more than one wave of state-pass CTAs over sequences of different
+    // lengths: the CTAs of the longest sequences go first (grid y = the
+    // sequence's rank by length), so that no long chain starts late
+    const bool ordered = use_table && !use_seg && !narrow && n_slices == 1 && chain_ctas > n_sm && a.n_seq > 1 &&
+                         a.n_seq <= kMaxOrdered;
 
     if (use_table) {
-        kda_tc_schedule<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.n_seq, a.T_total, (int)ub, chunk_info,
-                                                  seq_info, a.status);
+        kda_tc_schedule<<<1, kMaxOrdered, 0, a.stream>>>(a.cu_seqlens, a.n_seq, a.T_total, (int)ub, chunk_info,
+                                                         seq_info, ordered ? seq_order : nullptr, a.status);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -1834,9 +1865,6 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     e = cudaFuncSetAttribute(kda_tc_seg_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM);
     if (e != cudaSuccess) return e;
 
-    // the state pass over 32-column slices when that still fits one wave of CTAs
-    // (one per SM) and runs alone (no segment scan, no prep beside it)
-    const bool narrow = !use_seg && n_slices == 1 && 4LL * a.n_seq * a.H <= n_sm;
     CUtensorMap tm_q, tm_k, tm_v, tm_g, tm_o;
     std::memset(&tm_o, 0, sizeof(tm_o));
     // full output chunks leave the state pass by tensor stores when O is 16-byte aligned
@@ -1864,11 +1892,15 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         if (narrow)
             kda_tc_chain<32><<<dim3(ChainCfg<32>::NTL * a.n_seq, a.H), K2_THREADS, narrow_smem, st>>>(
                 seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
-                a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub, tm_o, o_tma);
+                a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub, tm_o, o_tma, nullptr);
+        else if (ordered)
+            kda_tc_chain<64><<<dim3(NTILES * a.H, a.n_seq), K2_THREADS, chain_smem, st>>>(
+                seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
+                a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub, tm_o, o_tma, seq_order);
         else
             kda_tc_chain<64><<<dim3(NTILES * a.n_seq, a.H), K2_THREADS, chain_smem, st>>>(
                 seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
-                a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub, tm_o, o_tma);
+                a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub, tm_o, o_tma, nullptr);
         return cudaGetLastError();
     };
 
@@ -1881,7 +1913,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         // pass 1: every segment from zero (-> seg_B) and as a map from the identity (-> seg_A)
         kda_tc_chain<64><<<dim3(NTILES * sp.s_max, a.H, 2), K2_THREADS, chain_smem, a.stream>>>(
             seg_info, 1, 0, 0, 0, INT32_MAX, blocks, nullptr, a.H, static_cast<bf16*>(a.O), seg_B, 0, nullptr, 0,
-            a.status, 1, seg_A, (int)ub, tm_o, o_tma);
+            a.status, 1, seg_A, (int)ub, tm_o, o_tma, nullptr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // pass 2: starting state of every segment, and the final states
         kda_tc_seg_scan<<<dim3(a.n_seq, a.H, DV / SC_COLS), 256, SC_SMEM, a.stream>>>(seq_seg, seg_A, seg_B, a.S0,
@@ -1891,7 +1923,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         // pass 3: every segment from its starting state, writing O
         kda_tc_chain<64><<<dim3(NTILES * sp.s_max, a.H), K2_THREADS, chain_smem, a.stream>>>(
             seg_info, 1, 0, 0, 0, INT32_MAX, blocks, seg_S, a.H, static_cast<bf16*>(a.O), nullptr, 0, nullptr, 0,
-            a.status, 0, nullptr, (int)ub, tm_o, o_tma);
+            a.status, 0, nullptr, (int)ub, tm_o, o_tma, nullptr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         trace_mark(a.stream);
         return cudaSuccess;

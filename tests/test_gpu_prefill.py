@@ -94,6 +94,20 @@ def test_tc_path_zero_state_and_device_only_cu_seqlens():
     assert eo <= 5e-3 and es <= 5e-3, (eo, es)
 
 
+@pytest.mark.parametrize("host_cu", [True, False])
+def test_tc_state_pass_longest_sequences_first(host_cu):
+    """More state-pass CTAs than SMs over sequences of different lengths (32
+    heads x 7 sequences, one of them empty): the CTAs are launched in the
+    order of their sequence's length, ranked on the device (also from a
+    device-only cu_seqlens); every sequence's rows and final state still come
+    out in place."""
+    dev = need_gpu()
+    w = inputs.Workload("tc", "prefill", H=32, dk=128, dv=128, dtype=torch.bfloat16, chunk=64, s0_std=0.02)
+    _, _, _, eo, es = run_case(w, dev, lengths=[300, 77, 0, 1000, 64, 1000, 5], seed=19, heads=(0, 3),
+                               host_cu=host_cu)
+    assert eo <= 5e-3 and es <= 5e-3, (eo, es)
+
+
 def test_tc_path_equal_lengths_without_cu_seqlens():
     """cu_seqlens = NULL: n_seq = 1 sequence covering all tokens."""
     dev = need_gpu()
