@@ -104,7 +104,9 @@ constexpr uint32_t K1_BYTES = 111936;
 constexpr int LDS_ = 68;                     // row stride (floats) of the fp32 64x64 matrices
 constexpr uint32_t K1_LS = 0;                // L   fp32 [64][68]
 constexpr uint32_t K1_IS = 17408;            // INV fp32 [64][68]
-constexpr uint32_t K1_XS = 34816;            // 4 x 16x16 fp32 scratch blocks (dense)
+constexpr uint32_t K1_XS = 34816;            // 4 x 16x16 fp32 scratch blocks (dense), slots 0-3
+constexpr uint32_t K1_XS2 = 55296;           // 4 more (slots 4-7), in the dead Gram A operand (the
+                                             //   [INV; X] low part lands there after the inverse)
 constexpr uint32_t K1_MH = 38912;            // M_qk high / low bf16 parts, K-major SW128, 64 rows, K = 64
 constexpr uint32_t K1_ML = 47104;            //   (the M = 128 product reads 64 rows past each: still in the tile)
 constexpr uint32_t K1_IH = 0;                // INV high / low bf16 parts, MN-major SW128, K = 64 rows, N = 64
@@ -166,6 +168,7 @@ static_assert(K1_BG + 160 * 256 <= K1_AG && K1_AG + 32768 == K1_BWU && K1_AG % 1
 static_assert(K1_SK + 16384 <= K1_AG && K1_SG + 32768 <= K1_BWU && (K1_BWU + 16384) % 1024 == 0, "input tiles");
 static_assert(K1_AIL + 16384 <= K1_SG + 32768 && K1_ML + 16384 <= K1_SG + 32768,
               "the next log-decay tile lands where only the last MMA's A operand was");
+static_assert(K1_XS2 >= K1_ML + 8192 && K1_XS2 + 4096 <= K1_AG + 32768, "inverse scratch slots 4-7");
 static_assert(K1_IS + 64 * LDS_ * 4 <= K1_XS && K1_XS + 4096 <= K1_MH && 16384 + 8192 <= K1_XS,
               "Q_decay rows land in the free L / INV region while the last MMA runs");
 static_assert(WS_BLOCK % 1024 == 0 && WS_AL + DK * 4 <= WS_BLOCK, "workspace block");
@@ -249,6 +252,17 @@ __device__ __forceinline__ void mm16(float (&acc)[8], const float* A, int lda, c
             mma_tf32(acc + 4 * h, ab, bs);
             mma_tf32(acc + 4 * h, ab, bb);
         }
+    }
+}
+
+// acc <- the 16x16 block C in the accumulator layout that st16 stores
+__device__ __forceinline__ void ld16(float (&acc)[8], const float* C, int ldc, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float2 a = *reinterpret_cast<const float2*>(C + g * ldc + 8 * h + 2 * t);
+        const float2 b = *reinterpret_cast<const float2*>(C + (g + 8) * ldc + 8 * h + 2 * t);
+        acc[4 * h] = a.x; acc[4 * h + 1] = a.y; acc[4 * h + 2] = b.x; acc[4 * h + 3] = b.y;
     }
 }
 
@@ -754,7 +768,6 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
         float* LS = reinterpret_cast<float*>(sm + K1_LS);
         float* IS = reinterpret_cast<float*>(sm + K1_IS);
-        float* XS = reinterpret_cast<float*>(sm + K1_XS);
         if (w < 4) gram_epilogue(tmem, w, lane, sm + K1_MH, sm + K1_ML, LS);
         kda::tc_fence_before();
         __syncthreads();
@@ -786,48 +799,58 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         __syncthreads();
         auto blkL = [&](int bi, int bj) { return LS + (16 * bi) * LDS_ + 16 * bj; };
         auto blkI = [&](int bi, int bj) { return IS + (16 * bi) * LDS_ + 16 * bj; };
-        // (2) INV_10 = -D1 (L10 D0), INV_32 = -D3 (L32 D2)   (warps 0, 1)
-        if (w < 2) {
-            const int b0 = 2 * w;
+        // scratch slots (dense 16x16): 0 F = L10 D0, 1 E = L32 D2, 2 -L21 D1, 3 -L31 D1,
+        // 4 L20 D0, 5 L30 D0, 6 Z00, 7 Z10
+        auto xs = [&](int i) { return reinterpret_cast<float*>(sm + (i < 4 ? K1_XS : K1_XS2)) + 256 * (i & 3); };
+        // The lower-left 2x2 block of INV is -INV_bottom Z with Z = L_[23][01] INV_top,
+        // INV_top / INV_bottom the inverses of the top-left / bottom-right 2x2 blocks;
+        // Z's blocks L20 D0 + L21 INV_10 (INV_10 = -D1 L10 D0) etc. are formed from
+        // products that need only the diagonal inverses, so the chain of dependent
+        // 16x16 products is four long (instead of six).
+        // (2) the products of L blocks with diagonal inverses (warps 0-5)
+        if (w < 6) {
+            // warp w: L block (bi, bj) times D_bj, with (bi, bj) = (1,0) (3,2) (2,1) (3,1) (2,0) (3,0),
+            // 4 bits per warp in one constant (no per-thread table in local memory)
+            const uint32_t code = (0x3276B1u >> (4 * w)) & 15u;    // warp 0 in the low nibble
+            const int bi = (int)(code & 3u), bj = (int)(code >> 2);
             float acc[8];
-            mm16(acc, blkL(b0 + 1, b0), LDS_, blkI(b0, b0), LDS_, lane, false);
-            st16(XS + 256 * w, 16, acc, lane, 1.f);
-            __syncwarp();
-            mm16(acc, blkI(b0 + 1, b0 + 1), LDS_, XS + 256 * w, 16, lane, false);
-            st16(blkI(b0 + 1, b0), LDS_, acc, lane, -1.f);
+            mm16(acc, blkL(bi, bj), LDS_, blkI(bj, bj), LDS_, lane, false);
+            st16(xs(w), 16, acc, lane, (w == 2 || w == 3) ? -1.f : 1.f);
         }
         __syncthreads();
-        // (3) X = L_[23][01] D_[01]:  X_i0 = L_{2+i,0} D0 + L_{2+i,1} INV_10,  X_i1 = L_{2+i,1} D1   (warps 0-3)
+        // (3) INV_10 = -D1 F, INV_32 = -D3 E, Z00 = L20 D0 - (L21 D1) F, Z10 = L30 D0 - (L31 D1) F  (warps 0-3)
         if (w < 4) {
-            const int xi = w >> 1, xj = w & 1;
             float acc[8];
-            if (xj == 0) {
-                mm16(acc, blkL(2 + xi, 0), LDS_, blkI(0, 0), LDS_, lane, false);
-                mm16(acc, blkL(2 + xi, 1), LDS_, blkI(1, 0), LDS_, lane, true);
+            if (w < 2) {
+                mm16(acc, blkI(2 * w + 1, 2 * w + 1), LDS_, xs(w), 16, lane, false);
+                st16(blkI(2 * w + 1, 2 * w), LDS_, acc, lane, -1.f);
             } else {
-                mm16(acc, blkL(2 + xi, 1), LDS_, blkI(1, 1), LDS_, lane, false);
+                ld16(acc, xs(w + 2), 16, lane);
+                mm16(acc, xs(w), 16, xs(0), 16, lane, true);
+                st16(xs(w + 4), 16, acc, lane, 1.f);
             }
-            st16(XS + 256 * w, 16, acc, lane, 1.f);
         }
         __syncthreads();
-        // (4) INV_[23][01] = -D_[23] X:  Y_0j = D2 X_0j,  Y_1j = INV_32 X_0j + D3 X_1j   (warps 0-3)
+        // (4) INV_20 = -D2 Z00, INV_21 = D2 (-Z01), INV_30 = -(INV_32 Z00 + D3 Z10),
+        //     INV_31 = INV_32 (-Z01) + D3 (-Z11)   (Z01 = L21 D1, Z11 = L31 D1; warps 0-3)
         if (w < 4) {
             const int yi = w >> 1, yj = w & 1;
             float acc[8];
+            const float* z0 = xs(yj ? 2 : 6);            // Z0j (negated for j = 1)
             if (yi == 0) {
-                mm16(acc, blkI(2, 2), LDS_, XS + 256 * yj, 16, lane, false);
+                mm16(acc, blkI(2, 2), LDS_, z0, 16, lane, false);
             } else {
-                mm16(acc, blkI(3, 2), LDS_, XS + 256 * yj, 16, lane, false);
-                mm16(acc, blkI(3, 3), LDS_, XS + 256 * (2 + yj), 16, lane, true);
+                mm16(acc, blkI(3, 2), LDS_, z0, 16, lane, false);
+                mm16(acc, blkI(3, 3), LDS_, xs(yj ? 3 : 7), 16, lane, true);
             }
-            st16(blkI(2 + yi, yj), LDS_, acc, lane, -1.f);
+            st16(blkI(2 + yi, yj), LDS_, acc, lane, yj ? 1.f : -1.f);
         }
         __syncthreads();
         // (5) X = M_qk INV on the tensor cores: INV -> high / low bf16 operand parts
         // (over L), then X = M_hi I_hi + M_hi I_lo + M_lo I_hi into TMEM
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int e = tid + 256 * it;
+        for (int half = 0; half < 2; ++half) {
+            const int e = tid + 256 * half;
             const int t = e >> 3, cc = e & 7;
             uint4 hi, lo;
             split_pack8(IS + t * LDS_ + 8 * cc, hi, lo);

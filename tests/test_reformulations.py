@@ -14,7 +14,10 @@ R2  S_out = A_c S_in + B_c, A_c = Diag(a_last) - K_restore^T W,
 R3  composing those maps over a segment of chunks, scanning the segments'
     maps for their starting states and re-running every segment from its
     starting state gives the token loop's outputs and final state;
-R4  (I + L)^-1 from 16x16 diagonal blocks and two levels of 2x2 block merges;
+R4  (I + L)^-1 from 16x16 diagonal blocks and two levels of 2x2 block merges,
+    and in the association the chunk-prep kernel uses (six products of L
+    blocks with the diagonal inverses first, so that the chain of dependent
+    products is four long);
 R5  the Gram weights exp(G_r - G_t) built from per-16-row-block reference
     points stay in the fp32 range at the page's log-decay bound (-5, 0), where
     the page's K_inv = K / a does not.
@@ -176,6 +179,43 @@ def test_r4_block_merge_inverse(n):
     ref = scipy.linalg.solve_triangular(np.eye(n) + L, np.eye(n), lower=True, unit_diagonal=True)
     assert rel(block_merge_inverse(L), ref) < 1e-12
     assert np.max(np.abs(block_merge_inverse(L) @ (np.eye(n) + L) - np.eye(n))) < 1e-12
+
+
+def four_block_inverse(L, b=16):
+    """(I + L)^-1 for a 4b x 4b strictly lower L the way the chunk-prep kernel
+    associates it: diagonal inverses D_i, then six products that need only
+    them, F = L10 D0, E = L32 D2, B0 = L21 D1, B1 = L31 D1, C0 = L20 D0,
+    C1 = L30 D0; then INV_10 = -D1 F, INV_32 = -D3 E and the blocks of
+    Z = L_[23][01] INV_top as Z00 = C0 - B0 F, Z10 = C1 - B1 F, Z01 = B0,
+    Z11 = B1; finally the lower-left quarter -INV_bottom Z."""
+    M = np.eye(4 * b) + L
+    blk = lambda X, i, j: X[b * i:b * (i + 1), b * j:b * (j + 1)]
+    D = [np.linalg.inv(blk(M, i, i)) for i in range(4)]
+    F, E = blk(L, 1, 0) @ D[0], blk(L, 3, 2) @ D[2]
+    B0, B1 = blk(L, 2, 1) @ D[1], blk(L, 3, 1) @ D[1]
+    C0, C1 = blk(L, 2, 0) @ D[0], blk(L, 3, 0) @ D[0]
+    I10, I32 = -D[1] @ F, -D[3] @ E
+    Z00, Z10 = C0 - B0 @ F, C1 - B1 @ F
+    INV = np.zeros_like(M)
+    for i in range(4):
+        INV[b * i:b * (i + 1), b * i:b * (i + 1)] = D[i]
+    INV[b:2 * b, 0:b], INV[3 * b:4 * b, 2 * b:3 * b] = I10, I32
+    INV[2 * b:3 * b, 0:b] = -D[2] @ Z00
+    INV[2 * b:3 * b, b:2 * b] = -D[2] @ B0
+    INV[3 * b:4 * b, 0:b] = -(I32 @ Z00 + D[3] @ Z10)
+    INV[3 * b:4 * b, b:2 * b] = -(I32 @ B0 + D[3] @ B1)
+    return INV
+
+
+@pytest.mark.parametrize("strong_decay", [False, True])
+def test_r4_four_block_association_of_the_kernel(strong_decay):
+    """The 64 x 64 inverse in the kernel's association equals the triangular
+    solve, at both ends of the decay range."""
+    Q, K, V, g, beta, _ = chunk_inputs(60 + strong_decay, dk=32, dv=8, strong_decay=strong_decay)
+    L = chunk_terms(Q, K, V, g, beta)["L"]
+    ref = scipy.linalg.solve_triangular(np.eye(C) + L, np.eye(C), lower=True, unit_diagonal=True)
+    assert rel(four_block_inverse(L), ref) < 1e-12
+    assert np.max(np.abs(four_block_inverse(L) @ (np.eye(C) + L) - np.eye(C))) < 1e-12
 
 
 def test_r5_block_reference_staging_stays_in_fp32_range():
