@@ -56,8 +56,8 @@ PARTS = ("prefill", "decode", "verify", "few", "varlen", "long", "e2e")
 # them the traffic reads null until a new capture replaces the entry.
 PROFILED_TRAFFIC = {
     "kda_tc_prep": {
-        "read_mb": 337.512448, "write_mb": 482.086400, "profile": "profiles/prefill_tc_T8192_H32_D128.md",
-        "sources": {"csrc/prefill_tc.cu": "6bda46d6a61fa522", "csrc/umma.cuh": "284f4428858e7949",
+        "read_mb": 337.590528, "write_mb": 481.933824, "profile": "profiles/prefill_tc_T8192_H32_D128.md",
+        "sources": {"csrc/prefill_tc.cu": "67335db186e292a6", "csrc/umma.cuh": "306795314462cda0",
                     "csrc/common.cuh": "9b104993be79c2d2"}},
     "kda_decode_kernel": {
         "read_mb": 547.414016, "write_mb": 477.989376, "profile": "profiles/decode_N256_H32_D128.md",
