@@ -13,14 +13,14 @@
  * section "The KDA update, in plain words").  The gate is passed as
  * log_alpha = ln(alpha_t), expected in [-5, 0): the log-decay bound stated on
  * that page.  Values outside it are computed but not guaranteed to meet the
- * accuracy target.  Known limit of the bf16 tensor-core path: with no decay
- * on any channel (log_alpha = -1e-4 everywhere, the gate's upper clamp)
- * together with beta = 1 on every token, the rounding of the intra-chunk
- * operands (the Gram factors, K_decay, W) is carried by the state through the
- * whole sequence and the output error reaches about 5.8e-3 relative to
- * max|o| over 8192 tokens and 32 heads, past the 5e-3 bf16 target; with beta
- * from (0, 1) as drawn by sigmoid it stays inside (4.8e-3 at the same
- * extreme).  The fp32 CUDA-core path has no such limit.
+ * accuracy target.  The tightest case of the bf16 tensor-core path is the
+ * no-decay end of the range (log_alpha = -1e-4 on every channel, the gate's
+ * upper clamp), where the state carries each chunk's operand rounding through
+ * the whole sequence: over 8192 tokens and 32 heads the output error is about
+ * 4.8e-3 with beta = 1 on every token and 5.0e-3 with beta drawn by sigmoid,
+ * relative to max|o|, against the 5e-3 bf16 target (in that range the chunk
+ * prep feeds its Gram operands to the tensor cores as f16).  The fp32
+ * CUDA-core path stays well inside it (about 3e-3).
  *
  * Two entry points compute it:
  *   kda_prefill -- many tokens at once in the chunked form ("Kimi K3: the

@@ -59,6 +59,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "umma.cuh"
@@ -281,6 +282,24 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
     return make_uint4(kda::pack_bf16x2(f[0], f[1]), kda::pack_bf16x2(f[2], f[3]),
                       kda::pack_bf16x2(f[4], f[5]), kda::pack_bf16x2(f[6], f[7]));
 }
+
+// Eight values as f16 (nearest even) instead of bf16: three more mantissa bits
+// for a Gram operand whose values the chunk's decay range keeps inside f16.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint4 pack8g(const float* f, bool f16) {
+    if (f16)
+        return make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                          pack_f16x2(f[6], f[7]));
+    return pack8(f);
+}
+// Largest log-decay across one 16-row block (over every channel) for which
+// the Gram operands go to the tensor cores as f16: the column factors are at
+// most e^10 = 22026 (below f16's 65504; |k| <= 1 for unit-length keys, and
+// the factor itself is what the bound limits), the row factors at least e^-10.
+constexpr float kF16GramLog = 10.f;
 
 // ============================================================== schedule
 // cu_seqlens -> per-chunk (token start, rows, sequence) and per-sequence
@@ -628,6 +647,9 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         float myG[8], acc[8], fb[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) { acc[j] = 0.f; myG[j] = 0.f; fb[j] = 0.f; }
+        // the largest decay across a block, G(block start) - G(block end) =
+        // first - tot, decides the Gram operands' type for the whole item
+        bool wide = false;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             const float4 f0 = *reinterpret_cast<const float4*>(first + m * 128 + c0);
@@ -640,8 +662,13 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             for (int j = 0; j < 8; ++j) {
                 if (m == b) { myG[j] = acc[j] + fm[j]; fb[j] = fm[j]; }
                 acc[j] += tm[j];
+                wide |= !(fm[j] - tm[j] <= kF16GramLog);   // (a NaN counts as wide)
             }
         }
+        // Gram operands as f16 when every block's decay allows it (the weak-decay
+        // end of the gate range, where the rounding of q~ and k^ is carried
+        // through the most chunks), else bf16
+        const bool gram_f16 = !__syncthreads_or(wide);
         float ap[8], R[8];                         // a at the block start; a_last / a(block start)
 #pragma unroll
         for (int j = 0; j < 8; ++j) { ap[j] = __expf(myG[j]); R[j] = __expf(acc[j] - myG[j]); }
@@ -661,89 +688,96 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
             for (int j = 0; j < 8; ++j) e[i][j] = __expf(e[i][j] - fb[j]);
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = r0 + i;
-            float q[8], k[8];
-            load_qk(i, q, k);
-            if (PROLOGUE) {                        // unit-length q and k rows
-                const float iq = rsqrtf(nrm[r] + nrm[64 + r] + kda::kNormEps);
-                const float ik = rsqrtf(nrm[128 + r] + nrm[192 + r] + kda::kNormEps);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) { q[j] *= iq; k[j] *= ik; }
-            }
-            // each operand row is formed and stored before the next one is formed
-            // (few values live at a time)
-            {
-                float t[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) t[j] = q[j] * e[i][j];            // q~ (row factor)
-                *reinterpret_cast<uint4*>(sm + K1_AG + kda::sw128(32 * b + 4 * rq + i, c0, 128)) = pack8(t);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) t[j] *= ap[j];                    // Q_decay
-                // -> rows 0..63 of the [Q_decay; W] image (read back for Q')
-                *reinterpret_cast<uint4*>(blk + WS_A1 + kda::sw128(r, c0, 128)) = pack8(t);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) t[j] = bt[i] * k[j] * e[i][j];    // k^ = beta k (row factor)
-                *reinterpret_cast<uint4*>(sm + K1_AG + kda::sw128(32 * b + 16 + 4 * rq + i, c0, 128)) = pack8(t);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) t[j] = k[j] * e[i][j] * ap[j];    // K_decay
-                *reinterpret_cast<uint4*>(sm + K1_BWU + kda::sw128(r, c0, 64)) = pack8(t);
-            }
-            float kt[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) kt[j] = k[j] * __fdividef(1.f, e[i][j]);   // k (column factor, own block)
-            // K_restore -> K_restore^T images, high and low bf16 parts (MN-major:
-            // row = token, contiguous = channel)
-            {
-                float kr[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) kr[j] = kt[j] * R[j];
-                uint4 hi, lo;
-                split_pack8(kr, hi, lo);
-                const uint32_t off = kda::sw128(r, c0, 64);
-                *reinterpret_cast<uint4*>(blk + WS_KR + off) = hi;
-                *reinterpret_cast<uint4*>(blk + WS_KRL + off) = lo;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) e[i][j] = kt[j];           // kept for the later tiles
-        }
-        // the column operands overlay the q / k input tiles: every thread has read its rows
-        __syncthreads();
-        // own block's column operand (block b of tile b)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint4*>(sm + K1_BG + kda::sw128(8 * b * (b + 1) + r0 + i, c0, 160)) = pack8(e[i]);
-        // tiles m > b hold this block's column factors times a(p_m) / a(p_b) <= 1
-        // (a rolled loop keeps this replicated part of the code small)
-#pragma unroll 1
-        for (int m = b + 1; m < 4; ++m) {
-            float sc[8], gm[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) gm[j] = 0.f;
-            for (int mm = 0; mm < m; ++mm) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) gm[j] += tot[mm * 128 + c0 + j];
-            }
-            float gb[8];                           // this block's reference G_pb
-#pragma unroll
-            for (int j = 0; j < 8; ++j) gb[j] = 0.f;
-            for (int mm = 0; mm < b; ++mm) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) gb[j] += tot[mm * 128 + c0 + j];
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                sc[j] = __expf((gm[j] + first[m * 128 + c0 + j]) - (gb[j] + first[b * 128 + c0 + j]));
-            uint8_t* tile = sm + K1_BG + 1024 * m * (m + 1);        // row 8 m (m + 1), an 8-row atom boundary
-#pragma unroll
+        // the row operands and the Gram column tiles, once per operand type (a
+        // uniform branch over two copies, so that no store converts twice)
+        auto operands = [&](auto f16_tag) {
+            constexpr bool F16 = decltype(f16_tag)::value;
+    #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                float f[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) f[j] = e[i][j] * sc[j];
-                *reinterpret_cast<uint4*>(tile + kda::sw128(16 * b + 4 * rq + i, c0, 160)) = pack8(f);
+                const int r = r0 + i;
+                float q[8], k[8];
+                load_qk(i, q, k);
+                if (PROLOGUE) {                        // unit-length q and k rows
+                    const float iq = rsqrtf(nrm[r] + nrm[64 + r] + kda::kNormEps);
+                    const float ik = rsqrtf(nrm[128 + r] + nrm[192 + r] + kda::kNormEps);
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) { q[j] *= iq; k[j] *= ik; }
+                }
+                // each operand row is formed and stored before the next one is formed
+                // (few values live at a time)
+                {
+                    float t[8];
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) t[j] = q[j] * e[i][j];            // q~ (row factor)
+                    *reinterpret_cast<uint4*>(sm + K1_AG + kda::sw128(32 * b + 4 * rq + i, c0, 128)) = pack8g(t, F16);
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) t[j] *= ap[j];                    // Q_decay
+                    // -> rows 0..63 of the [Q_decay; W] image (read back for Q')
+                    *reinterpret_cast<uint4*>(blk + WS_A1 + kda::sw128(r, c0, 128)) = pack8(t);
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) t[j] = bt[i] * k[j] * e[i][j];    // k^ = beta k (row factor)
+                    *reinterpret_cast<uint4*>(sm + K1_AG + kda::sw128(32 * b + 16 + 4 * rq + i, c0, 128)) = pack8g(t, F16);
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) t[j] = k[j] * e[i][j] * ap[j];    // K_decay
+                    *reinterpret_cast<uint4*>(sm + K1_BWU + kda::sw128(r, c0, 64)) = pack8(t);
+                }
+                float kt[8];
+    #pragma unroll
+                for (int j = 0; j < 8; ++j) kt[j] = k[j] * __fdividef(1.f, e[i][j]);   // k (column factor, own block)
+                // K_restore -> K_restore^T images, high and low bf16 parts (MN-major:
+                // row = token, contiguous = channel)
+                {
+                    float kr[8];
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) kr[j] = kt[j] * R[j];
+                    uint4 hi, lo;
+                    split_pack8(kr, hi, lo);
+                    const uint32_t off = kda::sw128(r, c0, 64);
+                    *reinterpret_cast<uint4*>(blk + WS_KR + off) = hi;
+                    *reinterpret_cast<uint4*>(blk + WS_KRL + off) = lo;
+                }
+    #pragma unroll
+                for (int j = 0; j < 8; ++j) e[i][j] = kt[j];           // kept for the later tiles
             }
-        }
+            // the column operands overlay the q / k input tiles: every thread has read its rows
+            __syncthreads();
+            // own block's column operand (block b of tile b)
+    #pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint4*>(sm + K1_BG + kda::sw128(8 * b * (b + 1) + r0 + i, c0, 160)) = pack8g(e[i], F16);
+            // tiles m > b hold this block's column factors times a(p_m) / a(p_b) <= 1
+            // (a rolled loop keeps this replicated part of the code small)
+    #pragma unroll 1
+            for (int m = b + 1; m < 4; ++m) {
+                float sc[8], gm[8];
+    #pragma unroll
+                for (int j = 0; j < 8; ++j) gm[j] = 0.f;
+                for (int mm = 0; mm < m; ++mm) {
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) gm[j] += tot[mm * 128 + c0 + j];
+                }
+                float gb[8];                           // this block's reference G_pb
+    #pragma unroll
+                for (int j = 0; j < 8; ++j) gb[j] = 0.f;
+                for (int mm = 0; mm < b; ++mm) {
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) gb[j] += tot[mm * 128 + c0 + j];
+                }
+    #pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    sc[j] = __expf((gm[j] + first[m * 128 + c0 + j]) - (gb[j] + first[b * 128 + c0 + j]));
+                uint8_t* tile = sm + K1_BG + 1024 * m * (m + 1);        // row 8 m (m + 1), an 8-row atom boundary
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float f[8];
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] = e[i][j] * sc[j];
+                    *reinterpret_cast<uint4*>(tile + kda::sw128(16 * b + 4 * rq + i, c0, 160)) = pack8g(f, F16);
+                }
+            }
+        };
+        if (gram_f16) operands(std::true_type{});
+        else operands(std::false_type{});
         kda::fence_proxy_async_all();              // shared operands and the Q_decay rows read back later
         kda::tc_fence_before();
         __syncthreads();
@@ -753,7 +787,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         if (tid == 0 && !*abort_f) {
             kda::tc_fence_after();
             const uint32_t sAG = kda::smem_u32(sm + K1_AG), sBG = kda::smem_u32(sm + K1_BG);
-            const uint32_t idesc = kda::idesc_bf16(128, 160, 0, 0);
+            const uint32_t idesc = gram_f16 ? kda::idesc_f16(128, 160, 0, 0) : kda::idesc_bf16(128, 160, 0, 0);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint64_t ad = kda::sw128_desc(sAG + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);

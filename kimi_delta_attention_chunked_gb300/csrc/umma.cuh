@@ -234,6 +234,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, uint32
            | ((M >> 4) << 24);
 }
 
+// The same with f16 A and B (A and B always share one type).
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
+    return (1u << 4)                 // D format: f32
+           | (a_mn << 15) | (b_mn << 16)   // A, B format: f16 (0)
+           | ((N >> 3) << 17)
+           | ((M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {

@@ -41,6 +41,18 @@ def hilo(x):
     return h.astype(np.float64) + bf(x32 - h)
 
 
+def f16(x):
+    """Round to f16 (nearest even) via fp32: the Gram operands' type when the
+    chunk's decay range allows it (see model)."""
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.float16).to(torch.float64).numpy()
+
+
+# The kernel feeds the Gram operands as f16 instead of bf16 when, for every
+# 16-row block and channel of the chunk, G(block start) - G(block end) <= 10
+# (column factors <= e^10, inside f16's range).
+F16_GRAM_LOG = 10.0
+
+
 def tf32(x):
     """Round an fp32 value to tf32 (10 mantissa bits, nearest even), as an
     operand of a kind::tf32 MMA would carry it."""
@@ -83,13 +95,14 @@ def gram(rows, cols_k, G, incl, rnd):
     return out
 
 
-def model(q, k, v, g, beta, S0, split=True, exact=(), as_tf32=(), as_pair=(), as_single=()):
+def model(q, k, v, g, beta, S0, split=True, exact=(), as_tf32=(), as_pair=(), as_single=(), gram_f16=True):
     """Outputs and final state of the chunked form with the kernels' rounding
     points.  split=False carries every operand as a single bf16 part; the
     points named in ``exact`` (from POINTS) are not rounded at all, those in
     ``as_tf32`` are rounded to tf32 instead of bf16, single-part points in
     ``as_pair`` are carried as a high/low bf16 pair, and split points in
-    ``as_single`` as one bf16 part."""
+    ``as_single`` as one bf16 part.  gram_f16: the Gram operands are f16 in
+    the chunks whose decay range allows it, as built (else always bf16)."""
     exact_fn = lambda x: np.asarray(x, dtype=np.float64)
 
     def pick(name, f):
@@ -110,8 +123,10 @@ def model(q, k, v, g, beta, S0, split=True, exact=(), as_tf32=(), as_pair=(), as
         n = Q.shape[0]
         G = np.cumsum(g[sl], axis=0)
         a = np.exp(G)
-        M = gram(Q, K, G, True, pick("gram", bf))           # M_qk = tril(Q_decay K_inv^T)
-        L = b[:, None] * gram(K, K, G, False, pick("gram", bf))   # StrictTril(Diag(beta) K_decay K_inv^T)
+        span = max(np.max(G[p] - G[min(p + BLK, n) - 1]) for p in range(0, n, BLK))
+        g_rnd = f16 if (gram_f16 and split and span <= F16_GRAM_LOG) else bf
+        M = gram(Q, K, G, True, pick("gram", g_rnd))        # M_qk = tril(Q_decay K_inv^T)
+        L = b[:, None] * gram(K, K, G, False, pick("gram", g_rnd))   # StrictTril(Diag(beta) K_decay K_inv^T)
         INV = np.linalg.inv(np.eye(n) + L)                  # fp32 on the GPU
         X = pick("x", two)(M) @ pick("x", two)(INV)         # X = M_qk INV
         rhs = np.concatenate([pick("k_decay", bf)(K * a), V], axis=1)   # [K_decay | V]
@@ -174,10 +189,12 @@ def test_no_decay_extreme(beta_one):
     """log alpha = -1e-4 on every channel (the gate's upper clamp): the state
     hardly decays, so the state pass's bf16 operands carry their rounding
     through every later chunk.  As built (S_in, K_restore and U as high/low
-    pairs) the model keeps O inside the bar, also with beta = 1; with S_in and
-    K_restore as single bf16 parts it puts O past it.  A tf32 state pass would
-    do about as well as the pairs, and with the staged K_decay and Gram
-    operands in tf32 too O is near the floor set by the bf16 store of O."""
+    pairs; the Gram operands in f16, which this decay range allows) the model
+    keeps O inside the bar, also with beta = 1; with S_in and K_restore as
+    single bf16 parts it puts O past it, and with bf16 Gram operands beta = 1
+    loses most of the margin.  A tf32 state pass would do about as well as
+    the pairs, and with the staged K_decay and Gram operands in tf32 too O is
+    near the floor set by the bf16 store of O."""
     q, k, v, g, beta, S0 = workload(5, 1024 + 37, 0.0, 0.02)
     g = np.full_like(g, np.float32(-1e-4)).astype(np.float64)
     if beta_one:
@@ -187,14 +204,16 @@ def test_no_decay_extreme(beta_one):
     err = lambda OS: (rel(OS[0], O_ref), rel(OS[1], S_ref))
     state_pass = {"q_prime", "w", "s_in", "k_restore"}
     eo, es = err(model(q, k, v, g, beta, S0))
+    eo_bf, _ = err(model(q, k, v, g, beta, S0, gram_f16=False))
     eo_1, es_1 = err(model(q, k, v, g, beta, S0, as_single={"s_in", "k_restore"}))
     eo_t, es_t = err(model(q, k, v, g, beta, S0, as_tf32=state_pass))
     eo_t2, es_t2 = err(model(q, k, v, g, beta, S0, as_tf32=state_pass | {"k_decay", "gram"}))
     eo_store, _ = err(model(q, k, v, g, beta, S0, exact=set(POINTS) - {"o_store"}))
-    print(f"no decay (beta = 1: {beta_one}): as built O {eo:.2e} S {es:.2e}; single S_in, K_restore "
+    print(f"no decay (beta = 1: {beta_one}): as built O {eo:.2e} S {es:.2e}; bf16 Gram O {eo_bf:.2e}; single S_in, K_restore "
           f"O {eo_1:.2e} S {es_1:.2e}; tf32 state pass O {eo_t:.2e} S {es_t:.2e}; + tf32 K_decay, Gram "
           f"O {eo_t2:.2e} S {es_t2:.2e}; O store alone {eo_store:.2e}")
     assert eo <= 0.9 * BAR and es <= 0.6 * BAR, (eo, es)
+    assert eo <= eo_bf, (eo, eo_bf)                   # f16 Gram operands only help here
     assert eo_1 > BAR, eo_1                           # the single-part state pass misses the bar
     assert es_1 > 1.5 * es, (es_1, es)
     assert eo_t <= 0.85 * BAR
