@@ -56,15 +56,15 @@ PARTS = ("prefill", "decode", "verify", "few", "varlen", "long", "e2e")
 # them the traffic reads null until a new capture replaces the entry.
 PROFILED_TRAFFIC = {
     "kda_tc_prep": {
-        "read_mb": 337.590528, "write_mb": 481.933824, "profile": "profiles/prefill_tc_T8192_H32_D128.md",
-        "sources": {"csrc/prefill_tc.cu": "67335db186e292a6", "csrc/umma.cuh": "306795314462cda0",
-                    "csrc/common.cuh": "9b104993be79c2d2"}},
+        "read_mb": 336.892928, "write_mb": 483.446784, "profile": "profiles/prefill_tc_T8192_H32_D128.md",
+        "sources": {"csrc/prefill_tc.cu": "7e25e26e54257587", "csrc/umma.cuh": "351aa210ce878847",
+                    "csrc/common.cuh": "cef06e6ff0b08c46"}},
     "kda_decode_kernel": {
-        "read_mb": 547.414016, "write_mb": 477.989376, "profile": "profiles/decode_N256_H32_D128.md",
-        "sources": {"csrc/decode.cu": "ca2b6a97d7eeaad3", "csrc/common.cuh": "9b104993be79c2d2"}},
+        "read_mb": 547.411712, "write_mb": 477.935616, "profile": "profiles/decode_N256_H32_D128.md",
+        "sources": {"csrc/decode.cu": "ca2b6a97d7eeaad3", "csrc/common.cuh": "cef06e6ff0b08c46"}},
     "kda_decode_multi_kernel": {
-        "read_mb": 621.050880, "write_mb": 491.888128, "profile": "profiles/decode_N256_H32_D128.md",
-        "sources": {"csrc/decode.cu": "ca2b6a97d7eeaad3", "csrc/common.cuh": "9b104993be79c2d2"}},
+        "read_mb": 621.051648, "write_mb": 492.077056, "profile": "profiles/decode_N256_H32_D128.md",
+        "sources": {"csrc/decode.cu": "ca2b6a97d7eeaad3", "csrc/common.cuh": "cef06e6ff0b08c46"}},
 }
 
 
