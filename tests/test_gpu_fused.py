@@ -75,3 +75,25 @@ def test_fused_decode(dtype, dk, dv):
     eo, es = rel_err(o, o_ref), rel_err(S, S_ref)
     print(f"PARITY fused decode dtype={dtype} dk={dk} dv={dv} o={eo:.3e} S={es:.3e}")
     assert eo <= tol_for(dtype) and es <= tol_for(dtype), (eo, es)
+
+
+def test_fused_tensor_core_no_decay():
+    """The fused tensor-core prep at the no-decay end: gate pre-activations of
+    -40 give log alpha at the upper clamp (-1e-4) on every channel, and beta
+    logits of +20 give beta ~ 1, so the prep takes its f16 Gram operands in
+    the prologue instantiation too."""
+    dev = need_gpu()
+    w = inputs.Workload("fused_nodecay", "prefill", H=4, dk=128, dv=128, dtype=torch.bfloat16, chunk=64,
+                        s0_std=0.02)
+    d = inputs.make_prefill(w, device=dev, seed=23, lengths=[2048 + 29], raw=True)
+    d["gate"].fill_(-40.0)
+    d["beta_logit"].fill_(20.0)
+    O, Sf = kda.kda_prefill_fused(d["q"], d["k"], d["v"], d["gate"], d["beta_logit"], S0=d["S0"],
+                                  cu_seqlens=d["cu_seqlens"], cu_seqlens_host=d["cu_seqlens_host"], chunk=64)
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_device_status() == 0
+    O_ref, S_ref = oracle.prefill_fused(d["q"], d["k"], d["v"], d["gate"], d["beta_logit"],
+                                        cu_seqlens=d["cu_seqlens_host"], S0=d["S0"])
+    eo, es = rel_err(O, O_ref), rel_err(Sf, S_ref)
+    print(f"PARITY fused no-decay tc O={eo:.3e} S={es:.3e}")
+    assert eo <= 5e-3 and es <= 5e-3, (eo, es)
