@@ -11,7 +11,7 @@
 // parallel; only the state pass is sequential.  Two kernels:
 //
 //  kda_tc_prep   persistent, two CTAs per SM, one (chunk, head) item at a time.
-//      a1  gate prep: fp32 cumulative log-decay, then bf16 MMA operands.
+//      a1  gate prep: fp32 cumulative log-decay, then the MMA operands.
 //          K_inv = k / a would overflow (|cumsum| reaches 5 * 64 = 320 under
 //          the (-5, 0) log-decay bound of the "LLM architecture at trillion
 //          scale" page), so the Gram matrices are built per 16-row block b with
@@ -19,13 +19,15 @@
 //             row factor  q_r exp(G_r - G_pb), k_r exp(G_r - G_pb)   (<= 1)
 //             col factor  k_t exp(G_pb - G_t)  for t < p_b + 16      (<= e^75)
 //          so every exponent stays inside [-75, 75] (fp32/bf16 range) and the
-//          product equals the exact exp(G_r - G_t) weight.
+//          product equals the exact exp(G_r - G_t) weight.  Where no block
+//          decays by more than e^10 the Gram operands are f16 instead of bf16.
 //      a2  Gram MMAs (tcgen05, M = 128 stacked q/k rows; the four blocks'
 //          column operands stacked along N = 160): M_qk (diagonal included)
 //          and L (strict, beta folded in).
 //      a3  INV = (I + L)^-1 in fp32 (16x16 diagonal blocks by substitution,
-//          then two levels of 2x2 block merges done warp by warp) and
-//          X = M_qk INV; then one MMA with M = 128 stacked rows
+//          then the off-diagonal blocks from products of L blocks with those
+//          inverses, warp by warp) and X = M_qk INV; then one MMA with
+//          M = 128 stacked rows
 //             [INV Diag(beta); X Diag(beta)] [K_decay | V]
 //          gives W = INV Diag(beta) K_decay, U0 = INV Diag(beta) V and, in the
 //          same instruction, M_qk W and O0 = M_qk U0.  Since U = U0 - W S_in,
@@ -34,9 +36,10 @@
 //      Writes, per (chunk, head), the MMA-ready operand images the chain
 //      needs: [Q'; W], K_restore^T, U0, O0, a_last.
 //
-//  kda_tc_chain  one CTA per (sequence, head, 64-column slice of d_v);
+//  kda_tc_chain  one CTA per (sequence, head, 64- or 32-column slice of d_v);
 //      a4/a5  for each chunk in order (operands streamed by bulk copies into
-//          rings two and three stages deep), with S kept in TMEM in fp32:
+//          two rings of two stages, U0 / O0 tiles one chunk at a time), with
+//          S kept in TMEM in fp32:
 //             P  = [Q'; W] S_in                         (MMA, M = 128)
 //             U  = U0 - P_w                             (W S_in = K_decay part)
 //             O  = P_q + O0
@@ -44,15 +47,19 @@
 //
 // With few chains and long sequences the state pass runs as a segment scan
 // instead (kda_tc_segments, two passes of kda_tc_chain around kda_tc_seg_scan;
-// see the section "segment scan" below).
+// see the section "segment scan" below); with many chains and long sequences
+// the prep of later chunk slices runs beside the state pass (launch_prefill_tc).
 //
-// Precision: MMA operands are bf16 with fp32 accumulation.  The operands
-// whose rounding dominated the error budget -- [INV; X] Diag(beta) and U --
-// are carried as a high and a low bf16 part, and U0 and O0 stay fp32, which
-// leaves the bf16 output rounding as the largest single error term.
+// Precision: MMA operands are bf16 (or f16) with fp32 accumulation.  The
+// operands whose rounding mattered -- X, [INV; X] Diag(beta), and in the
+// state pass S_in, U and K_restore -- are carried as a high and a low bf16
+// part, and U0 and O0 stay fp32, which leaves the bf16 output rounding as the
+// largest single error term.
 //
 // Every wait on an asynchronous event is bounded; a wait that runs out records
-// KDA_ERR_TIMEOUT in the status word and the kernel runs to completion.
+// KDA_ERR_TIMEOUT in the status word and sets the CTA's abort flag: the CTA
+// issues no further copy or MMA, waits (bounded) for what is in flight, and
+// returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -69,7 +76,8 @@ namespace {
 using bf16 = __nv_bfloat16;
 
 constexpr int DK = 128, DV = 128, C = 64;
-constexpr int NT = 64;                       // d_v columns per chain CTA
+constexpr int NT = 64;                       // d_v columns of a workspace U0 / O0 tile (and of a state-pass
+                                             // CTA, unless it runs 32-column slices: ChainCfg)
 constexpr int NTILES = DV / NT;
 
 // ---- per (chunk, head) workspace block: images of shared-memory operands
