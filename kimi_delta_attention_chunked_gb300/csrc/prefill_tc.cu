@@ -76,8 +76,7 @@ namespace {
 using bf16 = __nv_bfloat16;
 
 constexpr int DK = 128, DV = 128, C = 64;
-constexpr int NT = 64;                       // d_v columns of a workspace U0 / O0 tile (and of a state-pass
-                                             // CTA, unless it runs 32-column slices: ChainCfg)
+constexpr int NT = 64;                       // d_v columns of a workspace U0 / O0 tile (ChainCfg: of a CTA)
 constexpr int NTILES = DV / NT;
 
 // ---- per (chunk, head) workspace block: images of shared-memory operands
