@@ -84,12 +84,34 @@ def test_tc_ckpt_device_only_lengths():
     assert e <= tol_for(w.dtype), e
 
 
-def test_tc_ckpt_one_sequence_sliced():
-    """One long sequence, few heads: the state pass runs in overlapped slices and
-    checkpoints fall on both sides of slice borders."""
+def test_tc_ckpt_one_sequence_narrow_slices():
+    """One sequence, few heads: the state pass runs over 32-column slices."""
     dev = need_gpu()
     w = inputs.Workload("tc_ckpt_one", "prefill", s0_std=0.02, **TC)
     e = run_ckpt(w, dev, [4096], 256, seed=13, one_seq=True, heads=(0, 2))
+    assert e <= tol_for(w.dtype), e
+
+
+def test_tc_ckpt_long_sequence_overlapped_slices():
+    """A long sequence (1027 chunks, 2 heads; checkpoints keep it off the
+    segment scan): the prep of later chunk slices runs beside the state pass,
+    which carries the state across slice borders, and checkpoints fall near
+    them."""
+    dev = need_gpu()
+    w = inputs.Workload("tc_ckpt_long", "prefill", H=2, dk=128, dv=128, dtype=torch.bfloat16, chunk=64,
+                        s0_std=0.02)
+    e = run_ckpt(w, dev, [64 * 1027], 8192, seed=14, one_seq=True)
+    assert e <= tol_for(w.dtype), e
+
+
+def test_tc_ckpt_many_heads_longest_sequences_first():
+    """More state-pass CTAs than SMs (32 heads x 7 sequences): the CTAs run in
+    the order of their sequence's length, and each writes its own sequence's
+    checkpoints."""
+    dev = need_gpu()
+    w = inputs.Workload("tc_ckpt_many", "prefill", H=32, dk=128, dv=128, dtype=torch.bfloat16, chunk=64,
+                        s0_std=0.02)
+    e = run_ckpt(w, dev, [300, 77, 0, 1000, 64, 1000, 5], 64, seed=15, heads=(0, 2))
     assert e <= tol_for(w.dtype), e
 
 
