@@ -60,11 +60,14 @@ def prefill_guarded(w, dev, lengths, seed, tol, host_cu=True):
     assert eo <= tol and es <= tol, (eo, es)
 
 
-# the tensor-core prefill's launch shapes: one state pass (varlen, device-only
-# lengths), the segment scan (2 heads, one long sequence), and prep slices
-# overlapped with the state pass on two streams (17 heads, one sequence)
+# the tensor-core prefill's launch shapes: one state pass over 32-column slices
+# (varlen, device-only lengths), the segment scan (2 heads, one long
+# sequence), prep slices beside the state pass on two streams (17 heads, one
+# sequence of 1025 chunks), and more state-pass CTAs than SMs, launched
+# longest sequence first (32 heads, 7 sequences)
 TC_CASES = {"tc_varlen": (4, [300, 77, 0, 129, 1]), "tc_device_lengths": (4, [300, 77, 0, 129, 1]),
-            "tc_segment_scan": (2, [64 * 40 + 17]), "tc_overlap": (17, [64 * 40 + 17])}
+            "tc_segment_scan": (2, [64 * 40 + 17]), "tc_overlap": (17, [64 * 1024 + 17]),
+            "tc_ordered": (32, [300, 77, 0, 1000, 64, 1000, 5])}
 
 
 @pytest.mark.parametrize("case", list(TC_CASES) + ["simt_fp32"])
