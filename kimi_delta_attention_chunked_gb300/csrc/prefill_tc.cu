@@ -1933,7 +1933,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     std::memset(&tm_o, 0, sizeof(tm_o));
     // full output chunks leave the state pass by tensor stores when O is 16-byte aligned
     const int o_tma = a.T_total > 0 && a.O != nullptr && (reinterpret_cast<uintptr_t>(a.O) & 15) == 0;
-    if (o_tma && (e = make_output_map(&tm_o, a.O, a.H, a.T_total, narrow ? 32 : 64)) != cudaSuccess) return e;
+    // the segment scan's last pass (one CTA per segment, head and slice) over
+    // 32-column slices too when they fit one wave
+    const bool seg_narrow = use_seg && 4LL * sp.s_max * a.H <= n_sm;
+    if (o_tma && (e = make_output_map(&tm_o, a.O, a.H, a.T_total, (narrow || seg_narrow) ? 32 : 64)) != cudaSuccess)
+        return e;
     if (a.T_total > 0) {
         if ((e = make_input_map(&tm_q, a.q, 2, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
         if ((e = make_input_map(&tm_k, a.k, 2, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
@@ -1985,9 +1989,14 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
                                                                                        sp.s_max, a.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         // pass 3: every segment from its starting state, writing O
-        kda_tc_chain<64><<<dim3(NTILES * sp.s_max, a.H), K2_THREADS, chain_smem, a.stream>>>(
-            seg_info, 1, 0, 0, 0, INT32_MAX, blocks, seg_S, a.H, static_cast<bf16*>(a.O), nullptr, 0, nullptr, 0,
-            a.status, 0, nullptr, (int)ub, tm_o, o_tma, nullptr);
+        if (seg_narrow)
+            kda_tc_chain<32><<<dim3(ChainCfg<32>::NTL * sp.s_max, a.H), K2_THREADS, narrow_smem, a.stream>>>(
+                seg_info, 1, 0, 0, 0, INT32_MAX, blocks, seg_S, a.H, static_cast<bf16*>(a.O), nullptr, 0, nullptr, 0,
+                a.status, 0, nullptr, (int)ub, tm_o, o_tma, nullptr);
+        else
+            kda_tc_chain<64><<<dim3(NTILES * sp.s_max, a.H), K2_THREADS, chain_smem, a.stream>>>(
+                seg_info, 1, 0, 0, 0, INT32_MAX, blocks, seg_S, a.H, static_cast<bf16*>(a.O), nullptr, 0, nullptr, 0,
+                a.status, 0, nullptr, (int)ub, tm_o, o_tma, nullptr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         trace_mark(a.stream);
         return cudaSuccess;
