@@ -1929,15 +1929,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     e = cudaFuncSetAttribute(kda_tc_seg_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM);
     if (e != cudaSuccess) return e;
 
-    CUtensorMap tm_q, tm_k, tm_v, tm_g, tm_o;
+    CUtensorMap tm_q, tm_k, tm_v, tm_g, tm_o, tm_o32;
     std::memset(&tm_o, 0, sizeof(tm_o));
+    std::memset(&tm_o32, 0, sizeof(tm_o32));
     // full output chunks leave the state pass by tensor stores when O is 16-byte aligned
     const int o_tma = a.T_total > 0 && a.O != nullptr && (reinterpret_cast<uintptr_t>(a.O) & 15) == 0;
     // the segment scan's last pass (one CTA per segment, head and slice) over
-    // 32-column slices too when they fit one wave
+    // 32-column slices too when they fit one wave; likewise the last state-pass
+    // slice of an overlapped launch (nothing runs beside it)
     const bool seg_narrow = use_seg && 4LL * sp.s_max * a.H <= n_sm;
-    if (o_tma && (e = make_output_map(&tm_o, a.O, a.H, a.T_total, (narrow || seg_narrow) ? 32 : 64)) != cudaSuccess)
-        return e;
+    const bool last_narrow = n_slices > 1 && 4LL * a.n_seq * a.H <= n_sm;
+    if (o_tma && (e = make_output_map(&tm_o, a.O, a.H, a.T_total, 64)) != cudaSuccess) return e;
+    if (o_tma && (e = make_output_map(&tm_o32, a.O, a.H, a.T_total, 32)) != cudaSuccess) return e;
     if (a.T_total > 0) {
         if ((e = make_input_map(&tm_q, a.q, 2, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
         if ((e = make_input_map(&tm_k, a.k, 2, a.H, a.T_total, 128, false)) != cudaSuccess) return e;
@@ -1956,11 +1959,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
                                                   a.status, ctr, reserve);
         return cudaGetLastError();
     };
-    auto chain = [&](int c0, int c1, const float* s_in, float* s_out, cudaStream_t st) {
-        if (narrow)
+    auto chain = [&](int c0, int c1, const float* s_in, float* s_out, cudaStream_t st, bool nar) {
+        if (nar)
             kda_tc_chain<32><<<dim3(ChainCfg<32>::NTL * a.n_seq, a.H), K2_THREADS, narrow_smem, st>>>(
                 seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
-                a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub, tm_o, o_tma, nullptr);
+                a.ckpt_every, a.ckpt, a.ckpt_cap, a.status, 0, nullptr, (int)ub, tm_o32, o_tma, nullptr);
         else if (ordered)
             kda_tc_chain<64><<<dim3(NTILES * a.H, a.n_seq), K2_THREADS, chain_smem, st>>>(
                 seq_info, use_table, fixed_len, nch_per, c0, c1, blocks, s_in, a.H, static_cast<bf16*>(a.O), s_out,
@@ -1992,7 +1995,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         if (seg_narrow)
             kda_tc_chain<32><<<dim3(ChainCfg<32>::NTL * sp.s_max, a.H), K2_THREADS, narrow_smem, a.stream>>>(
                 seg_info, 1, 0, 0, 0, INT32_MAX, blocks, seg_S, a.H, static_cast<bf16*>(a.O), nullptr, 0, nullptr, 0,
-                a.status, 0, nullptr, (int)ub, tm_o, o_tma, nullptr);
+                a.status, 0, nullptr, (int)ub, tm_o32, o_tma, nullptr);
         else
             kda_tc_chain<64><<<dim3(NTILES * sp.s_max, a.H), K2_THREADS, chain_smem, a.stream>>>(
                 seg_info, 1, 0, 0, 0, INT32_MAX, blocks, seg_S, a.H, static_cast<bf16*>(a.O), nullptr, 0, nullptr, 0,
@@ -2005,7 +2008,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     if (n_slices == 1) {
         if ((e = prep(0, max_chunks, a.stream, nullptr, 0)) != cudaSuccess) return e;
         trace_mark(a.stream);
-        if ((e = chain(0, max_chunks, a.S0, a.S_final, a.stream)) != cudaSuccess) return e;
+        if ((e = chain(0, max_chunks, a.S0, a.S_final, a.stream, narrow)) != cudaSuccess) return e;
         trace_mark(a.stream);
         return cudaSuccess;
     }
@@ -2028,7 +2031,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
         if ((e = cudaEventRecord(r->ev[k], a.stream)) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(r->chain, r->ev[k], 0)) != cudaSuccess) return e;
         const bool last = (k == n_slices - 1);
-        if ((e = chain(c0, c1, k == 0 ? a.S0 : S_mid, last ? a.S_final : S_mid, r->chain)) != cudaSuccess)
+        if ((e = chain(c0, c1, k == 0 ? a.S0 : S_mid, last ? a.S_final : S_mid, r->chain, last && last_narrow)) !=
+            cudaSuccess)
             return e;
     }
     trace_mark(a.stream);                       // every prep slice enqueued
