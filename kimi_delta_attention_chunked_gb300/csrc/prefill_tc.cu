@@ -1664,7 +1664,7 @@ kda_tc_seg_scan(const int2* __restrict__ seq_seg, const float* __restrict__ A, c
 // sequence), then kSliceWords 8-byte words: the item counters of the chunk-prep
 // slices that run beside the state pass (and, once per device, the SM-id mask),
 // then the sequences' order by length (4 B a sequence, up to kMaxOrdered).
-constexpr int kSliceWords = 8;
+constexpr int kSliceWords = 16;
 constexpr int kMaxOrdered = 1024;            // the schedule kernel's block size
 size_t header_bytes(int n_seq, long long slots) {
     const size_t raw = 16u * (size_t)slots + 16u * (size_t)n_seq + 8u * kSliceWords +
@@ -1760,10 +1760,18 @@ cudaError_t make_output_map(CUtensorMap* m, void* base, int H, int T, int ntc) {
 // launched on a high-priority stream, but a prep slice launched first would
 // still take every SM; so the preps that run beside it draw their items from
 // a counter, and their CTAs that land on the SMs kept for the state pass (the
-// ones with the lowest ids) leave at once.  Per device: the state-pass
-// stream, a pool of events and the sorted SM ids, found on first use and kept
-// for the life of the process.
-constexpr int kMaxSlices = 8;
+// ones with the lowest ids) leave at once.  The whole call is bound by the
+// prep, which runs 1.7x slower per item beside the state pass than on the
+// whole GPU; so the first slice, prepared on the whole GPU, is made as large
+// as lets the prep of the rest (beside the state pass) still end about when
+// the state pass has caught up with it.  Per device: the state-pass stream, a
+// pool of events and the sorted SM ids, found on first use and kept for the
+// life of the process.
+constexpr int kMaxSlices = 16;
+// cycles of one chunk step of the state pass (64 columns) and of one (chunk,
+// head) item of the prep per SM (two CTAs share an SM), measured on GB300
+constexpr double kChainStepCycles = 3.5e3;
+constexpr double kPrepItemSmCycles = 15.7e3;
 static_assert(kMaxSlices <= kSliceWords, "one item counter per prep slice");
 constexpr int kSliceChunks = 16;                 // fewest chunks in a slice
 constexpr int kOverlapMinChunks = 1024;          // "long": chunks of the longest sequence
@@ -1900,7 +1908,21 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     const bool overlap = !use_seg && chain_ctas * 2 <= n_sm && max_chunks >= kOverlapMinChunks &&
                          !(use_table && a.max_chunks <= 0);
     const int n_slices = overlap ? std::min(kMaxSlices, max_chunks / kSliceChunks) : 1;
-    const int slice = n_slices > 1 ? (max_chunks + n_slices - 1) / n_slices : max_chunks;
+    // slice borders (chunk index within a sequence): slice 0 takes the share f
+    // for which the state pass's time over all chunks equals the prep's time
+    // over the rest on the SMs it leaves, f = 1 - t_chain / t_prep_beside
+    // (kept between one slice's and nine tenths); the others split the rest
+    auto slice_begin = [&](int k) -> int {
+        if (n_slices == 1) return k == 0 ? 0 : max_chunks;
+        const double t_chain = kChainStepCycles * max_chunks;
+        const double t_side = kPrepItemSmCycles * (double)a.total_chunks * a.H /
+                              (double)std::max<long long>(1, n_sm - chain_ctas);
+        const double f = std::min(0.9, std::max(1.0 / n_slices, 1.0 - t_chain / std::max(1.0, t_side)));
+        const int first = std::min(max_chunks - (n_slices - 1), std::max(1, (int)(f * max_chunks)));
+        if (k == 0) return 0;
+        const long long rest = max_chunks - first;
+        return first + (int)((rest * (k - 1) + (n_slices - 2)) / (n_slices - 1));
+    };
     // the state pass over 32-column slices when that still fits one wave of CTAs
     // (one per SM) and runs alone (no segment scan, no prep beside it)
     const bool narrow = !use_seg && n_slices == 1 && 4LL * a.n_seq * a.H <= n_sm;
@@ -2024,7 +2046,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a) {
     if ((e = cudaEventRecord(r->ev[n_slices], a.stream)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(r->chain, r->ev[n_slices], 0)) != cudaSuccess) return e;
     for (int k = 0; k < n_slices; ++k) {
-        const int c0 = k * slice, c1 = std::min(max_chunks, (k + 1) * slice);
+        const int c0 = slice_begin(k), c1 = k + 1 < n_slices ? slice_begin(k + 1) : max_chunks;
         // the first slice has the GPU to itself; the others run beside the state pass
         if ((e = prep(c0, c1 - c0, a.stream, k > 0 ? slice_ctr + k : nullptr, k > 0 ? reserve : 0)) != cudaSuccess)
             return e;
