@@ -1769,9 +1769,10 @@ cudaError_t make_output_map(CUtensorMap* m, void* base, int H, int T, int ntc) {
 // life of the process.
 constexpr int kMaxSlices = 16;
 // cycles of one chunk step of the state pass (64 columns) and of one (chunk,
-// head) item of the prep per SM (two CTAs share an SM), measured on GB300
-constexpr double kChainStepCycles = 3.5e3;
-constexpr double kPrepItemSmCycles = 15.7e3;
+// head) item of the prep per SM beside it (two CTAs share an SM), measured on
+// GB300 at 1M tokens x 32 heads
+constexpr double kChainStepCycles = 3.56e3;
+constexpr double kPrepItemSmCycles = 17.0e3;
 static_assert(kMaxSlices <= kSliceWords, "one item counter per prep slice");
 constexpr int kSliceChunks = 16;                 // fewest chunks in a slice
 constexpr int kOverlapMinChunks = 1024;          // "long": chunks of the longest sequence
