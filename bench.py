@@ -56,8 +56,8 @@ PARTS = ("prefill", "decode", "verify", "few", "varlen", "long", "e2e")
 # them the traffic reads null until a new capture replaces the entry.
 PROFILED_TRAFFIC = {
     "kda_tc_prep": {
-        "read_mb": 336.905728, "write_mb": 483.588864, "profile": "profiles/prefill_tc_T8192_H32_D128.md",
-        "sources": {"csrc/prefill_tc.cu": "7429edac0210b035", "csrc/umma.cuh": "351aa210ce878847",
+        "read_mb": 336.866304, "write_mb": 482.202112, "profile": "profiles/prefill_tc_T8192_H32_D128.md",
+        "sources": {"csrc/prefill_tc.cu": "e7098c99976f671c", "csrc/umma.cuh": "351aa210ce878847",
                     "csrc/common.cuh": "cef06e6ff0b08c46"}},
     "kda_decode_kernel": {
         "read_mb": 547.411712, "write_mb": 477.935616, "profile": "profiles/decode_N256_H32_D128.md",

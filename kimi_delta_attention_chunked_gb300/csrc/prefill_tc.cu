@@ -186,16 +186,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ void st_shared_u32(uint8_t* p, uint32_t x) { *reinterpret_cast<uint32_t*>(p) = x; }
-
-// (a, b) as a high / low pair of packed bf16x2 words: high = a, b truncated to
-// bf16, low = bf16 of the remainders (see split_pack8).
-__device__ __forceinline__ void split_pack2(float a, float b, uint32_t& hi, uint32_t& lo) {
-    const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
-    hi = __byte_perm(ua, ub, 0x7632);
-    lo = kda::pack_bf16x2(a - __uint_as_float(ua & 0xFFFF0000u), b - __uint_as_float(ub & 0xFFFF0000u));
-}
-
 // x = hi + lo with hi = x truncated to bf16 and lo = bf16(x - hi): the pair
 // carries ~16 significant bits (|x - hi| < 2^-7 |x|, and lo is rounded to
 // nearest), enough to keep an MMA operand's rounding out of the error budget.
@@ -290,17 +280,27 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
                       kda::pack_bf16x2(f[4], f[5]), kda::pack_bf16x2(f[6], f[7]));
 }
 
-// Eight values as f16 (nearest even) instead of bf16: three more mantissa bits
-// for a Gram operand whose values the chunk's decay range keeps inside f16.
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ uint4 pack8g(const float* f, bool f16) {
-    if (f16)
-        return make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
-                          pack_f16x2(f[6], f[7]));
-    return pack8(f);
+// Eight values as packed bf16, or as f16 (nearest even) when f16 != 0: three
+// more mantissa bits for a Gram operand whose values the chunk's decay range
+// keeps inside f16.  The type is a run-time choice: the bf16 conversions are
+// overwritten by predicated f16 ones, so that one copy of the operand code
+// serves both types without a branch (two copies, one per type, made the
+// kernel's code a quarter larger and every phase slower).
+__device__ __forceinline__ uint4 pack8g(const float* f, uint32_t f16) {
+    uint4 r;
+    asm("{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %12, 0;\n\t"
+        "cvt.rn.bf16x2.f32 %0, %5, %4;\n\t"
+        "cvt.rn.bf16x2.f32 %1, %7, %6;\n\t"
+        "cvt.rn.bf16x2.f32 %2, %9, %8;\n\t"
+        "cvt.rn.bf16x2.f32 %3, %11, %10;\n\t"
+        "@p cvt.rn.f16x2.f32 %0, %5, %4;\n\t"
+        "@p cvt.rn.f16x2.f32 %1, %7, %6;\n\t"
+        "@p cvt.rn.f16x2.f32 %2, %9, %8;\n\t"
+        "@p cvt.rn.f16x2.f32 %3, %11, %10;\n\t}"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]), "r"(f16));
+    return r;
 }
 // Largest log-decay across one 16-row block (over every channel) for which
 // the Gram operands go to the tensor cores as f16: the column factors are at
@@ -365,18 +365,20 @@ kda_tc_schedule(const int32_t* __restrict__ cu, int n_seq, int T_total, int slot
 }
 
 // ============================================================== prep (a1-a3)
-// One warp per row block B (0..3): TMEM lanes 32 B .. 32 B + 31 hold the
-// block's q~ rows (lanes 0..15) and k^ rows (lanes 16..31) against the first
-// 16 (B + 1) tokens, at columns 8 B (B + 1) ...  Writes the M_qk rows
-// (diagonal included) as high / low bf16 operand parts and the L rows (beta
-// folded in, strict) as fp32.  One rolled copy for all four blocks.
-__device__ __forceinline__ void gram_epilogue(uint32_t tmem, int B, int lane, uint8_t* mh, uint8_t* ml, float* LS) {
+// Two warps per row block B (0..3), one per 32-column half: TMEM lanes
+// 32 B .. 32 B + 31 hold the block's q~ rows (lanes 0..15) and k^ rows (lanes
+// 16..31) against the first 16 (B + 1) tokens, at columns 8 B (B + 1) ...
+// Writes the M_qk rows (diagonal included) as high / low bf16 operand parts and
+// the L rows (beta folded in, strict) as fp32, both zero past the row's last
+// kept column.  One rolled copy for all four blocks.
+__device__ __forceinline__ void gram_epilogue(uint32_t tmem, int B, int half, int lane, uint8_t* mh, uint8_t* ml,
+                                              float* LS) {
     const int N = 16 * (B + 1), OFF = 8 * B * (B + 1);
     const bool is_m = lane < 16;
     const int r = 16 * B + (lane & 15);
     const int lim = is_m ? r + 1 : r;             // columns t < lim are kept (lim <= N)
 #pragma unroll 1
-    for (int c = 0; c < 64; c += 16) {
+    for (int c = 32 * half; c < 32 * half + 32; c += 16) {
         float v[16];
         if (c < N) {                              // warp-uniform
             kda::tmem_ld16(tmem + ((uint32_t)(32 * B) << 16) + OFF + c, v);
@@ -695,10 +697,8 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
             for (int j = 0; j < 8; ++j) e[i][j] = __expf(e[i][j] - fb[j]);
         }
-        // the row operands and the Gram column tiles, once per operand type (a
-        // uniform branch over two copies, so that no store converts twice)
-        auto operands = [&](auto f16_tag) {
-            constexpr bool F16 = decltype(f16_tag)::value;
+        // the row operands and the Gram column tiles
+        auto operands = [&](uint32_t F16) {
     #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = r0 + i;
@@ -783,8 +783,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
             }
         };
-        if (gram_f16) operands(std::true_type{});
-        else operands(std::false_type{});
+        operands(gram_f16 ? 1u : 0u);
         kda::fence_proxy_async_all();              // shared operands and the Q_decay rows read back later
         kda::tc_fence_before();
         __syncthreads();
@@ -809,7 +808,7 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
         float* LS = reinterpret_cast<float*>(sm + K1_LS);
         float* IS = reinterpret_cast<float*>(sm + K1_IS);
-        if (w < 4) gram_epilogue(tmem, w, lane, sm + K1_MH, sm + K1_ML, LS);
+        gram_epilogue(tmem, w & 3, w >> 2, lane, sm + K1_MH, sm + K1_ML, LS);
         kda::tc_fence_before();
         __syncthreads();
 
@@ -1002,25 +1001,44 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 }
             }
         }
-        // TMEM lanes 0..63 hold [W | U0], lanes 64..127 hold [M_qk W | O0] (columns 0..127 | 128..255)
-        const int quad = w & 3, r = 32 * (quad & 1) + lane;
-        const uint32_t t_row = tmem + ((uint32_t)(32 * quad) << 16) + (w >= 4 ? 128u : 0u);
-        if (w == 0 || w == 1) {                    // W rows -> rows 64..127 of [Q'; W]
+        // TMEM lanes 0..63 hold [W | U0], lanes 64..127 hold [M_qk W | O0] (columns
+        // 0..127 | 128..255).  The two warps of a TMEM lane quarter (w and w + 4)
+        // each take two of the four 32-column blocks of both halves: first the fp32
+        // U0 / O0 rows, straight to the workspace (512 contiguous bytes a warp), then
+        // the W rows or, once Q_decay is back, the Q' rows of the [Q'; W] image.
+        const int quad = w & 3, r = 32 * (quad & 1) + lane, cb0 = 2 * (w >> 2);
+        const uint32_t t_lane = tmem + ((uint32_t)(32 * quad) << 16);
+        {
+            const uint32_t part = quad < 2 ? 0u : TILE_F32;    // U0 (lanes 0..63) or O0 (lanes 64..127)
 #pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
+            for (int cb = cb0; cb < cb0 + 2; ++cb) {
                 float x[32];
-                kda::tmem_ld32(t_row + 32 * cb, x);
+                kda::tmem_ld32(t_lane + 128 + 32 * cb, x);
+                kda::tmem_wait_ld();
+                const int tile = (32 * cb) / NT, c0 = (32 * cb) % NT;
+                uint8_t* dst = blk + WS_UO + 2 * TILE_F32 * tile + part;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<float4*>(dst + uo_off(r, c0 + 4 * u)) =
+                        make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+            }
+        }
+        if (quad < 2) {                            // W rows -> rows 64..127 of [Q'; W]
+#pragma unroll 1
+            for (int cb = cb0; cb < cb0 + 2; ++cb) {
+                float x[32];
+                kda::tmem_ld32(t_lane + 32 * cb, x);
                 kda::tmem_wait_ld();
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     *reinterpret_cast<uint4*>(sm + K1_OUT_A1 + kda::sw128(64 + r, 32 * cb + 8 * u, 128)) = pack8(x + 8 * u);
             }
-        } else if (w == 2 || w == 3) {             // Q' = Q_decay - M_qk W -> rows 0..63 of [Q'; W]
+        } else {                                   // Q' = Q_decay - M_qk W -> rows 0..63 of [Q'; W]
             wait(bar_q, n_done & 1);
 #pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
+            for (int cb = cb0; cb < cb0 + 2; ++cb) {
                 float x[32];
-                kda::tmem_ld32(t_row + 32 * cb, x);
+                kda::tmem_ld32(t_lane + 32 * cb, x);
                 kda::tmem_wait_ld();
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -1035,20 +1053,6 @@ kda_tc_prep(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                     }
                     *qp = pack8(x + 8 * u);
                 }
-            }
-        } else {                                   // U0 (warps 4, 5) or O0 (warps 6, 7) rows, fp32, per d_v slice,
-            const uint32_t part = w < 6 ? 0u : TILE_F32;   // straight to the workspace (512 contiguous bytes a warp)
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                float x[32];
-                kda::tmem_ld32(t_row + 32 * cb, x);
-                kda::tmem_wait_ld();
-                const int tile = (32 * cb) / NT, c0 = (32 * cb) % NT;
-                uint8_t* dst = blk + WS_UO + 2 * TILE_F32 * tile + part;
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<float4*>(dst + uo_off(r, c0 + 4 * u)) =
-                        make_float4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
             }
         }
         kda::fence_proxy_async_smem();
