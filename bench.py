@@ -226,19 +226,26 @@ def time_prefill(kda, d, steps, warmup, stream, dev):
         for _ in range(warmup):
             call()
         torch.cuda.synchronize()
-        # per-step events: [start, every chunk-prep launch done, state pass joined]
+        # the timed steps: the calls alone between two events
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(steps):
+            call()
+        end.record(stream)
+        torch.cuda.synchronize()
+        # then as many calls again with the library's trace events, per call
+        # [start, every chunk-prep launch done, state pass joined], for the
+        # split between the two kernels: an event between two kernels costs
+        # each call a few microseconds, so these calls are not the timed ones
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
         for row in evs:
             for e in row:
                 e.record(stream)
         torch.cuda.synchronize()
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(stream)
         for i in range(steps):
             kda.kda_set_trace_events(evs[i])
             call()
         kda.kda_set_trace_events(None)
-        end.record(stream)
         torch.cuda.synchronize()
     total_ms = start.elapsed_time(end)
     prep_ms = [r[0].elapsed_time(r[1]) for r in evs]
