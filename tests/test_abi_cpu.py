@@ -169,6 +169,30 @@ def test_decode_argument_checks(lib):
     assert call(dt=3) == E.KDA_ERR_INVALID_ARG
 
 
+def test_verify_argument_checks(lib):
+    """kda_decode_multi refuses before any launch: more tokens than the kernel
+    stages (16), negative sizes, unsupported head dims, null or aliased
+    pointers, an unaligned state; N = 0 or K = 0 is a no-op."""
+    P = ctypes.c_void_p
+    f = P(0x1000)
+    S = P(0x4000)
+    o = P(0x5000)
+    E = _lib
+    call = lambda **kw: lib.kda_decode_multi(kw.get("q", f), f, f, f, f, kw.get("S", S), None, kw.get("N", 4),
+                                             kw.get("K", 4), kw.get("H", 2), kw.get("dk", 64), kw.get("dv", 64),
+                                             kw.get("dt", E.KDA_BF16), kw.get("o", o), None)
+    assert call(K=17) == E.KDA_ERR_UNSUPPORTED
+    assert call(K=-1) == E.KDA_ERR_INVALID_ARG
+    assert call(N=-1) == E.KDA_ERR_INVALID_ARG
+    assert call(K=0) == E.KDA_OK
+    assert call(N=0) == E.KDA_OK
+    assert call(dk=96) == E.KDA_ERR_UNSUPPORTED
+    assert call(q=None) == E.KDA_ERR_INVALID_ARG
+    assert call(o=f) == E.KDA_ERR_INVALID_ARG            # o aliases an input
+    assert call(S=P(0x4004)) == E.KDA_ERR_INVALID_ARG    # state not 16-byte aligned
+    assert call(dt=3) == E.KDA_ERR_INVALID_ARG
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(_lib, "_lib", None)

@@ -99,11 +99,12 @@ def test_decode_matches_prefill_of_same_tokens():
     assert rel_err(S, Sf.double().cpu().numpy()) < 1e-5
 
 
-@pytest.mark.parametrize("K", [1, 3, 8])
+@pytest.mark.parametrize("K", [1, 3, 8, 16])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_verify_multi_token(K, dtype):
-    """K proposed tokens per sequence: every output vs the oracle; the state is
-    committed after commit_len[n] tokens (0 .. K, drawn per sequence)."""
+    """K proposed tokens per sequence (16 = the most the kernel stages): every
+    output vs the oracle; the state is committed after commit_len[n] tokens
+    (0 .. K, drawn per sequence)."""
     dev = need_gpu()
     N, H, D = 16, 4, 128
     w = inputs.Workload("verify", "prefill", H=H, dk=D, dv=D, dtype=dtype, chunk=64, T=K, B=N, s0_std=0.02)
@@ -129,6 +130,28 @@ def test_verify_multi_token(K, dtype):
                                    S0=d["S0"][n:n + 1])
             ref = Sf[0]
         assert rel_err(S[n], ref) <= tol_for(dtype), n
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 32), (32, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_verify_shapes(dk, dv, dtype):
+    """The verify kernel at the other head dims (one instantiation each): outputs
+    and the state after all K tokens vs the oracle."""
+    dev = need_gpu()
+    N, K, H = 8, 5, 2
+    w = inputs.Workload("verify4", "prefill", H=H, dk=dk, dv=dv, dtype=dtype, chunk=64, T=K, B=N, s0_std=0.02)
+    d = inputs.make_prefill(w, device=dev, seed=dk + dv, lengths=[K] * N)
+    q, k, g = (d[n].view(N, K, H, dk).contiguous() for n in ("q", "k", "log_alpha"))
+    v = d["v"].view(N, K, H, dv).contiguous()
+    b = d["beta"].view(N, K, H).contiguous()
+    S = d["S0"].clone()
+    o = kda.kda_decode_multi(q, k, v, g, b, S)
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_device_status() == 0
+    O_ref, S_ref = oracle.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], cu_seqlens=d["cu_seqlens_host"],
+                                  S0=d["S0"])
+    assert rel_err(o.view(N * K, H, dv), O_ref) <= tol_for(dtype)
+    assert rel_err(S, S_ref) <= tol_for(dtype)
 
 
 def test_verify_outputs_only_then_commit():
