@@ -119,6 +119,22 @@ def test_tc_path_equal_lengths_without_cu_seqlens():
     assert rel_err(Sf, Sf_ref) <= 5e-3
 
 
+@pytest.mark.parametrize("dtype,dim,chunk", [(torch.bfloat16, 128, 64), (torch.float32, 32, 16)],
+                         ids=["tensor_cores", "cuda_cores"])
+def test_all_sequences_empty(dtype, dim, chunk):
+    """Every sequence empty (T_total = 0): no output rows, and each S_final is
+    its S0 bit for bit (no chunk touches the state)."""
+    dev = need_gpu()
+    w = inputs.Workload("empty", "prefill", H=4, dk=dim, dv=dim, dtype=dtype, chunk=chunk, s0_std=0.02)
+    d = inputs.make_prefill(w, device=dev, seed=3, lengths=[0, 0, 0])
+    O, Sf = kda.kda_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=d["S0"],
+                            cu_seqlens=d["cu_seqlens"], cu_seqlens_host=d["cu_seqlens_host"], chunk=chunk)
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_device_status() == 0
+    assert O.shape == (0, 4, dim)
+    assert torch.equal(Sf, d["S0"])
+
+
 def test_tc_state_aliasing():
     dev = need_gpu()
     w = inputs.Workload("tc", "prefill", s0_std=0.02, **TC)
